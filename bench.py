@@ -1,0 +1,407 @@
+#!/usr/bin/env python
+"""MoE layer forward benchmark on GB300.
+
+One step = one moe_forward (router, dispatch, grouped expert FFN, combine) over
+one batch of n synthetic tokens with the layer's weights resident in HBM.
+Default workload: the Mixtral-shaped layer (n=4096, d=4096, d_ff=14336, E=8,
+top-2, SwiGLU, bf16).  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--n N]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on a bounded sample
+
+Multi-GPU (torchrun, one rank per GPU): each rank runs its own batch with its
+own copy of the weights (data parallel, no collective on the data path); the
+reported value is all ranks' tokens / max-over-ranks time ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import moe_synth  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--config", default="mixtral_bf16", choices=sorted(moe_synth.CONFIGS))
+    p.add_argument("--n", type=int, default=None, help="override the token count")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample", type=int, default=None,
+                   help="tokens in the oracle's timed sample")
+    return p.parse_args(argv)
+
+
+# --------------------------------------------------------------- distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over all ranks (the job's time is its slowest rank's)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        if device is not None and device.type == "cuda":
+            torch.distributed.barrier(device_ids=[device.index])
+        else:
+            torch.distributed.barrier()
+
+
+def job_throughput(units_per_rank: int, world: int, seconds: float) -> float:
+    """Whole-job units/s: all ranks' units over the (max-over-ranks) time."""
+    return units_per_rank * world / seconds
+
+
+# -------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def __enter__(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.f is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ roofline
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dominant_kernel(cfg):
+    """(stage name, bound, algorithmic units per launch, unit) of the dominant kernel.
+
+    Tensor-bound workloads: the up-projection grouped GEMM (W1 and W3, 2/3 of the
+    expert FLOPs with SwiGLU), FLOPs = 2 * (n*k) * d * d_ff * (2 for SwiGLU, else 1).
+    """
+    mats = 2 if cfg.act == "swiglu" else 1
+    flops = 2 * cfg.n * cfg.k * cfg.d * cfg.d_ff * mats
+    return "ffn_up", "tensor", flops, "TFLOP/s"
+
+
+# -------------------------------------------------------------- CPU baseline
+
+def host_copy(inputs_dev):
+    return {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inputs_dev.items()}
+
+
+def oracle_sample(cfg, inputs_host, tokens: int, seed: int):
+    """A bounded sample of the workload for the fp64 oracle: `tokens` seeded rows
+    of x with the full layer's weights."""
+    g = torch.Generator().manual_seed(seed)
+    rows = torch.sort(torch.randperm(cfg.n, generator=g)[:tokens]).values
+    sub = dict(inputs_host)
+    sub["x"] = inputs_host["x"][rows]
+    return cfg.scaled(n=int(rows.numel())), sub
+
+
+def time_oracle_step(scfg, sub):
+    from oracle import moe_oracle as O   # the CPU baseline leg is the oracle as it stands
+    t0 = time.perf_counter()
+    O.forward(scfg, sub)
+    return time.perf_counter() - t0
+
+
+def default_cpu_sample(cfg):
+    return {"tiny_switch_fp32": 256, "mixtral_bf16": 512, "gptoss_decode_mxfp4": cfg.n,
+            "gptoss_prefill_zipf_mxfp4": 256, "finegrained_shared_bf16": 64}.get(cfg.name, 64)
+
+
+# ----------------------------------------------------------------- our arm
+
+def workload_name(cfg):
+    return moe_synth.describe(cfg)
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    from mixture_experts_layer_moe_gb300 import build as _b
+    if rank == 0 or world == 1:
+        _b.build()
+    barrier(device)
+    from mixture_experts_layer_moe_gb300 import moe
+
+    cfg = moe_synth.CONFIGS[args.config]
+    if args.n:
+        cfg = cfg.scaled(n=args.n)
+    # each rank draws its own token batch; the weights are the same layer
+    inputs = moe_synth.make_inputs(cfg, seed=args.seed, device=device)
+    if rank:
+        g = torch.Generator(device=device).manual_seed(args.seed + 1000 * rank)
+        x = torch.randn(inputs["x"].shape, generator=g, device=device, dtype=torch.float32)
+        inputs["x"] = (x * cfg.x_std).to(inputs["x"].dtype)
+    w = moe.make_weights(inputs)
+    ws = moe.alloc_workspace(cfg, device)
+    y = torch.empty(cfg.n, cfg.d, dtype=inputs["x"].dtype, device=device)
+    stream = torch.cuda.current_stream(device)
+    weight_bytes = cfg.E * moe_synth.weight_bytes_per_expert(cfg)
+
+    stage_names = moe.STAGES
+    dom_stage, bound, dom_units, dom_unit = dominant_kernel(cfg)
+    dom_idx, dom_next = stage_names.index(dom_stage), stage_names.index(dom_stage) + 1
+    launches = {"n": 0}
+
+    def step(events=None):
+        def hook(stage, kernels):
+            if events is not None:
+                events[stage].record(stream)
+            if stage == len(stage_names) - 1:
+                launches["n"] = kernels
+        moe.moe_forward_staged(cfg, inputs["x"], w, y, ws, hook, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    st, detail = moe.moe_status_check(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {moe.status_string(st)} ({detail})")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in stage_names] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    with ClockSampler(device.index) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            step(ev[i])
+        stop.record(stream)
+        torch.cuda.synchronize(device)
+    barrier(device)
+    elapsed = start.elapsed_time(stop) / 1e3
+    t_job = max_over_ranks(elapsed, device)
+    kernels_per_step = launches["n"]
+
+    # per-stage durations (CUDA events on the launching stream, inside the timed region)
+    present = [s for s in range(len(stage_names) - 1)
+               if s != stage_names.index("shared") or cfg.d_ff_shared]
+    stage_ms = {}
+    for s in present:
+        nxt = next((t for t in range(s + 1, len(stage_names))
+                    if t in present or t == len(stage_names) - 1))
+        stage_ms[stage_names[s]] = statistics.mean(
+            ev[i][s].elapsed_time(ev[i][nxt]) for i in range(args.steps))
+    dom_ms = stage_ms[dom_stage]
+
+    # end to end: pinned host x in, pinned host y out, every step
+    x_host = inputs["x"].cpu().pin_memory()
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    x_dev = torch.empty_like(inputs["x"])
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_forward(cfg, x_dev, w, y, ws, stream)
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_forward(cfg, x_dev, w, y, ws, stream)
+        y_host.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, device)
+    st, detail = moe.moe_status_check(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {moe.status_string(st)} ({detail})")
+
+    peaks, peak_src = load_peaks()
+    if bound == "tensor":
+        peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        achieved = dom_units / (dom_ms / 1e3) / 1e12
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = dom_units / (dom_ms / 1e3) / 1e9
+
+    out = {
+        "metric": "MoE-layer tokens/s",
+        "value": job_throughput(cfg.n * args.steps, world, t_job),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_job / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp32" if cfg.act_dtype == "f32" else "bf16",
+        "data": "synthetic (seeded normal x and weights; MXFP4 codes/scales uniform)",
+        "config": {
+            "workload": workload_name(cfg),
+            "tokens_per_rank": cfg.n,
+            "parallelism": f"dp{world} (independent token batches, replicated weights)",
+            "l2": (f"inputs larger than L2: {weight_bytes / 1e9:.2f} GB of expert weights per step"
+                   if weight_bytes > L2_BYTES else "L2 not flushed: working set below L2"),
+        },
+        "e2e": {"value": job_throughput(cfg.n * args.steps, world, t_e2e), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+        "gpu_launches": kernels_per_step * args.steps,
+        "roofline": {"kernel": dom_stage, "bound": bound, "achieved": achieved, "peak": peak,
+                     "unit": dom_unit, "frac": achieved / peak,
+                     "peak_source": f"{peak_src} ({'bf16 sustained' if bound == 'tensor' else 'hbm copy'})",
+                     "traffic": None},
+        "stages_ms": stage_ms,
+        "clocks": clocks.summary(),
+    }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tokens = args.cpu_sample or default_cpu_sample(cfg)
+        del x_host, y_host, x_dev
+        scfg, sub = oracle_sample(cfg, host_copy(inputs), tokens, args.seed)
+        secs = time_oracle_step(scfg, sub)
+        out["cpu_baseline"] = {"value": scfg.n / secs, "unit": "tokens/s",
+                               "cores": torch.get_num_threads(), "kind": "oracle",
+                               "sample": f"{scfg.n} of {cfg.n} token rows, full layer weights, "
+                                         f"fp64 oracle, {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    cfg = moe_synth.CONFIGS[args.config]
+    if args.n:
+        cfg = cfg.scaled(n=args.n)
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    inputs = host_copy(moe_synth.make_inputs(cfg, seed=args.seed, device=device))
+    tokens = args.cpu_sample or max(1, default_cpu_sample(cfg) // 4)
+    times = []
+    scfg = None
+    for i in range(args.warmup + args.steps):
+        scfg, sub = oracle_sample(cfg, inputs, tokens, args.seed + i)
+        secs = time_oracle_step(scfg, sub)
+        if i >= args.warmup:
+            times.append(secs)
+    total = sum(times)
+    value = scfg.n * len(times) / total
+    out = {
+        "impl": "reference",
+        "metric": "MoE-layer tokens/s",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total / len(times) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (same generator and seed as the GPU arm)",
+        "config": {"workload": workload_name(cfg), "tokens_per_rank": cfg.n},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": torch.get_num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{scfg.n} of {cfg.n} token rows per step, full layer weights"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,115 @@
+// Combine: gate scaling fused with the un-permute back to token order.
+//
+// "How Mixture of Experts Scales Model Parameters", section "The forward
+// pass: dispatch, then combine": each expert's output rows are multiplied by
+// the probability the token was routed with, and combine puts the weighted
+// rows back in the tokens' original order.  With top-K ("Top-K: several
+// experts, added up by weight") the K weighted outputs of a token are added.
+//   y[t] = sum_{j<k} g[t][j] * y_perm[inv_perm[t*k + j]]  (+ y_shared[t])
+// fp32 accumulation in slot order, then one rounding to the output type.
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+template <typename T>
+struct Vec16 {
+  static constexpr int N = 16 / sizeof(T);
+};
+
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4 &u, float *f);
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4 &u, float *f) {
+  f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+template <>
+__device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4 &u, float *f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack16(const float *f);
+template <>
+__device__ __forceinline__ uint4 pack16<float>(const float *f) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                    __float_as_uint(f[3]));
+}
+template <>
+__device__ __forceinline__ uint4 pack16<__nv_bfloat16>(const float *f) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t *>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// One CTA per token row block; thread handles 16-byte vectors of the row.
+template <typename T>
+__global__ void __launch_bounds__(256)
+combine_kernel(const uint4 *__restrict__ y_perm, const int32_t *__restrict__ inv_perm,
+               const float *__restrict__ gates, const uint4 *__restrict__ y_shared,
+               uint4 *__restrict__ y, int n, int k, int vec_per_row, int *status) {
+  constexpr int V = Vec16<T>::N;
+  const int P = n * k;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)n * vec_per_row;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / vec_per_row);
+    const int v = (int)(i - (int64_t)t * vec_per_row);
+    float acc[V];
+#pragma unroll
+    for (int c = 0; c < V; ++c) acc[c] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int q = inv_perm[(int64_t)t * k + j];
+      if (q < 0 || q >= P) {
+        if (v == 0) set_status(status, MOE_ERR_BAD_INDEX, t * k + j);
+        continue;
+      }
+      const float g = gates[(int64_t)t * k + j];
+      float f[V];
+      unpack16<T>(y_perm[(int64_t)q * vec_per_row + v], f);
+#pragma unroll
+      for (int c = 0; c < V; ++c) acc[c] = fmaf(g, f[c], acc[c]);
+    }
+    if (y_shared) {
+      float f[V];
+      unpack16<T>(y_shared[i], f);
+#pragma unroll
+      for (int c = 0; c < V; ++c) acc[c] += f[c];
+    }
+    y[i] = pack16<T>(acc);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(int act_dtype, const void *y_perm, const int32_t *inv_perm,
+                           const float *gates, const void *y_shared, void *y, int n, int k,
+                           int d, int *status, cudaStream_t s) {
+  const int esz = act_dtype == MOE_F32 ? 4 : 2;
+  const int vpr = d * esz / 16;
+  const int64_t total = (int64_t)n * vpr;
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  if (act_dtype == MOE_F32)
+    combine_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
+        (const uint4 *)y_perm, inv_perm, gates, (const uint4 *)y_shared, (uint4 *)y, n, k, vpr,
+        status);
+  else
+    combine_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
+        (const uint4 *)y_perm, inv_perm, gates, (const uint4 *)y_shared, (uint4 *)y, n, k, vpr,
+        status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

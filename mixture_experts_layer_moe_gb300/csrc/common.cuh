@@ -1,0 +1,68 @@
+// Internal helpers shared by the kernels of the MoE library (device side).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- status word
+// The first 256 bytes of every workspace: int32 status, int32 detail, spare.
+struct DevStatus {
+  int status;
+  int detail;
+};
+
+__device__ __forceinline__ void set_status(int *st, int code, int detail) {
+  if (st == nullptr) return;
+  if (atomicCAS(st, 0, code) == 0) {
+    atomicExch(st + 1, detail);
+  }
+}
+
+__device__ __forceinline__ bool status_failed(const int *st) {
+  return st != nullptr && *reinterpret_cast<const volatile int *>(st) != 0;
+}
+
+// ------------------------------------------------------------- element types
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static __device__ __forceinline__ float load(const float *p) { return *p; }
+  static __device__ __forceinline__ float to_f(float v) { return v; }
+  static __device__ __forceinline__ float from_f(float v) { return v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float load(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+// ------------------------------------------------------------------- MXFP4
+// E2M1 element (OCP MX v1.0): sign bit 3, exponent bits 2..1 (bias 1),
+// mantissa bit 0; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+__device__ __forceinline__ float e2m1_to_float(uint32_t code) {
+  const uint32_t e = (code >> 1) & 3u;
+  const uint32_t m = code & 1u;
+  // normal: 2^(e-1) * (1 + m/2) -> fp32 bits: exponent e-1+127, mantissa m<<22
+  // subnormal (e == 0): m * 0.5
+  float mag = (e == 0) ? (m ? 0.5f : 0.0f) : __uint_as_float(((e + 126u) << 23) | (m << 22));
+  return (code & 8u) ? -mag : mag;
+}
+
+// E8M0 scale: 2^(s-127); s = 0 is the fp32 subnormal 2^-127; s = 255 is NaN.
+__device__ __forceinline__ float e8m0_to_float(uint32_t s) {
+  if (s == 0u) return __uint_as_float(0x00400000u);
+  if (s == 255u) return __uint_as_float(0x7fc00000u);
+  return __uint_as_float(s << 23);
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+}  // namespace moe

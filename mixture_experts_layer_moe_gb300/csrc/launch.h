@@ -1,0 +1,52 @@
+// Host-side launchers of the MoE kernels (internal; the public ABI is moe.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Router: logits (fp32 [n][E] scratch) -> softmax -> top-k -> gates.
+cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, const float *bias,
+                         float *logits, int32_t *topk_idx, float *topk_gate, float *probs,
+                         int *status, cudaStream_t s);
+
+// Stable counting sort of P pairs by expert (one CTA).
+cudaError_t launch_dispatch(int P, int E, const int32_t *topk_idx, int32_t *counts,
+                            int32_t *offsets, int32_t *perm, int32_t *inv_perm, int *status,
+                            cudaStream_t s);
+
+// x_perm[q] = x[perm[q] / k]; rows of row_bytes (multiple of 16).
+cudaError_t launch_gather(const void *x, const int32_t *perm, int P, int k, int n,
+                          int64_t row_bytes, void *x_perm, int *status, cudaStream_t s);
+
+// y[t] = sum_j g[t][j] * y_perm[inv[t*k+j]] (+ y_shared[t]).
+cudaError_t launch_combine(int act_dtype, const void *y_perm, const int32_t *inv_perm,
+                           const float *gates, const void *y_shared, void *y, int n, int k,
+                           int d, int *status, cudaStream_t s);
+
+// One grouped GEMM stage on CUDA cores (fp32 accumulate):
+//   out[q][j] = epi( sum_i A[q][i] * B_e[j][i] )  for q in segment e.
+// epi: 0 = none, 1 = relu, 2 = swiglu (B3 gives the linear branch).
+// offsets == nullptr means one segment [0, rows) using expert 0.
+struct GemmStage {
+  int a_dtype;          // MOE_F32 / MOE_BF16
+  int b_dtype;          // MOE_F32 / MOE_BF16 / MOE_MXFP4
+  int out_dtype;        // MOE_F32 / MOE_BF16
+  int epi;
+  const void *A;
+  const int32_t *offsets;
+  int num_experts;
+  int rows;             // total rows of A (P)
+  int N, K;
+  const void *B;        // [E][N][K] (or codes [E][N][K/2])
+  const uint8_t *SB;    // scales [E][N][K/32]
+  const void *B3;
+  const uint8_t *SB3;
+  void *out;            // [rows][N]
+};
+cudaError_t launch_gemm_simt(const GemmStage &g, int *status, cudaStream_t s);
+
+}  // namespace moe

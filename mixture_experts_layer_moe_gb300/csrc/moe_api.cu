@@ -1,0 +1,378 @@
+// The C ABI (include/moe.h): argument validation, workspace layout, and the
+// launch sequence of the MoE layer forward pass.
+#include <stdint.h>
+#include <string.h>
+
+#include "launch.h"
+#include "moe.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool ok_ptr(const void *p) { return p != nullptr && aligned(p, 16); }
+cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+int act_size(const moe_config &c) { return c.act_dtype == MOE_F32 ? 4 : 2; }
+int h_size(const moe_config &c) { return c.act_dtype == MOE_F32 ? 4 : 2; }
+
+moe_status check_config(const moe_config *c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->n < 1 || c->d < 1 || c->d_ff < 1) return MOE_ERR_INVALID_ARG;
+  if (c->n_experts < 1 || c->n_experts > 256) return MOE_ERR_INVALID_ARG;
+  if (c->top_k < 1 || c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
+  if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->weight_dtype != MOE_F32 && c->weight_dtype != MOE_BF16 && c->weight_dtype != MOE_MXFP4)
+    return MOE_ERR_INVALID_ARG;
+  if (c->gate != MOE_GATE_TOP_PROB && c->gate != MOE_GATE_RENORM) return MOE_ERR_INVALID_ARG;
+  if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (c->d_ff_shared < 0) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)c->n * c->top_k > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+  // fp32 activations go with fp32 weights; bf16 activations with bf16 or MXFP4
+  if (c->act_dtype == MOE_F32 && c->weight_dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
+  if (c->act_dtype == MOE_BF16 && c->weight_dtype == MOE_F32) return MOE_ERR_UNSUPPORTED;
+  // rows must be whole 16-byte vectors
+  const int vec = c->act_dtype == MOE_F32 ? 4 : 8;
+  if (c->d % vec || c->d_ff % vec || c->d_ff_shared % vec) return MOE_ERR_UNSUPPORTED;
+  if (c->weight_dtype == MOE_MXFP4 && (c->d % 32 || c->d_ff % 32)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status check_router_weights(const moe_config &c, const moe_weights *w) {
+  if (w == nullptr || !ok_ptr(w->Wg)) return MOE_ERR_INVALID_ARG;
+  if (w->router_bias != nullptr && !aligned(w->router_bias, 4)) return MOE_ERR_INVALID_ARG;
+  (void)c;
+  return MOE_OK;
+}
+
+moe_status check_expert_weights(const moe_config &c, const moe_weights *w) {
+  if (w == nullptr || !ok_ptr(w->W1) || !ok_ptr(w->W2)) return MOE_ERR_INVALID_ARG;
+  const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  if (swiglu != (w->W3 != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (swiglu && !ok_ptr(w->W3)) return MOE_ERR_INVALID_ARG;
+  if (c.weight_dtype == MOE_MXFP4) {
+    if (w->S1 == nullptr || w->S2 == nullptr) return MOE_ERR_INVALID_ARG;
+    if (swiglu != (w->S3 != nullptr)) return MOE_ERR_INVALID_ARG;
+  } else if (w->S1 || w->S2 || w->S3) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (c.d_ff_shared > 0) {
+    if (!ok_ptr(w->Ws1) || !ok_ptr(w->Ws3) || !ok_ptr(w->Ws2)) return MOE_ERR_INVALID_ARG;
+  } else if (w->Ws1 || w->Ws3 || w->Ws2) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+struct Layout {
+  size_t status, logits, topk_idx, topk_gate, counts, offsets, perm, inv_perm, x_perm, h, y_perm,
+      y_shared, h_shared, total;
+};
+
+Layout layout_of(const moe_config &c) {
+  Layout L{};
+  const size_t n = c.n, E = c.n_experts, P = (size_t)c.n * c.top_k;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes);
+    return at;
+  };
+  L.status = take(kAlign);
+  L.logits = take(n * E * 4);
+  L.topk_idx = take(P * 4);
+  L.topk_gate = take(P * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.perm = take(P * 4);
+  L.inv_perm = take(P * 4);
+  L.x_perm = take(P * c.d * act_size(c));
+  L.h = take(P * c.d_ff * h_size(c));
+  L.y_perm = take(P * c.d * act_size(c));
+  L.y_shared = c.d_ff_shared ? take(n * c.d * act_size(c)) : 0;
+  L.h_shared = c.d_ff_shared ? take(n * c.d_ff_shared * h_size(c)) : 0;
+  L.total = off;
+  return L;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+  return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+moe_status check_ws(const moe_config &c, const void *ws, size_t ws_bytes) {
+  if (ws == nullptr || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < layout_of(c).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                   \
+  do {                                  \
+    const moe_status _st = (expr);      \
+    if (_st != MOE_OK) return _st;      \
+  } while (0)
+
+template <typename StageFn>
+moe_status run_expert_ffn(const moe_config &c, const void *x_perm, const int32_t *offsets,
+                          const moe_weights *w, void *y_perm, void *ws, cudaStream_t s,
+                          StageFn &&stage) {
+  const Layout L = layout_of(c);
+  int *status = at<int>(ws, L.status);
+  const int P = c.n * c.top_k;
+  const int hdt = c.act_dtype == MOE_F32 ? MOE_F32 : MOE_BF16;
+  GemmStage up{};
+  up.a_dtype = c.act_dtype;
+  up.b_dtype = c.weight_dtype;
+  up.out_dtype = hdt;
+  up.epi = c.act == MOE_ACT_RELU ? 1 : 2;
+  up.A = x_perm;
+  up.offsets = offsets;
+  up.num_experts = c.n_experts;
+  up.rows = P;
+  up.N = c.d_ff;
+  up.K = c.d;
+  up.B = w->W1;
+  up.SB = w->S1;
+  up.B3 = w->W3;
+  up.SB3 = w->S3;
+  up.out = at<void>(ws, L.h);
+  stage(MOE_STAGE_FFN_UP, 1);
+  MOE_TRY(cuda_status(launch_gemm_simt(up, status, s)));
+  GemmStage dn = up;
+  dn.a_dtype = hdt;
+  dn.epi = 0;
+  dn.A = up.out;
+  dn.N = c.d;
+  dn.K = c.d_ff;
+  dn.B = w->W2;
+  dn.SB = w->S2;
+  dn.B3 = nullptr;
+  dn.SB3 = nullptr;
+  dn.out = y_perm;
+  stage(MOE_STAGE_FFN_DOWN, 1);
+  return cuda_status(launch_gemm_simt(dn, status, s));
+}
+
+moe_status run_shared_expert(const moe_config &c, const void *x, const moe_weights *w, void *ws,
+                             cudaStream_t s) {
+  const Layout L = layout_of(c);
+  int *status = at<int>(ws, L.status);
+  const int hdt = c.act_dtype == MOE_F32 ? MOE_F32 : MOE_BF16;
+  GemmStage up{};
+  up.a_dtype = c.act_dtype;
+  up.b_dtype = c.act_dtype;
+  up.out_dtype = hdt;
+  up.epi = 2;
+  up.A = x;
+  up.offsets = nullptr;
+  up.num_experts = 1;
+  up.rows = c.n;
+  up.N = c.d_ff_shared;
+  up.K = c.d;
+  up.B = w->Ws1;
+  up.B3 = w->Ws3;
+  up.out = at<void>(ws, L.h_shared);
+  MOE_TRY(cuda_status(launch_gemm_simt(up, status, s)));
+  GemmStage dn = up;
+  dn.a_dtype = hdt;
+  dn.epi = 0;
+  dn.A = up.out;
+  dn.N = c.d;
+  dn.K = c.d_ff_shared;
+  dn.B = w->Ws2;
+  dn.B3 = nullptr;
+  dn.out = at<void>(ws, L.y_shared);
+  return cuda_status(launch_gemm_simt(dn, status, s));
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status moe_workspace_size(const moe_config *cfg, size_t *bytes) {
+  MOE_TRY(check_config(cfg));
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = layout_of(*cfg).total;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_layout_of(const moe_config *cfg, moe_workspace_layout *out) {
+  MOE_TRY(check_config(cfg));
+  if (out == nullptr) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(*cfg);
+  out->status = L.status;
+  out->logits = L.logits;
+  out->topk_idx = L.topk_idx;
+  out->topk_gate = L.topk_gate;
+  out->counts = L.counts;
+  out->offsets = L.offsets;
+  out->perm = L.perm;
+  out->inv_perm = L.inv_perm;
+  out->x_perm = L.x_perm;
+  out->h = L.h;
+  out->y_perm = L.y_perm;
+  out->y_shared = L.y_shared;
+  out->h_shared = L.h_shared;
+  out->total = L.total;
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_config *cfg, const void *x, const moe_weights *w,
+                     int32_t *topk_idx, float *topk_gate, float *probs, void *ws,
+                     size_t ws_bytes, void *stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config &c = *cfg;
+  MOE_TRY(check_router_weights(c, w));
+  if (!ok_ptr(x) || !ok_ptr(topk_idx) || !ok_ptr(topk_gate)) return MOE_ERR_INVALID_ARG;
+  if (probs != nullptr && !aligned(probs, 16)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  const Layout L = layout_of(c);
+  return cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits), topk_idx,
+                                  topk_gate, probs, at<int>(ws, L.status), as_stream(stream)));
+}
+
+moe_status moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x,
+                        int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
+                        void *x_perm, void *ws, size_t ws_bytes, void *stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config &c = *cfg;
+  if (!ok_ptr(topk_idx) || !ok_ptr(counts) || !ok_ptr(offsets) || !ok_ptr(perm) ||
+      !ok_ptr(inv_perm))
+    return MOE_ERR_INVALID_ARG;
+  if (x_perm != nullptr && !ok_ptr(x)) return MOE_ERR_INVALID_ARG;
+  if (x_perm != nullptr && !ok_ptr(x_perm)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  const Layout L = layout_of(c);
+  int *status = at<int>(ws, L.status);
+  const int P = c.n * c.top_k;
+  cudaStream_t s = as_stream(stream);
+  MOE_TRY(cuda_status(
+      launch_dispatch(P, c.n_experts, topk_idx, counts, offsets, perm, inv_perm, status, s)));
+  if (x_perm != nullptr)
+    MOE_TRY(cuda_status(launch_gather(x, perm, P, c.top_k, c.n, (int64_t)c.d * act_size(c),
+                                      x_perm, status, s)));
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32_t *offsets,
+                          const moe_weights *w, void *y_perm, void *ws, size_t ws_bytes,
+                          void *stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config &c = *cfg;
+  if (c.d_ff_shared != 0) {
+    // the routed experts only; shared-expert weights are not read here
+    moe_config c2 = c;
+    c2.d_ff_shared = 0;
+    moe_weights w2 = w ? *w : moe_weights{};
+    w2.Ws1 = w2.Ws2 = w2.Ws3 = nullptr;
+    MOE_TRY(check_expert_weights(c2, &w2));
+  } else {
+    MOE_TRY(check_expert_weights(c, w));
+  }
+  if (!ok_ptr(x_perm) || !ok_ptr(offsets) || !ok_ptr(y_perm)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  return run_expert_ffn(c, x_perm, offsets, w, y_perm, ws, as_stream(stream), [](int, int) {});
+}
+
+moe_status moe_combine(const moe_config *cfg, const void *y_perm, const int32_t *inv_perm,
+                       const float *topk_gate, const void *y_shared, void *y, void *ws,
+                       size_t ws_bytes, void *stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config &c = *cfg;
+  if (!ok_ptr(y_perm) || !ok_ptr(inv_perm) || !ok_ptr(topk_gate) || !ok_ptr(y))
+    return MOE_ERR_INVALID_ARG;
+  if (y_shared != nullptr && !aligned(y_shared, 16)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  const Layout L = layout_of(c);
+  return cuda_status(launch_combine(c.act_dtype, y_perm, inv_perm, topk_gate, y_shared, y, c.n,
+                                    c.top_k, c.d, at<int>(ws, L.status), as_stream(stream)));
+}
+
+moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_weights *w, void *y,
+                              void *ws, size_t ws_bytes, void *stream, moe_stage_hook hook,
+                              void *user) {
+  MOE_TRY(check_config(cfg));
+  const moe_config &c = *cfg;
+  MOE_TRY(check_router_weights(c, w));
+  MOE_TRY(check_expert_weights(c, w));
+  if (!ok_ptr(x) || !ok_ptr(y)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  const Layout L = layout_of(c);
+  cudaStream_t s = as_stream(stream);
+  int *status = at<int>(ws, L.status);
+  const int P = c.n * c.top_k;
+  int launched = 0;
+  auto stage = [&](int id, int kernels) {
+    if (hook) hook(id, launched, user);
+    launched += kernels;
+  };
+  MOE_TRY(cuda_status(cudaMemsetAsync(status, 0, 2 * sizeof(int), s)));
+  int32_t *topk_idx = at<int32_t>(ws, L.topk_idx);
+  float *gates = at<float>(ws, L.topk_gate);
+  int32_t *offsets = at<int32_t>(ws, L.offsets);
+  int32_t *perm = at<int32_t>(ws, L.perm);
+  int32_t *inv_perm = at<int32_t>(ws, L.inv_perm);
+  stage(MOE_STAGE_ROUTE, 2);
+  MOE_TRY(cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits), topk_idx,
+                                   gates, nullptr, status, s)));
+  stage(MOE_STAGE_DISPATCH, 2);
+  MOE_TRY(cuda_status(launch_dispatch(P, c.n_experts, topk_idx, at<int32_t>(ws, L.counts), offsets,
+                                      perm, inv_perm, status, s)));
+  MOE_TRY(cuda_status(launch_gather(x, perm, P, c.top_k, c.n, (int64_t)c.d * act_size(c),
+                                    at<void>(ws, L.x_perm), status, s)));
+  MOE_TRY(run_expert_ffn(c, at<void>(ws, L.x_perm), offsets, w, at<void>(ws, L.y_perm), ws, s,
+                         stage));
+  const void *y_shared = nullptr;
+  if (c.d_ff_shared) {
+    stage(MOE_STAGE_SHARED, 2);
+    MOE_TRY(run_shared_expert(c, x, w, ws, s));
+    y_shared = at<void>(ws, L.y_shared);
+  }
+  stage(MOE_STAGE_COMBINE, 1);
+  MOE_TRY(cuda_status(launch_combine(c.act_dtype, at<void>(ws, L.y_perm), inv_perm, gates, y_shared,
+                                     y, c.n, c.top_k, c.d, status, s)));
+  stage(MOE_STAGE_END, 0);
+  return MOE_OK;
+}
+
+moe_status moe_forward(const moe_config *cfg, const void *x, const moe_weights *w, void *y,
+                       void *ws, size_t ws_bytes, void *stream) {
+  return moe_forward_staged(cfg, x, w, y, ws, ws_bytes, stream, nullptr, nullptr);
+}
+
+moe_status moe_status_check(const void *ws, void *stream, int32_t *detail) {
+  if (ws == nullptr || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t word[2] = {0, 0};
+  if (cudaMemcpy(word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (detail) *detail = word[1];
+  return static_cast<moe_status>(word[0]);
+}
+
+moe_status moe_status_clear(void *ws, void *stream) {
+  if (ws == nullptr || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, 2 * sizeof(int32_t), as_stream(stream)));
+}
+
+const char *moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: configuration not supported";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA runtime error";
+    case MOE_ERR_BAD_INDEX: return "MOE_ERR_BAD_INDEX: index out of range on the device";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: device pipeline wait ran out";
+  }
+  return "unknown moe_status";
+}
+
+}  // extern "C"

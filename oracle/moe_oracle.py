@@ -103,11 +103,12 @@ def mxfp4_decode(packed: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
     lo = packed & 0x0F
     hi = packed >> 4
     codes = torch.stack((lo, hi), dim=-1).reshape(*packed.shape[:-1], packed.shape[-1] * 2)
-    vals = e2m1_value(codes)
+    # the 16 code values from the closed form, then looked up per element
+    vals = e2m1_value(torch.arange(16, dtype=torch.uint8))[codes.to(torch.int64)]
     K = vals.shape[-1]
-    scale = e8m0_value(scales).repeat_interleave(32, dim=-1)
-    assert scale.shape[-1] == K
-    return vals * scale
+    scale = e8m0_value(scales)
+    assert scale.shape[-1] * 32 == K
+    return (vals.reshape(*vals.shape[:-1], K // 32, 32) * scale.unsqueeze(-1)).reshape(vals.shape)
 
 
 # ---------------------------------------------------------------------------

@@ -1,0 +1,259 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle.
+
+Small cases run the whole layer against the oracle on every token; the five
+workloads at full size run the same moe_forward launch sequence the benchmark
+times, with routing and dispatch checked on every token and expert outputs on
+a seeded sample of rows.
+"""
+import math
+
+import pytest
+import torch
+
+import moe_synth
+from oracle import moe_oracle as O
+import parity
+
+pytestmark = pytest.mark.gpu
+
+C = moe_synth.CONFIGS
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_layer_moe_gb300 import build
+    build.build()
+    from mixture_experts_layer_moe_gb300 import moe
+    assert torch.cuda.is_available()
+    return moe
+
+
+SMALL = {
+    "tiny_switch_fp32": C["tiny_switch_fp32"],
+    "tiny_switch_fp32_n1": C["tiny_switch_fp32"].scaled(n=1),
+    "mixtral_small": C["mixtral_bf16"].scaled(n=300, d=256, d_ff=512),
+    "mixtral_E1": C["mixtral_bf16"].scaled(n=37, d=128, d_ff=256, E=1, k=1),
+    "mixtral_k_eq_E": C["mixtral_bf16"].scaled(n=45, d=128, d_ff=192, E=5, k=5),
+    "decode_n1": C["gptoss_decode_mxfp4"].scaled(n=1),
+    "decode_n4": C["gptoss_decode_mxfp4"].scaled(n=4),
+    "prefill_zipf_small": C["gptoss_prefill_zipf_mxfp4"].scaled(n=600, d=256, d_ff=320, E=16),
+    "finegrained_small": C["finegrained_shared_bf16"].scaled(n=500, d=256, d_ff=128, E=32,
+                                                             d_ff_shared=192),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_forward_small(lib, name):
+    cfg = SMALL[name]
+    res = parity.full_parity(lib, cfg, seed=0)
+    print(f"{name}: err={res['err']:.3e} near_ties={res['near_ties']}")
+    if name == "prefill_zipf_small":
+        assert (res["counts"] == 0).any(), "the skewed router should leave some expert empty"
+
+
+FULL = {
+    "tiny_switch_fp32": (C["tiny_switch_fp32"], None),
+    "mixtral_bf16": (C["mixtral_bf16"], 24),
+    "gptoss_decode_mxfp4_n16": (C["gptoss_decode_mxfp4"].scaled(n=16), 8),
+    "gptoss_decode_mxfp4_n64": (C["gptoss_decode_mxfp4"].scaled(n=64), 8),
+    "gptoss_prefill_zipf_mxfp4": (C["gptoss_prefill_zipf_mxfp4"], 24),
+    "finegrained_shared_bf16": (C["finegrained_shared_bf16"], 12),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_forward_full_size(lib, name):
+    cfg, sample = FULL[name]
+    res = parity.full_parity(lib, cfg, seed=0, sample=sample)
+    counts = res["counts"]
+    print(f"{name}: err={res['err']:.3e} near_ties={res['near_ties']} "
+          f"empty_experts={(counts == 0).sum().item()} max_load={counts.max().item()}")
+    del res
+    torch.cuda.empty_cache()
+
+
+def test_forward_deterministic(lib):
+    cfg = SMALL["finegrained_small"]
+    inputs = moe_synth.make_inputs(cfg, seed=3, device="cuda")
+    y1, ws1, L, i1 = parity.run_forward(lib, cfg, inputs)
+    y2, ws2, _, i2 = parity.run_forward(lib, cfg, inputs)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    for k in i1:
+        assert torch.equal(i1[k], i2[k]), k
+
+
+# ------------------------------------------------------------------ router
+
+def test_route_page_example(lib):
+    """Router probabilities 0.45/0.19/0.05/0.31: top-1 picks expert 1 with gate 0.45;
+    top-2 picks experts 1 and 4 with 0.59/0.41."""
+    probs = [0.45, 0.19, 0.05, 0.31]
+    for k, gate in ((1, "top_prob"), (2, "renorm")):
+        cfg = moe_synth.MoEConfig("ex", n=1, d=4, d_ff=4, E=4, k=k, act_dtype="f32",
+                                  weight_dtype="f32", gate=gate, act="relu")
+        x = torch.tensor([[1.0, 0.0, 0.0, 0.0]], device="cuda")
+        Wg = torch.tensor([[math.log(p), 7.0, 7.0, 7.0] for p in probs], device="cuda")
+        w = lib.make_weights(dict(Wg=Wg))
+        ws = lib.alloc_workspace(cfg)
+        idx = torch.empty(1, k, dtype=torch.int32, device="cuda")
+        g = torch.empty(1, k, dtype=torch.float32, device="cuda")
+        pr = torch.empty(1, 4, dtype=torch.float32, device="cuda")
+        lib.moe_route(cfg, x, w, idx, g, pr, ws)
+        assert lib.moe_status_check(ws)[0] == 0
+        if k == 1:
+            assert idx.tolist() == [[0]]
+            assert abs(g.item() - 0.45) < 1e-6
+        else:
+            assert idx.tolist() == [[0, 3]]
+            assert [round(v, 2) for v in g[0].tolist()] == [0.59, 0.41]
+            assert abs(g[0, 0].item() - 0.45 / 0.76) < 1e-6
+        assert torch.allclose(pr.cpu(), torch.tensor([probs]), atol=1e-6)
+
+
+@pytest.mark.parametrize("name", ["mixtral_small", "prefill_zipf_small", "finegrained_small"])
+def test_route_probs(lib, name):
+    cfg = SMALL[name]
+    inputs = moe_synth.make_inputs(cfg, seed=5, device="cuda")
+    w = lib.make_weights(inputs)
+    ws = lib.alloc_workspace(cfg)
+    idx = torch.empty(cfg.n, cfg.k, dtype=torch.int32, device="cuda")
+    g = torch.empty(cfg.n, cfg.k, dtype=torch.float32, device="cuda")
+    pr = torch.empty(cfg.n, cfg.E, dtype=torch.float32, device="cuda")
+    lib.moe_route(cfg, inputs["x"], w, idx, g, pr, ws)
+    assert lib.moe_status_check(ws)[0] == 0
+    r = O.route(cfg, parity.oracle_inputs(inputs))
+    parity.check_routing(cfg, r, idx.cpu(), g.cpu())
+    assert (pr.cpu().double() - r["probs"]).abs().max().item() < 1e-5
+    assert (pr.sum(1).cpu().double() - 1).abs().max().item() < 1e-5
+
+
+# ---------------------------------------------------------------- dispatch
+
+def _dispatch(lib, cfg, idx, x=None):
+    P = cfg.n * cfg.k
+    dev = "cuda"
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(P, dtype=torch.int32, device=dev)
+    inv = torch.empty(P, dtype=torch.int32, device=dev)
+    x_perm = None if x is None else torch.empty(P, cfg.d, dtype=x.dtype, device=dev)
+    ws = lib.alloc_workspace(cfg)
+    lib.moe_dispatch(cfg, idx.to(dev, torch.int32).contiguous(), x, counts, offsets, perm, inv,
+                     x_perm, ws)
+    st = lib.moe_status_check(ws)
+    return st, counts.cpu(), offsets.cpu(), perm.cpu(), inv.cpu(), x_perm
+
+
+def _cfg(n, E, k, d=64):
+    return moe_synth.MoEConfig("t", n=n, d=d, d_ff=64, E=E, k=k, act_dtype="bf16",
+                               weight_dtype="bf16", gate="renorm", act="swiglu")
+
+
+def test_dispatch_page_example(lib):
+    """Six tokens, four experts: t2,t5 -> E1; t1,t4,t6 -> E2; t3 -> E4; E3 empty."""
+    idx = torch.tensor([[1], [0], [3], [1], [0], [1]])
+    st, counts, offsets, perm, inv, _ = _dispatch(lib, _cfg(6, 4, 1), idx)
+    assert st[0] == 0
+    assert counts.tolist() == [2, 3, 0, 1]
+    assert offsets.tolist() == [0, 2, 5, 5, 6]
+    assert perm.tolist() == [1, 4, 0, 3, 5, 2]
+    assert inv[perm.long()].tolist() == list(range(6))
+
+
+@pytest.mark.parametrize("n,E,k", [(1, 1, 1), (7, 3, 2), (33, 8, 8), (1000, 256, 8),
+                                   (4096, 8, 2), (8192, 128, 4), (16384, 256, 8)])
+def test_dispatch_random(lib, n, E, k):
+    g = torch.Generator().manual_seed(n * 31 + E)
+    logits = torch.randn(n, E, generator=g, dtype=torch.float64)
+    idx = O.topk_select(logits, k)
+    x = torch.randn(n, 64, generator=g).to(torch.bfloat16).cuda()
+    st, counts, offsets, perm, inv, x_perm = _dispatch(lib, _cfg(n, E, k), idx, x)
+    assert st[0] == 0
+    d = O.dispatch_arrays(idx, E)
+    assert torch.equal(counts.long(), d["counts"])
+    assert torch.equal(offsets.long(), d["offsets"])
+    assert torch.equal(perm.long(), d["perm"])
+    assert torch.equal(inv.long(), d["inv_perm"])
+    assert torch.equal(x_perm.cpu().view(torch.int16), x.cpu()[d["perm"] // k].view(torch.int16))
+
+
+def test_dispatch_all_to_one_expert(lib):
+    n, E, k = 3000, 64, 1
+    idx = torch.full((n, k), 37)
+    st, counts, offsets, perm, inv, _ = _dispatch(lib, _cfg(n, E, k), idx)
+    assert st[0] == 0
+    assert counts[37].item() == n and counts.sum().item() == n
+    assert perm.tolist() == list(range(n))
+
+
+def test_dispatch_bad_index_reported(lib):
+    """An out-of-range expert id is reported in the status word and skipped."""
+    idx = torch.tensor([[0], [1], [9], [2]])
+    st, counts, offsets, perm, inv, _ = _dispatch(lib, _cfg(4, 4, 1), idx)
+    assert st == (5, 2)                      # MOE_ERR_BAD_INDEX at pair 2
+    assert counts.tolist() == [1, 1, 1, 0]
+    assert inv[2].item() == -1
+
+
+# ----------------------------------------------------------------- combine
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_combine_random(lib, dtype):
+    n, E, k, d = 333, 16, 4, 128
+    cfg = moe_synth.MoEConfig("t", n=n, d=d, d_ff=64, E=E, k=k, act_dtype=dtype,
+                              weight_dtype=dtype, gate="renorm", act="swiglu", d_ff_shared=64)
+    g = torch.Generator().manual_seed(7)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    idx = O.topk_select(torch.randn(n, E, generator=g, dtype=torch.float64), k)
+    dd = O.dispatch_arrays(idx, E)
+    y_perm = torch.randn(n * k, d, generator=g).to(tdt)
+    gates = torch.rand(n, k, generator=g)
+    y_sh = torch.randn(n, d, generator=g).to(tdt)
+    y = torch.empty(n, d, dtype=tdt, device="cuda")
+    ws = lib.alloc_workspace(cfg)
+    lib.moe_combine(cfg, y_perm.cuda(), dd["inv_perm"].to(torch.int32).cuda(), gates.cuda(),
+                    y_sh.cuda(), y, ws)
+    assert lib.moe_status_check(ws)[0] == 0
+    o = O.combine(O.to_f64(y_perm), dd["inv_perm"], gates.double(), O.to_f64(y_sh))
+    err = (y.cpu().double() - o).abs()
+    bound = (2.0 ** -8 if dtype == "bf16" else 1e-6) * o.abs() + 1e-6
+    assert torch.all(err <= bound), err.max().item()
+
+
+def test_combine_bad_inverse_reported(lib):
+    n, k, d = 4, 2, 64
+    cfg = _cfg(n, 4, k, d)
+    inv = torch.tensor([0, 1, 2, 99, 4, 5, 6, 7], dtype=torch.int32, device="cuda")
+    y_perm = torch.ones(n * k, d, dtype=torch.bfloat16, device="cuda")
+    gates = torch.full((n, k), 0.5, device="cuda")
+    y = torch.empty(n, d, dtype=torch.bfloat16, device="cuda")
+    ws = lib.alloc_workspace(cfg)
+    lib.moe_combine(cfg, y_perm, inv, gates, None, y, ws)
+    assert lib.moe_status_check(ws) == (5, 3)
+    assert y[0].float().eq(1.0).all() and y[1].float().eq(0.5).all()
+
+
+# -------------------------------------------------------------- expert FFN
+
+@pytest.mark.parametrize("name", ["tiny_switch_fp32", "mixtral_small", "prefill_zipf_small"])
+def test_expert_ffn_segments(lib, name):
+    cfg = SMALL[name]
+    inputs = moe_synth.make_inputs(cfg, seed=8, device="cuda")
+    oin = parity.oracle_inputs(inputs)
+    r = O.route(cfg, oin)
+    dd = O.dispatch_arrays(r["topk_idx"], cfg.E)
+    x_perm = inputs["x"][(dd["perm"] // cfg.k).cuda()].contiguous()
+    y_perm = torch.empty_like(x_perm)
+    ws = lib.alloc_workspace(cfg)
+    lib.moe_expert_ffn(cfg, x_perm, dd["offsets"].to(torch.int32).cuda(), lib.make_weights(inputs),
+                       y_perm, ws)
+    assert lib.moe_status_check(ws)[0] == 0
+    want = torch.empty(cfg.P, cfg.d, dtype=torch.float64)
+    xp = O.to_f64(x_perm.cpu())
+    off = dd["offsets"].tolist()
+    for e in range(cfg.E):
+        if off[e] == off[e + 1]:
+            continue
+        W1, W3, W2 = O.expert_weights(oin, cfg, e)
+        want[off[e]:off[e + 1]] = O.expert_ffn(xp[off[e]:off[e + 1]], W1, W2, cfg.act, W3)
+    parity.check_output(cfg, y_perm, want)
