@@ -39,7 +39,7 @@ L2_BYTES = 129 * 1024 * 1024
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=300)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--config", default="mixtral_bf16", choices=sorted(moe_synth.CONFIGS))

@@ -1,0 +1,401 @@
+// Grouped expert GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Each expert runs its FFN projection on its own dispatched segment ("How
+// Mixture of Experts Scales Model Parameters", sections "Dense models" and
+// "The forward pass: dispatch, then combine"):
+//   out[q][j] = epi( sum_i A[q][i] * W_e[j][i] )   for q in segment e,
+// with the SwiGLU form h = silu(A W1_e^T) * (A W3_e^T) fused in the epilogue.
+//
+// Design (one CTA per SM, persistent):
+//   warp 0      TMA producer: A tile 128 x 64 (rows of the segment) and B tile
+//               256 x 64 (W rows of expert e; for SwiGLU 128 rows of W1 then
+//               128 rows of W3) per stage, 128-byte swizzle, 4-stage ring.
+//   warp 1      allocates 512 TMEM columns; one thread issues
+//               tcgen05.mma.kind::f16 M=128 N=256 K=16 (fp32 accumulate),
+//               double-buffered accumulators (2 x 256 columns).
+//   warps 2-5   epilogue: tcgen05.ld rows of the accumulator, activation,
+//               bf16 rounding, 16-byte stores masked to the segment.
+// Tiles are ordered expert-major, then output column block, then row block,
+// so CTAs working at the same time share one expert's weight columns and its
+// whole activation segment in L2.  The tile list is derived on the device
+// from the segment offsets; empty segments produce no tiles.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int THREADS = 192;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int DYN_SMEM = STAGES * STAGE_BYTES + 1024;
+constexpr int MAX_E = 256;
+constexpr uint32_t TMEM_COLS = 512;
+
+struct TcArgs {
+  const int32_t *offsets;  // nullptr: one segment [0, rows) of expert 0
+  int num_experts;
+  int rows;
+  int K;
+  int N;           // output columns
+  __nv_bfloat16 *out;
+  int *status;
+};
+
+struct TcShared {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int failed_on_entry;
+  int num_tiles;
+  int offs[MAX_E + 1];
+  int tile_start[MAX_E];
+};
+
+struct Tile {
+  int e, row0, seg_end, n_idx;
+};
+
+__device__ __forceinline__ Tile decode_tile(const TcShared &sh, int E, int t) {
+  int lo = 0, hi = E;   // largest e with tile_start[e] <= t (skips empty experts)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (sh.tile_start[mid] <= t) lo = mid; else hi = mid;
+  }
+  Tile tl;
+  tl.e = lo;
+  const int beg = sh.offs[lo], end = sh.offs[lo + 1];
+  const int m_tiles = (end - beg + BM - 1) / BM;
+  const int local = t - sh.tile_start[lo];
+  tl.n_idx = local / m_tiles;
+  tl.row0 = beg + (local - tl.n_idx * m_tiles) * BM;
+  tl.seg_end = end;
+  return tl;
+}
+
+__device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + __expf(-a)) * b; }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// EPI: 0 plain, 1 relu, 2 swiglu (B = W1 rows, B3 = W3 rows, 128 each).
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmB3, TcArgs args) {
+  constexpr int N_OUT = (EPI == 2) ? BN / 2 : BN;   // output columns per tile
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ TcShared sh;
+  uint8_t *smem = dyn_smem + ((1024 - (tc::smem_u32(dyn_smem) & 1023)) & 1023);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = args.offsets ? args.num_experts : 1;
+  const int n_tiles = (args.N + N_OUT - 1) / N_OUT;
+  const int KB = (args.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    sh.failed_on_entry = status_failed(args.status) ? 1 : 0;
+    sh.abort = sh.failed_on_entry;
+  }
+  for (int i = threadIdx.x; i <= E; i += THREADS)
+    sh.offs[i] = args.offsets ? args.offsets[i] : (i == 0 ? 0 : args.rows);
+  if (warp == 1) tc::tmem_alloc(&sh.tmem_base, TMEM_COLS);
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&sh.full[s], 1);
+      tc::mbar_init(&sh.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&sh.tfull[a], 1);
+      tc::mbar_init(&sh.tempty[a], 128);
+    }
+    tc::mbar_init(&sh.drain, 1);
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // tile prefix over experts: lane l owns experts 8l .. 8l+7
+    int cnt[8];
+    int sum = 0, bad = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      cnt[i] = 0;
+      if (e < E) {
+        const int b = sh.offs[e], en = sh.offs[e + 1];
+        if (b < 0 || en < b || en > args.rows) bad = 1;
+        else cnt[i] = ((en - b + BM - 1) / BM) * n_tiles;
+      }
+      sum += cnt[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      if (e < E) sh.tile_start[e] = run;
+      run += cnt[i];
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      sh.num_tiles = bad ? 0 : total;
+      if (bad) set_status(args.status, MOE_ERR_BAD_INDEX, -1);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = sh.tmem_base;
+  const int num_tiles = sh.num_tiles;
+  volatile int *abort = &sh.abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      tc::prefetch_tmap(&tmA);
+      tc::prefetch_tmap(&tmB);
+      if (EPI == 2) tc::prefetch_tmap(&tmB3);
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_phase[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
+      for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
+        const Tile tl = decode_tile(sh, E, t);
+        const int wrow = tl.n_idx * N_OUT;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc::mbar_wait(&sh.empty[stage], phase ^ 1u, abort)) break;
+          uint8_t *sa = smem + stage * STAGE_BYTES;
+          uint8_t *sb = sa + A_BYTES;
+          tc::mbar_arrive_expect_tx(&sh.full[stage], STAGE_BYTES);
+          tc::tma_load_2d(&tmA, &sh.full[stage], sa, kb * BK, tl.row0);
+          if (EPI == 2) {
+            tc::tma_load_3d(&tmB, &sh.full[stage], sb, kb * BK, wrow, tl.e);
+            tc::tma_load_3d(&tmB3, &sh.full[stage], sb + B_BYTES / 2, kb * BK, wrow, tl.e);
+          } else {
+            tc::tma_load_3d(&tmB, &sh.full[stage], sb, kb * BK, wrow, tl.e);
+          }
+          last_phase[stage] = (int)phase;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (*abort) {
+        // let the copies this thread issued land before the CTA exits
+        for (int s = 0; s < STAGES; ++s)
+          if (last_phase[s] >= 0)
+            tc::mbar_wait_drain(&sh.full[s], (uint32_t)last_phase[s], 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok && !*abort; t += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!tc::mbar_wait(&sh.tempty[acc], acc_phase ^ 1u, abort)) break;
+        tc::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc::mbar_wait(&sh.full[stage], phase, abort)) { ok = false; break; }
+          tc::tc_fence_after();
+          const uint32_t sa = tc::smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc::mma_bf16(d_tmem, tc::smem_desc_sw128(sa + k * 32), tc::smem_desc_sw128(sb + k * 32),
+                         idesc, (kb | k) != 0 ? 1u : 0u);
+          tc::mma_commit(&sh.empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (ok) tc::mma_commit(&sh.tfull[acc]);
+      }
+      if (*abort) {
+        tc::mma_commit(&sh.drain);
+        tc::mbar_wait_drain(&sh.drain, 0, 100000000ull);
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5; warp w reads TMEM lanes 32*(w%4)..
+    const int quarter = warp & 3;
+    const int r_local = quarter * 32 + lane;
+    int local = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+      const Tile tl = decode_tile(sh, E, t);
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      const bool ok = tc::mbar_wait(&sh.tfull[acc], acc_phase, abort);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc::tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      const int row = tl.row0 + r_local;
+      const bool row_ok = row < tl.seg_end;
+      __nv_bfloat16 *orow = args.out + (size_t)row * args.N;
+      constexpr int CHUNKS = N_OUT / 32;
+#pragma unroll 1
+      for (int c = 0; c < CHUNKS; ++c) {
+        uint32_t a[32];
+        uint32_t b[EPI == 2 ? 32 : 1];
+        tc::tmem_ld32(tb + c * 32, a);
+        if constexpr (EPI == 2) tc::tmem_ld32(tb + N_OUT + c * 32, b);
+        tc::tmem_ld_wait();
+        if (c == CHUNKS - 1) {
+          tc::tc_fence_before();
+          tc::mbar_arrive(&sh.tempty[acc]);
+        }
+        const int col0 = tl.n_idx * N_OUT + c * 32;
+        if (row_ok) {
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float v0 = __uint_as_float(a[2 * i]), v1 = __uint_as_float(a[2 * i + 1]);
+            if constexpr (EPI == 1) {
+              v0 = fmaxf(v0, 0.f);
+              v1 = fmaxf(v1, 0.f);
+            } else if constexpr (EPI == 2) {
+              v0 = silu_mul(v0, __uint_as_float(b[2 * i]));
+              v1 = silu_mul(v1, __uint_as_float(b[2 * i + 1]));
+            }
+            packed[i] = pack_bf16x2(v0, v1);
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            if (col0 + v * 8 < args.N)
+              *reinterpret_cast<uint4 *>(orow + col0 + v * 8) =
+                  make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && sh.abort && !sh.failed_on_entry)
+    set_status(args.status, MOE_ERR_TIMEOUT, blockIdx.x);
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// bf16 tensor map, innermost dimension first; box inner extent 64 elements
+// (128 bytes, one swizzle row).
+bool make_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
+              const uint32_t *box) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t gdim[3], gstride[2];
+  cuuint32_t gbox[3], estr[3] = {1, 1, 1};
+  uint64_t stride = dims[0] * 2;
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    gbox[i] = box[i];
+    if (i + 1 < rank) {
+      gstride[i] = stride;
+      stride *= dims[i + 1];
+    }
+  }
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), gdim, gstride,
+            gbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+template <int EPI>
+cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, DYN_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int E = g.offsets ? g.num_experts : 1;
+  CUtensorMap mA, mB, mB3;
+  const uint64_t dA[2] = {(uint64_t)g.K, (uint64_t)g.rows};
+  const uint32_t bA[2] = {BK, BM};
+  const int wrows = (EPI == 2) ? BN / 2 : BN;
+  const uint64_t dB[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)E};
+  const uint32_t bB[3] = {BK, (uint32_t)wrows, 1};
+  if (!make_map(&mA, g.A, 2, dA, bA) || !make_map(&mB, g.B, 3, dB, bB))
+    return cudaErrorInvalidValue;
+  if (EPI == 2) {
+    if (!make_map(&mB3, g.B3, 3, dB, bB)) return cudaErrorInvalidValue;
+  } else {
+    mB3 = mB;
+  }
+  TcArgs a;
+  a.offsets = g.offsets;
+  a.num_experts = g.num_experts;
+  a.rows = g.rows;
+  a.K = g.K;
+  a.N = g.N;
+  a.out = static_cast<__nv_bfloat16 *>(g.out);
+  a.status = status;
+  gemm_tc_kernel<EPI><<<num_sms(), THREADS, DYN_SMEM, s>>>(mA, mB, mB3, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemm_tc_supported(const GemmStage &g) {
+  return g.a_dtype == MOE_BF16 && g.b_dtype == MOE_BF16 && g.out_dtype == MOE_BF16 &&
+         g.K % 8 == 0 && g.N % 8 == 0 && g.rows > 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s) {
+  switch (g.epi) {
+    case 0: return launch_epi<0>(g, status, s);
+    case 1: return launch_epi<1>(g, status, s);
+    default: return launch_epi<2>(g, status, s);
+  }
+}
+
+}  // namespace moe

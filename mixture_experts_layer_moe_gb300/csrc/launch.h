@@ -49,4 +49,15 @@ struct GemmStage {
 };
 cudaError_t launch_gemm_simt(const GemmStage &g, int *status, cudaStream_t s);
 
+// The same stage on tcgen05 tensor cores (bf16 operands, fp32 accumulate in
+// TMEM, TMA-fed); gemm_tc_supported() says whether the shape/dtypes qualify.
+bool gemm_tc_supported(const GemmStage &g);
+cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s);
+
+// Picks the tensor-core kernel when it applies, else the CUDA-core one.
+inline cudaError_t launch_gemm(const GemmStage &g, int *status, cudaStream_t s) {
+  if (g.rows == 0) return cudaSuccess;
+  return gemm_tc_supported(g) ? launch_gemm_tc(g, status, s) : launch_gemm_simt(g, status, s);
+}
+
 }  // namespace moe

@@ -141,7 +141,7 @@ moe_status run_expert_ffn(const moe_config &c, const void *x_perm, const int32_t
   up.SB3 = w->S3;
   up.out = at<void>(ws, L.h);
   stage(MOE_STAGE_FFN_UP, 1);
-  MOE_TRY(cuda_status(launch_gemm_simt(up, status, s)));
+  MOE_TRY(cuda_status(launch_gemm(up, status, s)));
   GemmStage dn = up;
   dn.a_dtype = hdt;
   dn.epi = 0;
@@ -154,7 +154,7 @@ moe_status run_expert_ffn(const moe_config &c, const void *x_perm, const int32_t
   dn.SB3 = nullptr;
   dn.out = y_perm;
   stage(MOE_STAGE_FFN_DOWN, 1);
-  return cuda_status(launch_gemm_simt(dn, status, s));
+  return cuda_status(launch_gemm(dn, status, s));
 }
 
 moe_status run_shared_expert(const moe_config &c, const void *x, const moe_weights *w, void *ws,
@@ -176,7 +176,7 @@ moe_status run_shared_expert(const moe_config &c, const void *x, const moe_weigh
   up.B = w->Ws1;
   up.B3 = w->Ws3;
   up.out = at<void>(ws, L.h_shared);
-  MOE_TRY(cuda_status(launch_gemm_simt(up, status, s)));
+  MOE_TRY(cuda_status(launch_gemm(up, status, s)));
   GemmStage dn = up;
   dn.a_dtype = hdt;
   dn.epi = 0;
@@ -186,7 +186,7 @@ moe_status run_shared_expert(const moe_config &c, const void *x, const moe_weigh
   dn.B = w->Ws2;
   dn.B3 = nullptr;
   dn.out = at<void>(ws, L.y_shared);
-  return cuda_status(launch_gemm_simt(dn, status, s));
+  return cuda_status(launch_gemm(dn, status, s));
 }
 
 }  // namespace
