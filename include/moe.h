@@ -144,6 +144,21 @@ moe_status moe_route(const moe_config *cfg, const void *x, const moe_weights *w,
                      int32_t *topk_idx, float *topk_gate, float *probs,
                      void *ws, size_t ws_bytes, void *stream);
 
+/* moe_route without a workspace, for callers that cannot allocate device
+ * memory: code running during CUDA graph capture under an allocator that is
+ * not capture-safe, plugins handed only their input and output buffers by a
+ * host runtime that owns all device memory, fixed-arena embedded runtimes.
+ * (An addition of this library; the pages have no counterpart.)
+ * Same arguments and results as moe_route, minus ws/ws_bytes.  The logits
+ * live in one file-scope device array of 16 MiB that every GPU loading the
+ * library holds until exit; n * n_experts above 4,194,304 returns
+ * MOE_ERR_WORKSPACE.  The first call on a device (with it current) looks up
+ * the array's address; make that call before any stream capture.  All calls
+ * share the array: calls that overlap on the GPU race and must be serialised
+ * by the caller.  No allocation, no synchronisation. */
+moe_status moe_route_noalloc(const moe_config *cfg, const void *x, const moe_weights *w,
+                             int32_t *topk_idx, float *topk_gate, float *probs, void *stream);
+
 /* Dispatch ("The forward pass: dispatch, then combine"): a stable counting
  * sort of the n*K (token, slot) pairs by expert.  Bit-exact.
  *   topk_idx int32 [n][K] (any values; out-of-range ones set MOE_ERR_BAD_INDEX

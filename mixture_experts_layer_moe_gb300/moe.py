@@ -59,6 +59,7 @@ def _load() -> ctypes.CDLL:
         "moe_workspace_size": [cfgp, ctypes.POINTER(SZ)],
         "moe_workspace_layout_of": [cfgp, ctypes.POINTER(moe_workspace_layout)],
         "moe_route": [cfgp, P, wp, P, P, P, P, SZ, P],
+        "moe_route_noalloc": [cfgp, P, wp, P, P, P, P],
         "moe_dispatch": [cfgp, P, P, P, P, P, P, P, P, SZ, P],
         "moe_expert_ffn": [cfgp, P, P, wp, P, P, SZ, P],
         "moe_combine": [cfgp, P, P, P, P, P, P, SZ, P],
@@ -151,6 +152,14 @@ def moe_route(cfg, x, w: moe_weights, topk_idx, topk_gate, probs, ws, stream=Non
     _check(_lib.moe_route(ctypes.byref(c), _ptr(x), ctypes.byref(w), _ptr(topk_idx),
                           _ptr(topk_gate), _ptr(probs), _ptr(ws), ws.numel(), _stream(stream)),
            "moe_route")
+
+
+def moe_route_noalloc(cfg, x, w: moe_weights, topk_idx, topk_gate, probs, stream=None):
+    """moe_route without a workspace (scratch in a static device array; calls must not overlap)."""
+    c = make_config(cfg)
+    _check(_lib.moe_route_noalloc(ctypes.byref(c), _ptr(x), ctypes.byref(w), _ptr(topk_idx),
+                                  _ptr(topk_gate), _ptr(probs), _stream(stream)),
+           "moe_route_noalloc")
 
 
 def moe_dispatch(cfg, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, ws, stream=None):
