@@ -155,15 +155,41 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def dominant_kernel(cfg):
+DECODE_MAX_PAIRS = 256   # the library's small-batch MXFP4 path (n*k up to this)
+DECODE_BATCHES = 8       # token batches rotated through in decode timing
+
+
+def is_decode(cfg) -> bool:
+    return cfg.weight_dtype == "mxfp4" and cfg.n * cfg.k <= DECODE_MAX_PAIRS
+
+
+def dominant_kernel(cfg, active_experts=None):
     """(stage name, bound, algorithmic units per launch, unit) of the dominant kernel.
 
     Tensor-bound workloads: the up-projection grouped GEMM (W1 and W3, 2/3 of the
     expert FLOPs with SwiGLU), FLOPs = 2 * (n*k) * d * d_ff * (2 for SwiGLU, else 1).
+    Small-batch MXFP4 (decode): the up-projection kernel streams the selected
+    experts' W1/W3 codes and scales once, reads the tokens' x rows and writes h:
+    bytes = u * mats * d_ff * (d/2 + d/32) + n*k*d*2 + n*k*d_ff*2.
     """
     mats = 2 if cfg.act == "swiglu" else 1
+    if is_decode(cfg):
+        u = active_experts if active_experts is not None else min(cfg.E, cfg.n * cfg.k)
+        P = cfg.n * cfg.k
+        nbytes = (u * mats * cfg.d_ff * (cfg.d // 2 + cfg.d // 32)
+                  + P * cfg.d * 2 + P * cfg.d_ff * 2)
+        return "ffn_up", "hbm", nbytes, "GB/s"
     flops = 2 * cfg.n * cfg.k * cfg.d * cfg.d_ff * mats
     return "ffn_up", "tensor", flops, "TFLOP/s"
+
+
+def make_event(timing=True, external=False):
+    if external:
+        try:
+            return torch.cuda.Event(enable_timing=timing, external=True)
+        except TypeError:
+            return None
+    return torch.cuda.Event(enable_timing=timing)
 
 
 # -------------------------------------------------------------- CPU baseline
@@ -223,45 +249,102 @@ def run_ours(args):
     w = moe.make_weights(inputs)
     ws = moe.alloc_workspace(cfg, device)
     y = torch.empty(cfg.n, cfg.d, dtype=inputs["x"].dtype, device=device)
-    stream = torch.cuda.current_stream(device)
-    weight_bytes = cfg.E * moe_synth.weight_bytes_per_expert(cfg)
+    # a non-default stream: CUDA graphs cannot be captured on the legacy default stream
+    stream = torch.cuda.Stream(device)
+    torch.cuda.set_stream(stream)
 
     stage_names = moe.STAGES
-    dom_stage, bound, dom_units, dom_unit = dominant_kernel(cfg)
-    dom_idx, dom_next = stage_names.index(dom_stage), stage_names.index(dom_stage) + 1
     launches = {"n": 0}
+    # Small-batch MXFP4 steps read only the selected experts (tens of MB, below
+    # L2): rotate over seeded token batches so each step routes differently and
+    # its experts come from HBM, as in a real decode loop.
+    n_batches = DECODE_BATCHES if is_decode(cfg) else 1
+    x_pool = [inputs["x"]]
+    for r in range(1, n_batches):
+        gr = torch.Generator(device=device).manual_seed(args.seed + 7919 * r + 1000 * rank)
+        xr = torch.randn(inputs["x"].shape, generator=gr, device=device, dtype=torch.float32)
+        x_pool.append((xr * cfg.x_std).to(inputs["x"].dtype))
 
-    def step(events=None):
+    def step(i, events=None):
         def hook(stage, kernels):
             if events is not None:
                 events[stage].record(stream)
             if stage == len(stage_names) - 1:
                 launches["n"] = kernels
-        moe.moe_forward_staged(cfg, inputs["x"], w, y, ws, hook, stream)
+        moe.moe_forward_staged(cfg, x_pool[i % n_batches], w, y, ws, hook, stream)
 
-    for _ in range(args.warmup):
-        step()
+    L = moe.moe_workspace_layout_of(cfg)
+    counts = ws[L["counts"]:L["counts"] + 4 * cfg.E].view(torch.int32)
+    active_per_batch = []
+    for i in range(max(args.warmup, n_batches)):
+        step(i)
+        if i < n_batches:
+            torch.cuda.synchronize(device)
+            active_per_batch.append(int((counts > 0).sum().item()))
     torch.cuda.synchronize(device)
     st, detail = moe.moe_status_check(ws)
     if st != 0:
         raise RuntimeError(f"device status {moe.status_string(st)} ({detail})")
+    step_units = [dominant_kernel(cfg, active_per_batch[i % n_batches])[2]
+                  for i in range(args.steps)]
+    active = statistics.mean(active_per_batch[i % n_batches] for i in range(args.steps))
+    dom_stage, bound, _, dom_unit = dominant_kernel(cfg)
+    dom_units = statistics.mean(step_units)
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in stage_names] for _ in range(args.steps)]
+    # The timed region: K steps captured into one CUDA graph (external event
+    # nodes between stages) and replayed once; eager launches if capture fails.
+    timing = "cuda_graph"
+    graph = None
+    plain = None
+    ev = [[make_event(external=True) for _ in stage_names] for _ in range(args.steps)]
+    if any(e is None for row in ev for e in row):
+        print("bench: torch.cuda.Event(external=True) unavailable; timing eager launches",
+              file=sys.stderr)
+        timing = "eager"
+    else:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for i in range(args.steps):
+                    step(i, ev[i])
+            plain = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(plain, stream=stream):
+                for i in range(args.steps):
+                    step(i)
+            torch.cuda.synchronize(device)
+        except Exception as exc:  # capture unsupported here: time eager launches instead
+            print(f"bench: CUDA graph capture failed ({exc!r}); timing eager launches",
+                  file=sys.stderr)
+            graph, timing = None, "eager"
+            torch.cuda.synchronize(device)
+    if graph is None:
+        ev = [[make_event() for _ in stage_names] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(device)
     torch.cuda.synchronize(device)
+    # timed region: the K steps (the graph without stage events when captured),
+    # then the same K steps with the stage events for the per-stage breakdown
     with ClockSampler(device.index) as clocks:
         start.record(stream)
-        for i in range(args.steps):
-            step(ev[i])
+        if plain is not None:
+            plain.replay()
+        else:
+            for i in range(args.steps):
+                step(i, ev[i])
         stop.record(stream)
+        if graph is not None:
+            graph.replay()
         torch.cuda.synchronize(device)
     barrier(device)
     elapsed = start.elapsed_time(stop) / 1e3
     t_job = max_over_ranks(elapsed, device)
     kernels_per_step = launches["n"]
+    st, detail = moe.moe_status_check(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {moe.status_string(st)} ({detail})")
 
     # per-stage durations (CUDA events on the launching stream, inside the timed region)
+    dom_idx = stage_names.index(dom_stage)
     present = [s for s in range(len(stage_names) - 1)
                if s != stage_names.index("shared") or cfg.d_ff_shared]
     stage_ms = {}
@@ -270,7 +353,8 @@ def run_ours(args):
                     if t in present or t == len(stage_names) - 1))
         stage_ms[stage_names[s]] = statistics.mean(
             ev[i][s].elapsed_time(ev[i][nxt]) for i in range(args.steps))
-    dom_ms = stage_ms[dom_stage]
+    dom_ms = sum(ev[i][dom_idx].elapsed_time(ev[i][dom_idx + 1]) for i in range(args.steps)) / args.steps
+    del graph, plain
 
     # end to end: pinned host x in, pinned host y out, every step
     x_host = inputs["x"].cpu().pin_memory()
@@ -296,12 +380,24 @@ def run_ours(args):
         raise RuntimeError(f"device status {moe.status_string(st)} ({detail})")
 
     peaks, peak_src = load_peaks()
+    step_bytes = (active if is_decode(cfg) else cfg.E) * moe_synth.weight_bytes_per_expert(cfg)
+    if n_batches > 1:
+        l2_note = (f"{n_batches} seeded token batches rotate through the timed steps, so each "
+                   f"step routes to other experts ({step_bytes / 1e6:.1f} MB of expert weights "
+                   f"per step on average; L2 is {L2_BYTES / 1e6:.0f} MB)")
+    else:
+        l2_note = (f"inputs larger than L2: {step_bytes / 1e9:.3f} GB of expert weights read per "
+                   f"step" if step_bytes > L2_BYTES else
+                   f"expert weights read per step ({step_bytes / 1e6:.1f} MB) fit in L2 and are "
+                   f"not flushed: the step may run from L2")
     if bound == "tensor":
         peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
         achieved = dom_units / (dom_ms / 1e3) / 1e12
     else:
         peak = peaks["hbm_gbs"]
         achieved = dom_units / (dom_ms / 1e3) / 1e9
+    per_launch = ({"flops_per_launch": dom_units} if bound == "tensor"
+                  else {"bytes_per_launch": dom_units, "active_experts_mean": active})
 
     out = {
         "metric": "MoE-layer tokens/s",
@@ -320,8 +416,8 @@ def run_ours(args):
             "workload": workload_name(cfg),
             "tokens_per_rank": cfg.n,
             "parallelism": f"dp{world} (independent token batches, replicated weights)",
-            "l2": (f"inputs larger than L2: {weight_bytes / 1e9:.2f} GB of expert weights per step"
-                   if weight_bytes > L2_BYTES else "L2 not flushed: working set below L2"),
+            "l2": l2_note,
+            "timing": timing,
         },
         "e2e": {"value": job_throughput(cfg.n * args.steps, world, t_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
@@ -330,7 +426,7 @@ def run_ours(args):
         "roofline": {"kernel": dom_stage, "bound": bound, "achieved": achieved, "peak": peak,
                      "unit": dom_unit, "frac": achieved / peak,
                      "peak_source": f"{peak_src} ({'bf16 sustained' if bound == 'tensor' else 'hbm copy'})",
-                     "traffic": None},
+                     "traffic": None, **per_launch},
         "stages_ms": stage_ms,
         "clocks": clocks.summary(),
     }

@@ -117,11 +117,13 @@ typedef struct {
   size_t offsets;    /* int32 [E+1] */
   size_t perm;       /* int32 [n*K]: segment position -> pair t*K+j */
   size_t inv_perm;   /* int32 [n*K]: pair t*K+j -> segment position */
-  size_t x_perm;     /* act_dtype [n*K][d] (not written by the decode path) */
+  size_t x_perm;     /* act_dtype [n*K][d] (not written by the small-batch MXFP4 path) */
   size_t h;          /* [n*K][d_ff]: bf16, or fp32 when act_dtype is F32 */
   size_t y_perm;     /* act_dtype [n*K][d], unweighted expert outputs */
   size_t y_shared;   /* act_dtype [n][d] shared-expert output, 0 if none */
   size_t h_shared;   /* [n][d_ff_shared] shared-expert intermediate, 0 if none */
+  size_t act16;      /* small-batch MXFP4 path: f16 copies of the expert-ordered
+                        activation rows [n*K][d] then of h [n*K][d_ff]; 0 if unused */
   size_t total;      /* = moe_workspace_size() */
 } moe_workspace_layout;
 

@@ -19,8 +19,6 @@
 // so CTAs working at the same time share one expert's weight columns and its
 // whole activation segment in L2.  The tile list is derived on the device
 // from the segment offsets; empty segments produce no tiles.
-#include <cudaTypedefs.h>
-
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -43,7 +41,8 @@ struct TcArgs {
   int rows;
   int K;
   int N;           // output columns
-  __nv_bfloat16 *out;
+  void *out;       // bf16 [rows][N], fp32 for EPI 3
+  const float *bias;
   int *status;
 };
 
@@ -89,12 +88,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// EPI: 0 plain, 1 relu, 2 swiglu (B = W1 rows, B3 = W3 rows, 128 each).
+// EPI: 0 plain, 1 relu, 2 swiglu (B = W1 rows, B3 = W3 rows, 128 each),
+// 3 fp32 output + per-column bias (router logits).
+//
+// EPI 3 keeps the router's logits accurate to fp32 rounding: the tensor core
+// sums each 64-wide k-block into a fresh TMEM partial (N = 128 columns, two
+// partial buffers in flight), and the epilogue warps add the partials in fp32
+// registers with round-to-nearest.  Accumulating the whole reduction in TMEM
+// instead drifted by ~2e-5 on d = 4096 rows, too close to the 1e-5 near-tie
+// margin of the routing decision.
 template <int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmB3, TcArgs args) {
-  constexpr int N_OUT = (EPI == 2) ? BN / 2 : BN;   // output columns per tile
+  constexpr bool KPART = (EPI == 3);                 // per-k-block partials
+  constexpr int BNT = KPART ? 128 : BN;              // MMA N = B rows per stage
+  constexpr int N_OUT = (EPI == 2) ? BN / 2 : BNT;   // output columns per tile
+  constexpr uint32_t TX_BYTES = A_BYTES + BNT * BK * 2;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ TcShared sh;
   uint8_t *smem = dyn_smem + ((1024 - (tc::smem_u32(dyn_smem) & 1023)) & 1023);
@@ -183,7 +193,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (!tc::mbar_wait(&sh.empty[stage], phase ^ 1u, abort)) break;
           uint8_t *sa = smem + stage * STAGE_BYTES;
           uint8_t *sb = sa + A_BYTES;
-          tc::mbar_arrive_expect_tx(&sh.full[stage], STAGE_BYTES);
+          tc::mbar_arrive_expect_tx(&sh.full[stage], TX_BYTES);
           tc::tma_load_2d(&tmA, &sh.full[stage], sa, kb * BK, tl.row0);
           if (EPI == 2) {
             tc::tma_load_3d(&tmB, &sh.full[stage], sb, kb * BK, wrow, tl.e);
@@ -205,18 +215,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BNT);
       int stage = 0;
       uint32_t phase = 0;
-      int local = 0;
+      int local = 0;   // accumulator uses so far (tiles, or k-blocks with KPART)
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok && !*abort; t += gridDim.x, ++local) {
-        const int acc = local & 1;
-        const uint32_t acc_phase = (local >> 1) & 1;
-        if (!tc::mbar_wait(&sh.tempty[acc], acc_phase ^ 1u, abort)) break;
-        tc::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      for (int t = blockIdx.x; t < num_tiles && ok && !*abort; t += gridDim.x) {
         for (int kb = 0; kb < KB; ++kb) {
+          const bool fresh = KPART || kb == 0;
+          const int acc = local & 1;
+          if (fresh) {
+            const uint32_t acc_phase = (local >> 1) & 1;
+            if (!tc::mbar_wait(&sh.tempty[acc], acc_phase ^ 1u, abort)) { ok = false; break; }
+            tc::tc_fence_after();
+          }
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
           if (!tc::mbar_wait(&sh.full[stage], phase, abort)) { ok = false; break; }
           tc::tc_fence_after();
           const uint32_t sa = tc::smem_u32(smem + stage * STAGE_BYTES);
@@ -224,11 +237,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             tc::mma_bf16(d_tmem, tc::smem_desc_sw128(sa + k * 32), tc::smem_desc_sw128(sb + k * 32),
-                         idesc, (kb | k) != 0 ? 1u : 0u);
+                         idesc, (k != 0 || (!KPART && kb != 0)) ? 1u : 0u);
           tc::mma_commit(&sh.empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (KPART || kb == KB - 1) {
+            tc::mma_commit(&sh.tfull[acc]);
+            ++local;
+          }
         }
-        if (ok) tc::mma_commit(&sh.tfull[acc]);
       }
       if (*abort) {
         tc::mma_commit(&sh.drain);
@@ -239,51 +255,90 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ---------------- epilogue: warps 2..5; warp w reads TMEM lanes 32*(w%4)..
     const int quarter = warp & 3;
     const int r_local = quarter * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
     int local = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-      const Tile tl = decode_tile(sh, E, t);
-      const int acc = local & 1;
-      const uint32_t acc_phase = (local >> 1) & 1;
-      const bool ok = tc::mbar_wait(&sh.tfull[acc], acc_phase, abort);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      tc::tc_fence_after();
-      const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      const int row = tl.row0 + r_local;
-      const bool row_ok = row < tl.seg_end;
-      __nv_bfloat16 *orow = args.out + (size_t)row * args.N;
-      constexpr int CHUNKS = N_OUT / 32;
-#pragma unroll 1
-      for (int c = 0; c < CHUNKS; ++c) {
-        uint32_t a[32];
-        uint32_t b[EPI == 2 ? 32 : 1];
-        tc::tmem_ld32(tb + c * 32, a);
-        if constexpr (EPI == 2) tc::tmem_ld32(tb + N_OUT + c * 32, b);
-        tc::tmem_ld_wait();
-        if (c == CHUNKS - 1) {
+    if constexpr (KPART) {
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        const Tile tl = decode_tile(sh, E, t);
+        float sum[N_OUT];
+#pragma unroll
+        for (int i = 0; i < N_OUT; ++i) sum[i] = 0.f;
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++local) {
+          const int acc = local & 1;
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(&sh.tfull[acc], (local >> 1) & 1, abort));
+          if (!ok) break;
+          tc::tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < N_OUT / 32; ++c) {
+            uint32_t a[32];
+            tc::tmem_ld32(lane_base + (uint32_t)(acc * BN) + c * 32, a);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sum[c * 32 + i] += __uint_as_float(a[i]);
+          }
           tc::tc_fence_before();
           tc::mbar_arrive(&sh.tempty[acc]);
         }
-        const int col0 = tl.n_idx * N_OUT + c * 32;
-        if (row_ok) {
-          uint32_t packed[16];
+        if (!ok) break;
+        const int row = tl.row0 + r_local;
+        if (row < tl.seg_end) {
+          float *orow = static_cast<float *>(args.out) + (size_t)row * args.N;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float v0 = __uint_as_float(a[2 * i]), v1 = __uint_as_float(a[2 * i + 1]);
-            if constexpr (EPI == 1) {
-              v0 = fmaxf(v0, 0.f);
-              v1 = fmaxf(v1, 0.f);
-            } else if constexpr (EPI == 2) {
-              v0 = silu_mul(v0, __uint_as_float(b[2 * i]));
-              v1 = silu_mul(v1, __uint_as_float(b[2 * i + 1]));
+          for (int i = 0; i < N_OUT; ++i) {
+            const int col = tl.n_idx * N_OUT + i;
+            if (col < args.N) orow[col] = sum[i] + (args.bias ? args.bias[col] : 0.f);
+          }
+        }
+        __syncwarp();
+      }
+    } else {
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+        const Tile tl = decode_tile(sh, E, t);
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        const bool ok = tc::mbar_wait(&sh.tfull[acc], acc_phase, abort);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc::tc_fence_after();
+        const uint32_t tb = lane_base + (uint32_t)(acc * BN);
+        const int row = tl.row0 + r_local;
+        const bool row_ok = row < tl.seg_end;
+        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(args.out) + (size_t)row * args.N;
+        constexpr int CHUNKS = N_OUT / 32;
+#pragma unroll 1
+        for (int c = 0; c < CHUNKS; ++c) {
+          uint32_t a[32];
+          uint32_t b[EPI == 2 ? 32 : 1];
+          tc::tmem_ld32(tb + c * 32, a);
+          if constexpr (EPI == 2) tc::tmem_ld32(tb + N_OUT + c * 32, b);
+          tc::tmem_ld_wait();
+          if (c == CHUNKS - 1) {
+            tc::tc_fence_before();
+            tc::mbar_arrive(&sh.tempty[acc]);
+          }
+          const int col0 = tl.n_idx * N_OUT + c * 32;
+          if (row_ok && col0 < args.N) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float v0 = __uint_as_float(a[2 * i]), v1 = __uint_as_float(a[2 * i + 1]);
+              if constexpr (EPI == 1) {
+                v0 = fmaxf(v0, 0.f);
+                v1 = fmaxf(v1, 0.f);
+              } else if constexpr (EPI == 2) {
+                v0 = silu_mul(v0, __uint_as_float(b[2 * i]));
+                v1 = silu_mul(v1, __uint_as_float(b[2 * i + 1]));
+              }
+              packed[i] = pack_bf16x2(v0, v1);
             }
-            packed[i] = pack_bf16x2(v0, v1);
-          }
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            if (col0 + v * 8 < args.N)
-              *reinterpret_cast<uint4 *>(orow + col0 + v * 8) =
-                  make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+            for (int v = 0; v < 4; ++v) {
+              if (col0 + v * 8 < args.N)
+                *reinterpret_cast<uint4 *>(orow + col0 + v * 8) = make_uint4(
+                    packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+            }
           }
+          __syncwarp();
         }
       }
     }
@@ -302,50 +357,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // bf16 tensor map, innermost dimension first; box inner extent 64 elements
 // (128 bytes, one swizzle row).
 bool make_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
               const uint32_t *box) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t gdim[3], gstride[2];
-  cuuint32_t gbox[3], estr[3] = {1, 1, 1};
-  uint64_t stride = dims[0] * 2;
-  for (int i = 0; i < rank; ++i) {
-    gdim[i] = dims[i];
-    gbox[i] = box[i];
-    if (i + 1 < rank) {
-      gstride[i] = stride;
-      stride *= dims[i + 1];
-    }
-  }
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), gdim, gstride,
-            gbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
+  return make_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rank, dims, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int EPI>
@@ -361,7 +378,7 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
   CUtensorMap mA, mB, mB3;
   const uint64_t dA[2] = {(uint64_t)g.K, (uint64_t)g.rows};
   const uint32_t bA[2] = {BK, BM};
-  const int wrows = (EPI == 2) ? BN / 2 : BN;
+  const int wrows = (EPI == 2) ? BN / 2 : (EPI == 3 ? 128 : BN);
   const uint64_t dB[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)E};
   const uint32_t bB[3] = {BK, (uint32_t)wrows, 1};
   if (!make_map(&mA, g.A, 2, dA, bA) || !make_map(&mB, g.B, 3, dB, bB))
@@ -377,7 +394,8 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
   a.rows = g.rows;
   a.K = g.K;
   a.N = g.N;
-  a.out = static_cast<__nv_bfloat16 *>(g.out);
+  a.out = g.out;
+  a.bias = g.col_bias;
   a.status = status;
   gemm_tc_kernel<EPI><<<num_sms(), THREADS, DYN_SMEM, s>>>(mA, mB, mB3, a);
   return cudaGetLastError();
@@ -386,15 +404,18 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
 }  // namespace
 
 bool gemm_tc_supported(const GemmStage &g) {
-  return g.a_dtype == MOE_BF16 && g.b_dtype == MOE_BF16 && g.out_dtype == MOE_BF16 &&
-         g.K % 8 == 0 && g.N % 8 == 0 && g.rows > 0 && encode_fn() != nullptr;
+  const bool out_ok = g.epi == 3 ? g.out_dtype == MOE_F32 : g.out_dtype == MOE_BF16;
+  const bool n_ok = g.epi == 3 ? true : g.N % 8 == 0;
+  return g.a_dtype == MOE_BF16 && g.b_dtype == MOE_BF16 && out_ok && n_ok && g.K % 8 == 0 &&
+         g.rows > 0 && tensor_maps_available();
 }
 
 cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s) {
   switch (g.epi) {
     case 0: return launch_epi<0>(g, status, s);
     case 1: return launch_epi<1>(g, status, s);
-    default: return launch_epi<2>(g, status, s);
+    case 2: return launch_epi<2>(g, status, s);
+    default: return launch_epi<3>(g, status, s);
   }
 }
 

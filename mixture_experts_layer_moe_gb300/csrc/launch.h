@@ -1,12 +1,21 @@
 // Host-side launchers of the MoE kernels (internal; the public ABI is moe.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "moe.h"
 
 namespace moe {
+
+// Tensor-map encoding (cuTensorMapEncodeTiled through the runtime's driver
+// entry point), innermost dimension first, dense strides; and the SM count.
+bool tensor_maps_available();
+bool make_tensor_map(CUtensorMap *m, CUtensorMapDataType dtype, int elem_bytes, const void *base,
+                     int rank, const uint64_t *dims, const uint32_t *box,
+                     CUtensorMapSwizzle swizzle);
+int num_sms();
 
 // Router: logits (fp32 [n][E] scratch) -> softmax -> top-k -> gates.
 cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, const float *bias,
@@ -29,7 +38,8 @@ cudaError_t launch_combine(int act_dtype, const void *y_perm, const int32_t *inv
 
 // One grouped GEMM stage on CUDA cores (fp32 accumulate):
 //   out[q][j] = epi( sum_i A[q][i] * B_e[j][i] )  for q in segment e.
-// epi: 0 = none, 1 = relu, 2 = swiglu (B3 gives the linear branch).
+// epi: 0 = none, 1 = relu, 2 = swiglu (B3 gives the linear branch),
+//      3 = fp32 output + col_bias[j] (router logits; tensor-core path only).
 // offsets == nullptr means one segment [0, rows) using expert 0.
 struct GemmStage {
   int a_dtype;          // MOE_F32 / MOE_BF16
@@ -46,6 +56,7 @@ struct GemmStage {
   const void *B3;
   const uint8_t *SB3;
   void *out;            // [rows][N]
+  const float *col_bias; // epi 3: per-column bias or nullptr
 };
 cudaError_t launch_gemm_simt(const GemmStage &g, int *status, cudaStream_t s);
 
@@ -59,5 +70,18 @@ inline cudaError_t launch_gemm(const GemmStage &g, int *status, cudaStream_t s) 
   if (g.rows == 0) return cudaSuccess;
   return gemm_tc_supported(g) ? launch_gemm_tc(g, status, s) : launch_gemm_simt(g, status, s);
 }
+
+// Small-batch MXFP4 path over the selected experts only, weights streamed
+// once and dequantised in registers.  part 0: f16 copies of the activation
+// rows in segment order (x [n][d] gathered through perm, or x_perm [P][d] when
+// perm is nullptr) into act16, then up + activation -> h [P][d_ff] (bf16, and
+// an f16 copy in act16).  part 1: down -> y_perm [P][d].  act16 is workspace
+// of decode_act16_bytes(c).
+constexpr int kDecodeMaxPairs = 256;
+bool decode_supported(const moe_config &c);
+size_t decode_act16_bytes(const moe_config &c);
+cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
+                              const int32_t *perm, const int32_t *offsets, const moe_weights &w,
+                              void *h, void *y_perm, void *act16, int *status, cudaStream_t s);
 
 }  // namespace moe

@@ -68,7 +68,7 @@ moe_status check_expert_weights(const moe_config &c, const moe_weights *w) {
 
 struct Layout {
   size_t status, logits, topk_idx, topk_gate, counts, offsets, perm, inv_perm, x_perm, h, y_perm,
-      y_shared, h_shared, total;
+      y_shared, h_shared, act16, total;
 };
 
 Layout layout_of(const moe_config &c) {
@@ -93,6 +93,8 @@ Layout layout_of(const moe_config &c) {
   L.y_perm = take(P * c.d * act_size(c));
   L.y_shared = c.d_ff_shared ? take(n * c.d * act_size(c)) : 0;
   L.h_shared = c.d_ff_shared ? take(n * c.d_ff_shared * h_size(c)) : 0;
+  const size_t a16 = decode_act16_bytes(c);
+  L.act16 = a16 ? take(a16) : 0;
   L.total = off;
   return L;
 }
@@ -122,6 +124,14 @@ moe_status run_expert_ffn(const moe_config &c, const void *x_perm, const int32_t
                           StageFn &&stage) {
   const Layout L = layout_of(c);
   int *status = at<int>(ws, L.status);
+  if (decode_supported(c)) {
+    stage(MOE_STAGE_FFN_UP, 2);
+    MOE_TRY(cuda_status(launch_decode_ffn(c, 0, x_perm, nullptr, offsets, *w, at<void>(ws, L.h),
+                                          y_perm, at<void>(ws, L.act16), status, s)));
+    stage(MOE_STAGE_FFN_DOWN, 1);
+    return cuda_status(launch_decode_ffn(c, 1, x_perm, nullptr, offsets, *w, at<void>(ws, L.h),
+                                         y_perm, at<void>(ws, L.act16), status, s));
+  }
   const int P = c.n * c.top_k;
   const int hdt = c.act_dtype == MOE_F32 ? MOE_F32 : MOE_BF16;
   GemmStage up{};
@@ -220,6 +230,7 @@ moe_status moe_workspace_layout_of(const moe_config *cfg, moe_workspace_layout *
   out->y_perm = L.y_perm;
   out->y_shared = L.y_shared;
   out->h_shared = L.h_shared;
+  out->act16 = L.act16;
   out->total = L.total;
   return MOE_OK;
 }
@@ -322,13 +333,26 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
   stage(MOE_STAGE_ROUTE, 2);
   MOE_TRY(cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits), topk_idx,
                                    gates, nullptr, status, s)));
-  stage(MOE_STAGE_DISPATCH, 2);
+  const bool decode = decode_supported(c);
+  stage(MOE_STAGE_DISPATCH, decode ? 1 : 2);
   MOE_TRY(cuda_status(launch_dispatch(P, c.n_experts, topk_idx, at<int32_t>(ws, L.counts), offsets,
                                       perm, inv_perm, status, s)));
-  MOE_TRY(cuda_status(launch_gather(x, perm, P, c.top_k, c.n, (int64_t)c.d * act_size(c),
-                                    at<void>(ws, L.x_perm), status, s)));
-  MOE_TRY(run_expert_ffn(c, at<void>(ws, L.x_perm), offsets, w, at<void>(ws, L.y_perm), ws, s,
-                         stage));
+  if (decode) {
+    // small batch: the FFN reads x rows through perm, no x_perm copy
+    stage(MOE_STAGE_FFN_UP, 2);
+    MOE_TRY(cuda_status(launch_decode_ffn(c, 0, x, perm, offsets, *w, at<void>(ws, L.h),
+                                          at<void>(ws, L.y_perm), at<void>(ws, L.act16), status,
+                                          s)));
+    stage(MOE_STAGE_FFN_DOWN, 1);
+    MOE_TRY(cuda_status(launch_decode_ffn(c, 1, x, perm, offsets, *w, at<void>(ws, L.h),
+                                          at<void>(ws, L.y_perm), at<void>(ws, L.act16), status,
+                                          s)));
+  } else {
+    MOE_TRY(cuda_status(launch_gather(x, perm, P, c.top_k, c.n, (int64_t)c.d * act_size(c),
+                                      at<void>(ws, L.x_perm), status, s)));
+    MOE_TRY(run_expert_ffn(c, at<void>(ws, L.x_perm), offsets, w, at<void>(ws, L.y_perm), ws, s,
+                           stage));
+  }
   const void *y_shared = nullptr;
   if (c.d_ff_shared) {
     stage(MOE_STAGE_SHARED, 2);

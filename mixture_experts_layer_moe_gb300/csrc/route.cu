@@ -17,9 +17,15 @@ namespace moe {
 namespace {
 
 constexpr int RT_M = 64, RT_E = 64, RT_K = 32, RT_THREADS = 256;
+// From this many tokens on, the bf16 router GEMM runs on the tensor cores
+// (fp32 accumulation in TMEM); smaller batches use the CUDA-core kernel.
+constexpr int kTensorCoreRouterMinTokens = 128;
+// Up to this many tokens, the bf16 router runs one warp per expert.
+constexpr int kSmallRouterMaxTokens = 96;
 
-// logits[t][e] = sum_i x[t][i] * Wg[e][i], each thread accumulating its 4x4
-// outputs sequentially in i with fp32 FMA, then + bias[e].
+// logits[t][e] = sum_i x[t][i] * Wg[e][i] (+ bias[e]): each 32-wide chunk of i
+// is summed with fp32 FMA into a fresh partial, and the partials are added up,
+// which keeps the rounding error of long rows (d in the thousands) near 1e-7.
 template <typename T>
 __global__ void __launch_bounds__(RT_THREADS)
 route_logits_kernel(const T *__restrict__ x, const T *__restrict__ Wg,
@@ -38,6 +44,7 @@ route_logits_kernel(const T *__restrict__ x, const T *__restrict__ Wg,
       gs[kk][r] = (ge < E && gk < d) ? Elem<T>::load(Wg + (size_t)ge * d + gk) : 0.f;
     }
     __syncthreads();
+    float part[4][4] = {};
 #pragma unroll 8
     for (int kk = 0; kk < RT_K; ++kk) {
       float a[4], b[4];
@@ -48,8 +55,12 @@ route_logits_kernel(const T *__restrict__ x, const T *__restrict__ Wg,
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < 4; ++j) part[i][j] = fmaf(a[i], b[j], part[i][j]);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] += part[i][j];
     __syncthreads();
   }
 #pragma unroll
@@ -62,6 +73,60 @@ route_logits_kernel(const T *__restrict__ x, const T *__restrict__ Wg,
       if (ge < E) logits[(size_t)gm * E + ge] = acc[i][j] + (bias ? bias[ge] : 0.f);
     }
   }
+}
+
+// Small batches (decode): one warp per expert, RS_TOK tokens per CTA row.
+// Lane l walks the row in 8-element pieces (l*8, l*8 + 256, ...); each piece
+// is a fresh fp32 partial added to the token's sum, and the 32 lane sums are
+// combined by a shuffle tree.  Wg is read once per token group.
+constexpr int RS_WARPS = 8, RS_TOK = 16, RS_MAXV = 12;   // d <= 32 * 8 * RS_MAXV = 3072
+
+// All of a lane's Wg pieces are loaded before any arithmetic, and a token's
+// pieces before its dot product, so a warp waits on about two memory
+// latencies instead of one per piece.
+__global__ void __launch_bounds__(32 * RS_WARPS)
+route_logits_small_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ Wg,
+                          const float *__restrict__ bias, float *__restrict__ logits, int n, int d,
+                          int E) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * RS_WARPS + warp;
+  const int t0 = blockIdx.y * RS_TOK;
+  if (e >= E) return;
+  const int nt = min(RS_TOK, n - t0);
+  const int nv = (d / 8 - lane + 31) / 32;          // pieces of this lane: k0 = (lane + 32 v) * 8
+  const __nv_bfloat16 *wrow = Wg + (size_t)e * d;
+  uint4 wv[RS_MAXV];
+#pragma unroll
+  for (int v = 0; v < RS_MAXV; ++v)
+    if (v < nv) wv[v] = *reinterpret_cast<const uint4 *>(wrow + (size_t)(lane + 32 * v) * 8);
+  float mine = 0.f;
+  for (int j = 0; j < nt; ++j) {
+    const __nv_bfloat16 *xrow = x + (size_t)(t0 + j) * d;
+    uint4 xv[RS_MAXV];
+#pragma unroll
+    for (int v = 0; v < RS_MAXV; ++v)
+      if (v < nv) xv[v] = *reinterpret_cast<const uint4 *>(xrow + (size_t)(lane + 32 * v) * 8);
+    float acc = 0.f;
+#pragma unroll
+    for (int v = 0; v < RS_MAXV; ++v) {
+      if (v < nv) {
+        const uint32_t ww[4] = {wv[v].x, wv[v].y, wv[v].z, wv[v].w};
+        const uint32_t xx[4] = {xv[v].x, xv[v].y, xv[v].z, xv[v].w};
+        float part = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          part = fmaf(__uint_as_float(ww[i] << 16), __uint_as_float(xx[i] << 16), part);
+          part = fmaf(__uint_as_float(ww[i] & 0xffff0000u), __uint_as_float(xx[i] & 0xffff0000u),
+                      part);
+        }
+        acc += part;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == j) mine = acc;
+  }
+  if (lane < nt) logits[(size_t)(t0 + lane) * E + e] = mine + (bias ? bias[e] : 0.f);
 }
 
 // One warp per token.  Lane l holds experts l, l+32, ... (E <= 256).
@@ -143,16 +208,38 @@ route_select_kernel(const float *__restrict__ logits, int n, int E, int k, int g
 cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, const float *bias,
                          float *logits, int32_t *topk_idx, float *topk_gate, float *probs,
                          int *status, cudaStream_t s) {
-  (void)status;
+  cudaError_t err = cudaSuccess;
+  GemmStage g{};
+  g.a_dtype = c.act_dtype;
+  g.b_dtype = c.act_dtype;
+  g.out_dtype = MOE_F32;
+  g.epi = 3;
+  g.A = x;
+  g.offsets = nullptr;
+  g.num_experts = 1;
+  g.rows = c.n;
+  g.N = c.n_experts;
+  g.K = c.d;
+  g.B = Wg;
+  g.out = logits;
+  g.col_bias = bias;
   dim3 grid((c.n + RT_M - 1) / RT_M, (c.n_experts + RT_E - 1) / RT_E);
-  if (c.act_dtype == MOE_F32)
+  if (c.n >= kTensorCoreRouterMinTokens && gemm_tc_supported(g))
+    err = launch_gemm_tc(g, status, s);
+  else if (c.act_dtype == MOE_BF16 && c.n <= kSmallRouterMaxTokens && c.d <= 32 * 8 * RS_MAXV)
+    route_logits_small_kernel<<<dim3((c.n_experts + RS_WARPS - 1) / RS_WARPS,
+                                     (c.n + RS_TOK - 1) / RS_TOK),
+                                32 * RS_WARPS, 0, s>>>((const __nv_bfloat16 *)x,
+                                                       (const __nv_bfloat16 *)Wg, bias, logits,
+                                                       c.n, c.d, c.n_experts);
+  else if (c.act_dtype == MOE_F32)
     route_logits_kernel<float><<<grid, RT_THREADS, 0, s>>>(
         (const float *)x, (const float *)Wg, bias, logits, c.n, c.d, c.n_experts);
   else
     route_logits_kernel<__nv_bfloat16><<<grid, RT_THREADS, 0, s>>>(
         (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)Wg, bias, logits, c.n, c.d,
         c.n_experts);
-  cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const int warps_per_block = 8;
   route_select_kernel<<<(c.n + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0,

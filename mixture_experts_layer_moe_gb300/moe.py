@@ -44,7 +44,7 @@ class moe_weights(ctypes.Structure):
 class moe_workspace_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("status", "logits", "topk_idx", "topk_gate", "counts", "offsets", "perm",
-                 "inv_perm", "x_perm", "h", "y_perm", "y_shared", "h_shared", "total")]
+                 "inv_perm", "x_perm", "h", "y_perm", "y_shared", "h_shared", "act16", "total")]
 
 
 def _load() -> ctypes.CDLL:

@@ -68,6 +68,7 @@ def run_forward(lib, cfg, inputs: dict):
         offsets=ws_view(ws, L, "offsets", torch.int32, cfg.E + 1).cpu(),
         perm=ws_view(ws, L, "perm", torch.int32, P).cpu(),
         inv_perm=ws_view(ws, L, "inv_perm", torch.int32, P).cpu(),
+        logits=ws_view(ws, L, "logits", torch.float32, cfg.n * cfg.E).view(cfg.n, cfg.E).cpu(),
     )
     return y, ws, L, inter
 
@@ -153,4 +154,6 @@ def full_parity(lib, cfg, seed=0, sample=None):
         tokens[-1] = cfg.n - 1
     res = O.forward(cfg, oin, tokens=tokens, routing=r2)
     err = check_output(cfg, y[tokens.cuda()], res["y"])
-    return dict(err=err, near_ties=listed, counts=inter["counts"], y=y, inputs=inputs, ws=ws)
+    logit_err = (inter["logits"].double() - r["logits"]).abs().max().item()
+    return dict(err=err, near_ties=listed, counts=inter["counts"], y=y, inputs=inputs, ws=ws,
+                logit_err=logit_err)

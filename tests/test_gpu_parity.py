@@ -36,6 +36,9 @@ SMALL = {
     "mixtral_k_eq_E": C["mixtral_bf16"].scaled(n=45, d=128, d_ff=192, E=5, k=5),
     "decode_n1": C["gptoss_decode_mxfp4"].scaled(n=1),
     "decode_n4": C["gptoss_decode_mxfp4"].scaled(n=4),
+    "decode_many_tokens_per_expert": C["gptoss_decode_mxfp4"].scaled(n=64, d=256, d_ff=320, E=4),
+    "decode_relu_small": C["gptoss_decode_mxfp4"].scaled(n=16, d=128, d_ff=192, E=8, k=2,
+                                                         act="relu"),
     "prefill_zipf_small": C["gptoss_prefill_zipf_mxfp4"].scaled(n=600, d=256, d_ff=320, E=16),
     "finegrained_small": C["finegrained_shared_bf16"].scaled(n=500, d=256, d_ff=128, E=32,
                                                              d_ff_shared=192),
@@ -66,7 +69,9 @@ def test_forward_full_size(lib, name):
     cfg, sample = FULL[name]
     res = parity.full_parity(lib, cfg, seed=0, sample=sample)
     counts = res["counts"]
-    print(f"{name}: err={res['err']:.3e} near_ties={res['near_ties']} "
+    assert res["logit_err"] < 5e-6, res["logit_err"]
+    print(f"{name}: err={res['err']:.3e} logit_err={res['logit_err']:.2e} "
+          f"near_ties={res['near_ties']} "
           f"empty_experts={(counts == 0).sum().item()} max_load={counts.max().item()}")
     del res
     torch.cuda.empty_cache()
@@ -235,7 +240,9 @@ def test_combine_bad_inverse_reported(lib):
 
 # -------------------------------------------------------------- expert FFN
 
-@pytest.mark.parametrize("name", ["tiny_switch_fp32", "mixtral_small", "prefill_zipf_small"])
+@pytest.mark.parametrize("name", ["tiny_switch_fp32", "mixtral_small", "prefill_zipf_small",
+                                  "decode_n4", "decode_many_tokens_per_expert",
+                                  "decode_relu_small"])
 def test_expert_ffn_segments(lib, name):
     cfg = SMALL[name]
     inputs = moe_synth.make_inputs(cfg, seed=8, device="cuda")
