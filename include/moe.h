@@ -59,7 +59,9 @@ typedef enum {
   MOE_ERR_WORKSPACE = 3,    /* ws_bytes smaller than moe_workspace_size() */
   MOE_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, attribute, ...) */
   MOE_ERR_BAD_INDEX = 5,    /* device: expert index >= E or < 0, or perm entry out of range */
-  MOE_ERR_TIMEOUT = 6       /* device: a bounded pipeline wait ran out */
+  MOE_ERR_TIMEOUT = 6,      /* device: a bounded pipeline wait ran out */
+  MOE_ERR_RANGE = 7         /* device: an MXFP4 block scale outside the range the
+                               tensor-core path applies exactly (E8M0 byte 113..142) */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_MXFP4 = 2 } moe_dtype;
@@ -117,13 +119,14 @@ typedef struct {
   size_t offsets;    /* int32 [E+1] */
   size_t perm;       /* int32 [n*K]: segment position -> pair t*K+j */
   size_t inv_perm;   /* int32 [n*K]: pair t*K+j -> segment position */
-  size_t x_perm;     /* act_dtype [n*K][d] (not written by the small-batch MXFP4 path) */
+  size_t x_perm;     /* act_dtype [n*K][d] (not written for MXFP4 layers, which
+                        stage f16 rows in act16 instead) */
   size_t h;          /* [n*K][d_ff]: bf16, or fp32 when act_dtype is F32 */
   size_t y_perm;     /* act_dtype [n*K][d], unweighted expert outputs */
   size_t y_shared;   /* act_dtype [n][d] shared-expert output, 0 if none */
   size_t h_shared;   /* [n][d_ff_shared] shared-expert intermediate, 0 if none */
-  size_t act16;      /* small-batch MXFP4 path: f16 copies of the expert-ordered
-                        activation rows [n*K][d] then of h [n*K][d_ff]; 0 if unused */
+  size_t act16;      /* MXFP4 layers: f16 copies of the expert-ordered activation
+                        rows [n*K][d] then of h [n*K][d_ff]; 0 for other layers */
   size_t total;      /* = moe_workspace_size() */
 } moe_workspace_layout;
 

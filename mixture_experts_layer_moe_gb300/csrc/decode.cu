@@ -369,10 +369,21 @@ bool decode_supported(const moe_config &c) {
          c.d_ff % 32 == 0 && (int64_t)c.n * c.top_k <= kDecodeMaxPairs;
 }
 
-size_t decode_act16_bytes(const moe_config &c) {
-  if (!decode_supported(c)) return 0;
+size_t mx_act16_bytes(const moe_config &c) {
+  if (c.weight_dtype != MOE_MXFP4 || c.act_dtype != MOE_BF16) return 0;
   const size_t P = (size_t)c.n * c.top_k;
   return P * (size_t)c.d * 2 + P * (size_t)c.d_ff * 2;
+}
+
+cudaError_t launch_rows_to_f16(const void *src, const int32_t *perm, int top_k, int P, int K,
+                               void *dst, int *status, cudaStream_t s) {
+  const int vec = P * (K / 8);
+  int blocks = (vec + 255) / 256;
+  if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
+  if (blocks < 1) blocks = 1;
+  rows_to_f16_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), perm, top_k,
+                                           P, K, static_cast<uint16_t *>(dst), status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
@@ -391,12 +402,7 @@ cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
   // more tokens: 64 rows per CTA, each staged B fragment serving more weights
   a.row_groups = c.n <= 2 ? 1 : 4;
   if (part == 0) {
-    const int vec = P * (c.d / 8);
-    int blocks = (vec + 255) / 256;
-    if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
-    rows_to_f16_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(act), perm,
-                                             c.top_k, P, c.d, x16, status);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_rows_to_f16(act, perm, c.top_k, P, c.d, x16, status, s);
     if (e != cudaSuccess) return e;
     a.act16 = x16;
     a.S = w.S1;

@@ -19,6 +19,16 @@
 // so CTAs working at the same time share one expert's weight columns and its
 // whole activation segment in L2.  The tile list is derived on the device
 // from the segment offsets; empty segments produce no tiles.
+//
+// MXFP4 weights (MX variant, feed post "What is MXFP4?"; OCP MX v1.0 E2M1
+// codes with one E8M0 scale per 32 elements): TMA brings the packed codes of
+// the B rows (32 bytes per row per k-block) next to the A tile, and four
+// transform warps (6-9) write the dequantised B tile into the 128-byte-swizzled
+// K-major layout the MMA reads: cvt.rn.f16x2.e2m1x2 on each code pair, times
+// the block scale as an f16 pair.  The MMA then runs kind::f16 on f16 operands
+// (the activations come as exact f16 copies of the bf16 rows).  A block scale
+// whose value is outside f16's normal range (E8M0 byte outside 113..142)
+// cannot be applied exactly and is reported as MOE_ERR_RANGE.
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -32,8 +42,18 @@ constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int DYN_SMEM = STAGES * STAGE_BYTES + 1024;
+// MX variant: 3 stages of [A 16 KB][B 32 KB][codes 8 KB], two scale buffers
+constexpr int MX_STAGES = 3;
+constexpr int MX_THREADS = 320;
+constexpr int CODE_BYTES = BN * BK / 2;
+constexpr int MX_STAGE_BYTES = A_BYTES + B_BYTES + CODE_BYTES;
 constexpr int MAX_E = 256;
 constexpr uint32_t TMEM_COLS = 512;
+
+__host__ __device__ inline size_t mx_scale_buf_bytes(int K) { return (size_t)BN * (K / 32); }
+size_t mx_dyn_smem(int K) {
+  return 1024 + (size_t)MX_STAGES * MX_STAGE_BYTES + 2 * ((mx_scale_buf_bytes(K) + 15) & ~15);
+}
 
 struct TcArgs {
   const int32_t *offsets;  // nullptr: one segment [0, rows) of expert 0
@@ -44,11 +64,15 @@ struct TcArgs {
   void *out;       // bf16 [rows][N], fp32 for EPI 3
   const float *bias;
   int *status;
+  // MX variant
+  const uint8_t *S, *S3;   // E8M0 scales [E][N][K/32] of B (and B3)
+  uint16_t *out16;         // f16 copy of out, or nullptr
 };
 
 struct TcShared {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
+  uint64_t bready[STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -88,6 +112,42 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t d;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(d)
+      : "r"(byte));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// E8M0 byte -> 2^(s-127) as an f16 pair; 0 (and *bad set) outside f16's normal range.
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t s, bool &bad) {
+  if (s < 113u || s > 142u) {
+    bad = true;
+    return 0u;
+  }
+  const uint32_t h = (s - 112u) << 10;
+  return h | (h << 16);
+}
+
+__device__ __forceinline__ uint32_t f16x2_from_bf16x2(uint32_t b) {
+  const float lo = fminf(fmaxf(__uint_as_float(b << 16), -65504.f), 65504.f);
+  const float hi = fminf(fmaxf(__uint_as_float(b & 0xffff0000u), -65504.f), 65504.f);
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
 // EPI: 0 plain, 1 relu, 2 swiglu (B = W1 rows, B3 = W3 rows, 128 each),
 // 3 fp32 output + per-column bias (router logits).
 //
@@ -97,14 +157,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // registers with round-to-nearest.  Accumulating the whole reduction in TMEM
 // instead drifted by ~2e-5 on d = 4096 rows, too close to the 1e-5 near-tie
 // margin of the routing decision.
-template <int EPI>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int EPI, bool MX>
+__global__ void __launch_bounds__(MX ? MX_THREADS : THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmB3, TcArgs args) {
   constexpr bool KPART = (EPI == 3);                 // per-k-block partials
   constexpr int BNT = KPART ? 128 : BN;              // MMA N = B rows per stage
   constexpr int N_OUT = (EPI == 2) ? BN / 2 : BNT;   // output columns per tile
-  constexpr uint32_t TX_BYTES = A_BYTES + BNT * BK * 2;
+  constexpr int NSTAGE = MX ? MX_STAGES : STAGES;
+  constexpr int SBYTES = MX ? MX_STAGE_BYTES : STAGE_BYTES;
+  constexpr int NTHREADS = MX ? MX_THREADS : THREADS;
+  constexpr uint32_t TX_BYTES = MX ? (A_BYTES + CODE_BYTES) : (A_BYTES + BNT * BK * 2);
   extern __shared__ uint8_t dyn_smem[];
   __shared__ TcShared sh;
   uint8_t *smem = dyn_smem + ((1024 - (tc::smem_u32(dyn_smem) & 1023)) & 1023);
@@ -117,13 +180,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     sh.failed_on_entry = status_failed(args.status) ? 1 : 0;
     sh.abort = sh.failed_on_entry;
   }
-  for (int i = threadIdx.x; i <= E; i += THREADS)
+  for (int i = threadIdx.x; i <= E; i += NTHREADS)
     sh.offs[i] = args.offsets ? args.offsets[i] : (i == 0 ? 0 : args.rows);
   if (warp == 1) tc::tmem_alloc(&sh.tmem_base, TMEM_COLS);
   if (threadIdx.x == 32) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NSTAGE; ++s) {
       tc::mbar_init(&sh.full[s], 1);
       tc::mbar_init(&sh.empty[s], 1);
+      tc::mbar_init(&sh.bready[s], 128);
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&sh.tfull[a], 1);
@@ -191,23 +255,32 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int wrow = tl.n_idx * N_OUT;
         for (int kb = 0; kb < KB; ++kb) {
           if (!tc::mbar_wait(&sh.empty[stage], phase ^ 1u, abort)) break;
-          uint8_t *sa = smem + stage * STAGE_BYTES;
+          uint8_t *sa = smem + stage * SBYTES;
           uint8_t *sb = sa + A_BYTES;
           tc::mbar_arrive_expect_tx(&sh.full[stage], TX_BYTES);
           tc::tma_load_2d(&tmA, &sh.full[stage], sa, kb * BK, tl.row0);
-          if (EPI == 2) {
+          if constexpr (MX) {
+            uint8_t *sc = sb + B_BYTES;
+            if (EPI == 2) {
+              tc::tma_load_3d(&tmB, &sh.full[stage], sc, kb * (BK / 2), wrow, tl.e);
+              tc::tma_load_3d(&tmB3, &sh.full[stage], sc + CODE_BYTES / 2, kb * (BK / 2), wrow,
+                              tl.e);
+            } else {
+              tc::tma_load_3d(&tmB, &sh.full[stage], sc, kb * (BK / 2), wrow, tl.e);
+            }
+          } else if (EPI == 2) {
             tc::tma_load_3d(&tmB, &sh.full[stage], sb, kb * BK, wrow, tl.e);
             tc::tma_load_3d(&tmB3, &sh.full[stage], sb + B_BYTES / 2, kb * BK, wrow, tl.e);
           } else {
             tc::tma_load_3d(&tmB, &sh.full[stage], sb, kb * BK, wrow, tl.e);
           }
           last_phase[stage] = (int)phase;
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
         }
       }
       if (*abort) {
         // let the copies this thread issued land before the CTA exits
-        for (int s = 0; s < STAGES; ++s)
+        for (int s = 0; s < NSTAGE; ++s)
           if (last_phase[s] >= 0)
             tc::mbar_wait_drain(&sh.full[s], (uint32_t)last_phase[s], 100000000ull);
       }
@@ -215,7 +288,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BNT);
+      constexpr uint32_t idesc = MX ? tc::idesc_f16_f32(BM, BNT) : tc::idesc_bf16_f32(BM, BNT);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;   // accumulator uses so far (tiles, or k-blocks with KPART)
@@ -231,15 +304,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
           if (!tc::mbar_wait(&sh.full[stage], phase, abort)) { ok = false; break; }
+          if (MX && !tc::mbar_wait(&sh.bready[stage], phase, abort)) { ok = false; break; }
           tc::tc_fence_after();
-          const uint32_t sa = tc::smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t sa = tc::smem_u32(smem + stage * SBYTES);
           const uint32_t sb = sa + A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             tc::mma_bf16(d_tmem, tc::smem_desc_sw128(sa + k * 32), tc::smem_desc_sw128(sb + k * 32),
                          idesc, (k != 0 || (!KPART && kb != 0)) ? 1u : 0u);
           tc::mma_commit(&sh.empty[stage]);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
           if (KPART || kb == KB - 1) {
             tc::mma_commit(&sh.tfull[acc]);
             ++local;
@@ -251,7 +325,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tc::mbar_wait_drain(&sh.drain, 0, 100000000ull);
       }
     }
-  } else {
+  } else if (warp < 6) {
     // ---------------- epilogue: warps 2..5; warp w reads TMEM lanes 32*(w%4)..
     const int quarter = warp & 3;
     const int r_local = quarter * 32 + lane;
@@ -304,6 +378,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int row = tl.row0 + r_local;
         const bool row_ok = row < tl.seg_end;
         __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(args.out) + (size_t)row * args.N;
+        uint16_t *orow16 = args.out16 ? args.out16 + (size_t)row * args.N : nullptr;
         constexpr int CHUNKS = N_OUT / 32;
 #pragma unroll 1
         for (int c = 0; c < CHUNKS; ++c) {
@@ -333,15 +408,109 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              if (col0 + v * 8 < args.N)
+              if (col0 + v * 8 < args.N) {
                 *reinterpret_cast<uint4 *>(orow + col0 + v * 8) = make_uint4(
                     packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                if (orow16)
+                  *reinterpret_cast<uint4 *>(orow16 + col0 + v * 8) = make_uint4(
+                      f16x2_from_bf16x2(packed[4 * v]), f16x2_from_bf16x2(packed[4 * v + 1]),
+                      f16x2_from_bf16x2(packed[4 * v + 2]), f16x2_from_bf16x2(packed[4 * v + 3]));
+              }
             }
           }
           __syncwarp();
         }
       }
     }
+  } else if constexpr (MX) {
+    // ---------------- transform: warps 6..9 dequantise the B tile of each stage.
+    // Thread tt owns B rows tt and tt + 128.  Scales of a tile's 256 rows are
+    // copied (cp.async) into one of two buffers while the previous tile runs.
+    const int tt = threadIdx.x - 192;
+    const int KBLK = args.K / 32;
+    const size_t sbuf = mx_scale_buf_bytes(args.K);
+    const size_t spitch = (sbuf + 15) & ~(size_t)15;
+    uint8_t *scale_buf[2] = {smem + (size_t)MX_STAGES * MX_STAGE_BYTES,
+                             smem + (size_t)MX_STAGES * MX_STAGE_BYTES + spitch};
+    // scales of tile t's rows -> buffer b (rows past N are left unset: their
+    // codes are zero-filled by TMA and their columns are never stored)
+    auto fetch_scales = [&](int t, int b) {
+      const Tile tl = decode_tile(sh, E, t);
+      const int wrow = tl.n_idx * N_OUT;
+      const int nmat = (EPI == 2) ? 2 : 1;
+      const int rows_per = BN / nmat;
+      for (int m = 0; m < nmat; ++m) {
+        const uint8_t *S = m == 0 ? args.S : args.S3;
+        const int rows = min(rows_per, args.N - wrow);
+        const size_t bytes = (size_t)rows * KBLK;           // a multiple of 16
+        const uint8_t *src = S + ((size_t)tl.e * args.N + wrow) * KBLK;
+        uint8_t *dst = scale_buf[b] + (size_t)m * rows_per * KBLK;
+        for (size_t o = (size_t)tt * 16; o < bytes; o += 128 * 16) cp_async16(dst + o, src + o);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    int stage = 0;
+    uint32_t phase = 0;
+    int buf = 0;
+    bool bad_scale = false;
+    if (blockIdx.x < num_tiles) fetch_scales(blockIdx.x, 0);
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, buf ^= 1) {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      // this tile's scales are in; the four transform warps also agree here on
+      // stopping (a warp whose wait ran out has raised *abort)
+      uint32_t stop;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+          "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+          : "=r"(stop)
+          : "r"((uint32_t)*abort)
+          : "memory");
+      if (stop) break;
+      if (t + (int)gridDim.x < num_tiles) fetch_scales(t + gridDim.x, buf ^ 1);
+      const uint8_t *scl = scale_buf[buf];
+      const int wrow = decode_tile(sh, E, t).n_idx * N_OUT;
+      const int rows_per = (EPI == 2) ? BN / 2 : BN;
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        ok = tc::mbar_wait(&sh.full[stage], phase, abort);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const uint8_t *codes = smem + stage * SBYTES + A_BYTES + B_BYTES;
+        uint8_t *btile = smem + stage * SBYTES + A_BYTES;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = tt + 128 * h;                      // B row in the tile
+          uint8_t *brow = btile + (r >> 3) * 1024 + (r & 7) * 128;
+          if (wrow + (r % rows_per) >= args.N) {           // past the matrix: zero row
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4 *>(brow + (j << 4)) = make_uint4(0u, 0u, 0u, 0u);
+            continue;
+          }
+          const uint4 c0 = *reinterpret_cast<const uint4 *>(codes + r * 32);
+          const uint4 c1 = *reinterpret_cast<const uint4 *>(codes + r * 32 + 16);
+          const uint8_t *srow = scl + (size_t)r * KBLK;
+          const uint32_t s0 = 2 * kb < KBLK ? srow[2 * kb] : 127u;
+          const uint32_t s1 = 2 * kb + 1 < KBLK ? srow[2 * kb + 1] : 127u;
+          const uint32_t f0 = scale_f16x2(s0, bad_scale), f1 = scale_f16x2(s1, bad_scale);
+          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t w = words[j], f = j < 4 ? f0 : f1;
+            const uint4 v = make_uint4(hmul2(e2m1x2_to_f16x2(w), f), hmul2(e2m1x2_to_f16x2(w >> 8), f),
+                                       hmul2(e2m1x2_to_f16x2(w >> 16), f),
+                                       hmul2(e2m1x2_to_f16x2(w >> 24), f));
+            *reinterpret_cast<uint4 *>(brow + ((j ^ (r & 7)) << 4)) = v;
+          }
+        }
+        // generic-proxy writes of the B tile -> visible to the tensor core
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc::mbar_arrive(&sh.bready[stage]);
+        if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
+      }
+      (void)ok;   // a failed wait raised *abort: the next tile's barrier stops all four warps
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (bad_scale) set_status(args.status, MOE_ERR_RANGE, 0);
   }
 
   __syncwarp();
@@ -357,38 +526,53 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
 // ---------------------------------------------------------------- host side
 
-// bf16 tensor map, innermost dimension first; box inner extent 64 elements
-// (128 bytes, one swizzle row).
-bool make_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
-              const uint32_t *box) {
-  return make_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rank, dims, box,
-                         CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
-template <int EPI>
+template <int EPI, bool MX>
 cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, DYN_SMEM);
+  const size_t smem = MX ? mx_dyn_smem(g.K) : (size_t)DYN_SMEM;
+  static size_t smem_set = 0;
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, MX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    smem_set = smem;
   }
   const int E = g.offsets ? g.num_experts : 1;
   CUtensorMap mA, mB, mB3;
   const uint64_t dA[2] = {(uint64_t)g.K, (uint64_t)g.rows};
   const uint32_t bA[2] = {BK, BM};
   const int wrows = (EPI == 2) ? BN / 2 : (EPI == 3 ? 128 : BN);
-  const uint64_t dB[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)E};
-  const uint32_t bB[3] = {BK, (uint32_t)wrows, 1};
-  if (!make_map(&mA, g.A, 2, dA, bA) || !make_map(&mB, g.B, 3, dB, bB))
+  const CUtensorMapDataType adt = MX ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_tensor_map(&mA, adt, 2, g.A, 2, dA, bA, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if (EPI == 2) {
-    if (!make_map(&mB3, g.B3, 3, dB, bB)) return cudaErrorInvalidValue;
+  if (MX) {
+    // packed codes: [E][N][K/2] bytes, boxes of 32 bytes (one k-block) x wrows rows
+    const uint64_t dC[3] = {(uint64_t)g.K / 2, (uint64_t)g.N, (uint64_t)E};
+    const uint32_t bC[3] = {BK / 2, (uint32_t)wrows, 1};
+    if (!make_tensor_map(&mB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.B, 3, dC, bC,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    if (EPI == 2) {
+      if (!make_tensor_map(&mB3, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.B3, 3, dC, bC,
+                           CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    } else {
+      mB3 = mB;
+    }
   } else {
-    mB3 = mB;
+    const uint64_t dB[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)E};
+    const uint32_t bB[3] = {BK, (uint32_t)wrows, 1};
+    if (!make_tensor_map(&mB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.B, 3, dB, bB,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    if (EPI == 2) {
+      if (!make_tensor_map(&mB3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.B3, 3, dB, bB,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    } else {
+      mB3 = mB;
+    }
   }
-  TcArgs a;
+  TcArgs a{};
   a.offsets = g.offsets;
   a.num_experts = g.num_experts;
   a.rows = g.rows;
@@ -397,25 +581,35 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
   a.out = g.out;
   a.bias = g.col_bias;
   a.status = status;
-  gemm_tc_kernel<EPI><<<num_sms(), THREADS, DYN_SMEM, s>>>(mA, mB, mB3, a);
+  a.S = g.SB;
+  a.S3 = g.SB3;
+  a.out16 = static_cast<uint16_t *>(g.out16);
+  gemm_tc_kernel<EPI, MX><<<num_sms(), MX ? MX_THREADS : THREADS, smem, s>>>(mA, mB, mB3, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool gemm_tc_supported(const GemmStage &g) {
+  if (g.rows <= 0 || !tensor_maps_available()) return false;
+  if (g.b_dtype == MOE_MXFP4) {
+    // f16 activations, MXFP4 weights; all scale buffers must fit in shared memory
+    return g.a_dtype == kF16 && g.out_dtype == MOE_BF16 && (g.epi == 0 || g.epi == 2) &&
+           g.K % 64 == 0 && g.N % 32 == 0 && mx_dyn_smem(g.K) + sizeof(TcShared) <= 227 * 1024;
+  }
   const bool out_ok = g.epi == 3 ? g.out_dtype == MOE_F32 : g.out_dtype == MOE_BF16;
   const bool n_ok = g.epi == 3 ? true : g.N % 8 == 0;
-  return g.a_dtype == MOE_BF16 && g.b_dtype == MOE_BF16 && out_ok && n_ok && g.K % 8 == 0 &&
-         g.rows > 0 && tensor_maps_available();
+  return g.a_dtype == MOE_BF16 && g.b_dtype == MOE_BF16 && out_ok && n_ok && g.K % 8 == 0;
 }
 
 cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s) {
+  if (g.b_dtype == MOE_MXFP4) return g.epi == 2 ? launch_epi<2, true>(g, status, s)
+                                                : launch_epi<0, true>(g, status, s);
   switch (g.epi) {
-    case 0: return launch_epi<0>(g, status, s);
-    case 1: return launch_epi<1>(g, status, s);
-    case 2: return launch_epi<2>(g, status, s);
-    default: return launch_epi<3>(g, status, s);
+    case 0: return launch_epi<0, false>(g, status, s);
+    case 1: return launch_epi<1, false>(g, status, s);
+    case 2: return launch_epi<2, false>(g, status, s);
+    default: return launch_epi<3, false>(g, status, s);
   }
 }
 

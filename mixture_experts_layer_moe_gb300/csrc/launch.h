@@ -41,8 +41,11 @@ cudaError_t launch_combine(int act_dtype, const void *y_perm, const int32_t *inv
 // epi: 0 = none, 1 = relu, 2 = swiglu (B3 gives the linear branch),
 //      3 = fp32 output + col_bias[j] (router logits; tensor-core path only).
 // offsets == nullptr means one segment [0, rows) using expert 0.
+// Internal element type: f16 activation copies feeding the MXFP4 tensor-core path.
+constexpr int kF16 = 3;
+
 struct GemmStage {
-  int a_dtype;          // MOE_F32 / MOE_BF16
+  int a_dtype;          // MOE_F32 / MOE_BF16 / kF16
   int b_dtype;          // MOE_F32 / MOE_BF16 / MOE_MXFP4
   int out_dtype;        // MOE_F32 / MOE_BF16
   int epi;
@@ -57,6 +60,7 @@ struct GemmStage {
   const uint8_t *SB3;
   void *out;            // [rows][N]
   const float *col_bias; // epi 3: per-column bias or nullptr
+  void *out16;          // MXFP4 path: f16 copy of out (next projection's input) or nullptr
 };
 cudaError_t launch_gemm_simt(const GemmStage &g, int *status, cudaStream_t s);
 
@@ -76,10 +80,15 @@ inline cudaError_t launch_gemm(const GemmStage &g, int *status, cudaStream_t s) 
 // rows in segment order (x [n][d] gathered through perm, or x_perm [P][d] when
 // perm is nullptr) into act16, then up + activation -> h [P][d_ff] (bf16, and
 // an f16 copy in act16).  part 1: down -> y_perm [P][d].  act16 is workspace
-// of decode_act16_bytes(c).
+// of mx_act16_bytes(c).
 constexpr int kDecodeMaxPairs = 256;
 bool decode_supported(const moe_config &c);
-size_t decode_act16_bytes(const moe_config &c);
+// Workspace for f16 copies of the activation rows ([P][d] then [P][d_ff]) used
+// by both MXFP4 paths; 0 for other configurations.
+size_t mx_act16_bytes(const moe_config &c);
+// dst[q] = f16(src[perm[q] / top_k]) (perm given) or f16(src[q]); rows of K.
+cudaError_t launch_rows_to_f16(const void *src, const int32_t *perm, int top_k, int P, int K,
+                               void *dst, int *status, cudaStream_t s);
 cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
                               const int32_t *perm, const int32_t *offsets, const moe_weights &w,
                               void *h, void *y_perm, void *act16, int *status, cudaStream_t s);

@@ -93,7 +93,7 @@ Layout layout_of(const moe_config &c) {
   L.y_perm = take(P * c.d * act_size(c));
   L.y_shared = c.d_ff_shared ? take(n * c.d * act_size(c)) : 0;
   L.h_shared = c.d_ff_shared ? take(n * c.d_ff_shared * h_size(c)) : 0;
-  const size_t a16 = decode_act16_bytes(c);
+  const size_t a16 = mx_act16_bytes(c);
   L.act16 = a16 ? take(a16) : 0;
   L.total = off;
   return L;
@@ -118,6 +118,71 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
     if (_st != MOE_OK) return _st;      \
   } while (0)
 
+// The two GEMM stages of the MXFP4 tensor-core path (f16 activations).
+void mx_stages(const moe_config &c, const int32_t *offsets, const moe_weights *w, void *ws,
+               void *y_perm, GemmStage &up, GemmStage &dn) {
+  const Layout L = layout_of(c);
+  const int P = c.n * c.top_k;
+  uint16_t *x16 = at<uint16_t>(ws, L.act16);
+  uint16_t *h16 = x16 + (size_t)P * c.d;
+  up = GemmStage{};
+  up.a_dtype = kF16;
+  up.b_dtype = MOE_MXFP4;
+  up.out_dtype = MOE_BF16;
+  up.epi = c.act == MOE_ACT_RELU ? 1 : 2;
+  up.A = x16;
+  up.offsets = offsets;
+  up.num_experts = c.n_experts;
+  up.rows = P;
+  up.N = c.d_ff;
+  up.K = c.d;
+  up.B = w->W1;
+  up.SB = w->S1;
+  up.B3 = w->W3;
+  up.SB3 = w->S3;
+  up.out = at<void>(ws, L.h);
+  up.out16 = h16;
+  dn = up;
+  dn.epi = 0;
+  dn.A = h16;
+  dn.N = c.d;
+  dn.K = c.d_ff;
+  dn.B = w->W2;
+  dn.SB = w->S2;
+  dn.B3 = nullptr;
+  dn.SB3 = nullptr;
+  dn.out = y_perm;
+  dn.out16 = nullptr;
+}
+
+bool mx_tc_path(const moe_config &c) {
+  if (c.weight_dtype != MOE_MXFP4 || c.act_dtype != MOE_BF16 || decode_supported(c)) return false;
+  moe_weights w{};
+  GemmStage up, dn;
+  mx_stages(c, nullptr, &w, nullptr, nullptr, up, dn);
+  up.offsets = dn.offsets = reinterpret_cast<const int32_t *>(16);   // shape check only
+  return gemm_tc_supported(up) && gemm_tc_supported(dn);
+}
+
+// MXFP4 prefill on tensor cores: f16 copies of the expert-ordered rows (x
+// through perm, or x_perm), then the up and down grouped GEMMs with on-the-fly
+// dequantisation.
+template <typename StageFn>
+moe_status run_mx_ffn(const moe_config &c, const void *act, const int32_t *perm,
+                      const int32_t *offsets, const moe_weights *w, void *y_perm, void *ws,
+                      cudaStream_t s, StageFn &&stage) {
+  const Layout L = layout_of(c);
+  int *status = at<int>(ws, L.status);
+  GemmStage up, dn;
+  mx_stages(c, offsets, w, ws, y_perm, up, dn);
+  stage(MOE_STAGE_FFN_UP, 2);
+  MOE_TRY(cuda_status(launch_rows_to_f16(act, perm, c.top_k, c.n * c.top_k, c.d,
+                                         at<void>(ws, L.act16), status, s)));
+  MOE_TRY(cuda_status(launch_gemm_tc(up, status, s)));
+  stage(MOE_STAGE_FFN_DOWN, 1);
+  return cuda_status(launch_gemm_tc(dn, status, s));
+}
+
 template <typename StageFn>
 moe_status run_expert_ffn(const moe_config &c, const void *x_perm, const int32_t *offsets,
                           const moe_weights *w, void *y_perm, void *ws, cudaStream_t s,
@@ -132,6 +197,7 @@ moe_status run_expert_ffn(const moe_config &c, const void *x_perm, const int32_t
     return cuda_status(launch_decode_ffn(c, 1, x_perm, nullptr, offsets, *w, at<void>(ws, L.h),
                                          y_perm, at<void>(ws, L.act16), status, s));
   }
+  if (mx_tc_path(c)) return run_mx_ffn(c, x_perm, nullptr, offsets, w, y_perm, ws, s, stage);
   const int P = c.n * c.top_k;
   const int hdt = c.act_dtype == MOE_F32 ? MOE_F32 : MOE_BF16;
   GemmStage up{};
@@ -334,7 +400,8 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
   MOE_TRY(cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits), topk_idx,
                                    gates, nullptr, status, s)));
   const bool decode = decode_supported(c);
-  stage(MOE_STAGE_DISPATCH, decode ? 1 : 2);
+  const bool mx_tc = mx_tc_path(c);
+  stage(MOE_STAGE_DISPATCH, (decode || mx_tc) ? 1 : 2);
   MOE_TRY(cuda_status(launch_dispatch(P, c.n_experts, topk_idx, at<int32_t>(ws, L.counts), offsets,
                                       perm, inv_perm, status, s)));
   if (decode) {
@@ -347,6 +414,9 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
     MOE_TRY(cuda_status(launch_decode_ffn(c, 1, x, perm, offsets, *w, at<void>(ws, L.h),
                                           at<void>(ws, L.y_perm), at<void>(ws, L.act16), status,
                                           s)));
+  } else if (mx_tc) {
+    // prefill over MXFP4 weights: the f16 staging gathers the rows itself
+    MOE_TRY(run_mx_ffn(c, x, perm, offsets, w, at<void>(ws, L.y_perm), ws, s, stage));
   } else {
     MOE_TRY(cuda_status(launch_gather(x, perm, P, c.top_k, c.n, (int64_t)c.d * act_size(c),
                                       at<void>(ws, L.x_perm), status, s)));
@@ -395,6 +465,7 @@ const char *moe_status_string(moe_status s) {
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA runtime error";
     case MOE_ERR_BAD_INDEX: return "MOE_ERR_BAD_INDEX: index out of range on the device";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: device pipeline wait ran out";
+    case MOE_ERR_RANGE: return "MOE_ERR_RANGE: MXFP4 block scale outside the exact range";
   }
   return "unknown moe_status";
 }
