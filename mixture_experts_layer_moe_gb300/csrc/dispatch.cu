@@ -119,22 +119,20 @@ dispatch_kernel(const int32_t *__restrict__ topk_idx, int P, int E, int32_t *__r
   }
 }
 
-// x_perm[q] = x[perm[q] / k], 16-byte vectors.  perm entries outside [0, P)
-// are reported and their row is zero-filled.
-__global__ void gather_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ perm,
-                              int P, int k, int n, int64_t vec_per_row,
-                              uint4 *__restrict__ x_perm, int *status) {
-  const int64_t total = (int64_t)P * vec_per_row;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t q = i / vec_per_row, v = i - q * vec_per_row;
+// x_perm[q] = x[perm[q] / k], 16-byte vectors; one row per CTA iteration so
+// the source row is resolved once per row.  perm entries outside [0, P) are
+// reported and their row is zero-filled.
+__global__ void __launch_bounds__(256)
+gather_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ perm, int P, int k, int n,
+              int vec_per_row, uint4 *__restrict__ x_perm, int *status) {
+  for (int q = blockIdx.x; q < P; q += gridDim.x) {
     const int p = perm[q];
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (p >= 0 && p < P && p / k < n)
-      val = x[(int64_t)(p / k) * vec_per_row + v];
-    else if (v == 0)
-      set_status(status, MOE_ERR_BAD_INDEX, (int)q);
-    x_perm[i] = val;
+    const bool ok = p >= 0 && p < P && p / k < n;
+    if (!ok && threadIdx.x == 0) set_status(status, MOE_ERR_BAD_INDEX, q);
+    const uint4 *src = x + (int64_t)(ok ? p / k : 0) * vec_per_row;
+    uint4 *dst = x_perm + (int64_t)q * vec_per_row;
+    for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x)
+      dst[v] = ok ? src[v] : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -156,13 +154,11 @@ cudaError_t launch_dispatch(int P, int E, const int32_t *topk_idx, int32_t *coun
 
 cudaError_t launch_gather(const void *x, const int32_t *perm, int P, int k, int n,
                           int64_t row_bytes, void *x_perm, int *status, cudaStream_t s) {
-  const int64_t vpr = row_bytes / 16;
-  const int64_t total = (int64_t)P * vpr;
-  int64_t blocks = (total + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  const int vpr = (int)(row_bytes / 16);
+  int blocks = P < 152 * 16 ? P : 152 * 16;
   if (blocks < 1) blocks = 1;
-  gather_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint4 *)x, perm, P, k, n, vpr,
-                                                 (uint4 *)x_perm, status);
+  gather_kernel<<<blocks, 256, 0, s>>>((const uint4 *)x, perm, P, k, n, vpr, (uint4 *)x_perm,
+                                       status);
   return cudaGetLastError();
 }
 

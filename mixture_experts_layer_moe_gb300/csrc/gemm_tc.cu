@@ -23,7 +23,7 @@
 // MXFP4 weights (MX variant, feed post "What is MXFP4?"; OCP MX v1.0 E2M1
 // codes with one E8M0 scale per 32 elements): TMA brings the packed codes of
 // the B rows (32 bytes per row per k-block) next to the A tile, and four
-// transform warps (6-9) write the dequantised B tile into the 128-byte-swizzled
+// transform warps (6-13) write the dequantised B tile into the 128-byte-swizzled
 // K-major layout the MMA reads: cvt.rn.f16x2.e2m1x2 on each code pair, times
 // the block scale as an f16 pair.  The MMA then runs kind::f16 on f16 operands
 // (the activations come as exact f16 copies of the bf16 rows).  A block scale
@@ -44,7 +44,8 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int DYN_SMEM = STAGES * STAGE_BYTES + 1024;
 // MX variant: 3 stages of [A 16 KB][B 32 KB][codes 8 KB], two scale buffers
 constexpr int MX_STAGES = 3;
-constexpr int MX_THREADS = 320;
+constexpr int MX_XWARPS = 8;                       // transform warps (one B row per thread)
+constexpr int MX_THREADS = 192 + 32 * MX_XWARPS;
 constexpr int CODE_BYTES = BN * BK / 2;
 constexpr int MX_STAGE_BYTES = A_BYTES + B_BYTES + CODE_BYTES;
 constexpr int MAX_E = 256;
@@ -187,7 +188,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int s = 0; s < NSTAGE; ++s) {
       tc::mbar_init(&sh.full[s], 1);
       tc::mbar_init(&sh.empty[s], 1);
-      tc::mbar_init(&sh.bready[s], 128);
+      tc::mbar_init(&sh.bready[s], 32 * MX_XWARPS);
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&sh.tfull[a], 1);
@@ -423,10 +424,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
     }
   } else if constexpr (MX) {
-    // ---------------- transform: warps 6..9 dequantise the B tile of each stage.
-    // Thread tt owns B rows tt and tt + 128.  Scales of a tile's 256 rows are
-    // copied (cp.async) into one of two buffers while the previous tile runs.
+    // ---------------- transform: warps 6..13 dequantise the B tile of each
+    // stage, thread tt owning B row tt.  Scales of a tile's 256 rows are copied
+    // (cp.async) into one of two buffers while the previous tile runs.  The
+    // codes arrive with a 32-byte swizzle: 16-byte half c of row r sits at
+    // c ^ ((r >> 2) & 1), which keeps the warp's row reads conflict-free.
     const int tt = threadIdx.x - 192;
+    constexpr int XT = 32 * MX_XWARPS;
     const int KBLK = args.K / 32;
     const size_t sbuf = mx_scale_buf_bytes(args.K);
     const size_t spitch = (sbuf + 15) & ~(size_t)15;
@@ -445,7 +449,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const size_t bytes = (size_t)rows * KBLK;           // a multiple of 16
         const uint8_t *src = S + ((size_t)tl.e * args.N + wrow) * KBLK;
         uint8_t *dst = scale_buf[b] + (size_t)m * rows_per * KBLK;
-        for (size_t o = (size_t)tt * 16; o < bytes; o += 128 * 16) cp_async16(dst + o, src + o);
+        for (size_t o = (size_t)tt * 16; o < bytes; o += XT * 16) cp_async16(dst + o, src + o);
       }
       asm volatile("cp.async.commit_group;" ::: "memory");
     };
@@ -453,42 +457,34 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint32_t phase = 0;
     int buf = 0;
     bool bad_scale = false;
+    const int r = tt;                                         // B row in the tile
+    const int rows_per = (EPI == 2) ? BN / 2 : BN;
+    const int sw = ((r >> 2) & 1) << 4;
     if (blockIdx.x < num_tiles) fetch_scales(blockIdx.x, 0);
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, buf ^= 1) {
       asm volatile("cp.async.wait_group 0;" ::: "memory");
-      // this tile's scales are in; the four transform warps also agree here on
+      // this tile's scales are in; the transform warps also agree here on
       // stopping (a warp whose wait ran out has raised *abort)
       uint32_t stop;
       asm volatile(
           "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-          "bar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+          "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
           : "=r"(stop)
-          : "r"((uint32_t)*abort)
+          : "r"((uint32_t)*abort), "n"(XT)
           : "memory");
       if (stop) break;
       if (t + (int)gridDim.x < num_tiles) fetch_scales(t + gridDim.x, buf ^ 1);
-      const uint8_t *scl = scale_buf[buf];
+      const uint8_t *srow = scale_buf[buf] + (size_t)r * KBLK;
       const int wrow = decode_tile(sh, E, t).n_idx * N_OUT;
-      const int rows_per = (EPI == 2) ? BN / 2 : BN;
-      bool ok = true;
+      const bool row_ok = wrow + (r % rows_per) < args.N;    // else: zero row
       for (int kb = 0; kb < KB; ++kb) {
-        ok = tc::mbar_wait(&sh.full[stage], phase, abort);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        const uint8_t *codes = smem + stage * SBYTES + A_BYTES + B_BYTES;
-        uint8_t *btile = smem + stage * SBYTES + A_BYTES;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = tt + 128 * h;                      // B row in the tile
-          uint8_t *brow = btile + (r >> 3) * 1024 + (r & 7) * 128;
-          if (wrow + (r % rows_per) >= args.N) {           // past the matrix: zero row
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              *reinterpret_cast<uint4 *>(brow + (j << 4)) = make_uint4(0u, 0u, 0u, 0u);
-            continue;
-          }
-          const uint4 c0 = *reinterpret_cast<const uint4 *>(codes + r * 32);
-          const uint4 c1 = *reinterpret_cast<const uint4 *>(codes + r * 32 + 16);
-          const uint8_t *srow = scl + (size_t)r * KBLK;
+        const bool ok = tc::mbar_wait(&sh.full[stage], phase, abort);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const uint8_t *codes = smem + stage * SBYTES + A_BYTES + B_BYTES + r * 32;
+        uint8_t *brow = smem + stage * SBYTES + A_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+        if (row_ok) {
+          const uint4 c0 = *reinterpret_cast<const uint4 *>(codes + sw);
+          const uint4 c1 = *reinterpret_cast<const uint4 *>(codes + (sw ^ 16));
           const uint32_t s0 = 2 * kb < KBLK ? srow[2 * kb] : 127u;
           const uint32_t s1 = 2 * kb + 1 < KBLK ? srow[2 * kb + 1] : 127u;
           const uint32_t f0 = scale_f16x2(s0, bad_scale), f1 = scale_f16x2(s1, bad_scale);
@@ -501,13 +497,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                                        hmul2(e2m1x2_to_f16x2(w >> 24), f));
             *reinterpret_cast<uint4 *>(brow + ((j ^ (r & 7)) << 4)) = v;
           }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4 *>(brow + (j << 4)) = make_uint4(0u, 0u, 0u, 0u);
         }
         // generic-proxy writes of the B tile -> visible to the tensor core
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc::mbar_arrive(&sh.bready[stage]);
         if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
       }
-      (void)ok;   // a failed wait raised *abort: the next tile's barrier stops all four warps
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     if (bad_scale) set_status(args.status, MOE_ERR_RANGE, 0);
@@ -549,11 +548,11 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
     const uint64_t dC[3] = {(uint64_t)g.K / 2, (uint64_t)g.N, (uint64_t)E};
     const uint32_t bC[3] = {BK / 2, (uint32_t)wrows, 1};
     if (!make_tensor_map(&mB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.B, 3, dC, bC,
-                         CU_TENSOR_MAP_SWIZZLE_NONE))
+                         CU_TENSOR_MAP_SWIZZLE_32B))
       return cudaErrorInvalidValue;
     if (EPI == 2) {
       if (!make_tensor_map(&mB3, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.B3, 3, dC, bC,
-                           CU_TENSOR_MAP_SWIZZLE_NONE))
+                           CU_TENSOR_MAP_SWIZZLE_32B))
         return cudaErrorInvalidValue;
     } else {
       mB3 = mB;
