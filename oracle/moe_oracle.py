@@ -299,6 +299,27 @@ def forward(cfg, inputs: dict, tokens: Optional[torch.Tensor] = None,
     return dict(y=y, y_shared=y_shared, tokens=tokens, routing=r)
 
 
+# ---------------------------------------------------------------------------
+# Routing statistics   [MoE] "Load balancing: how collapse happens, and how
+# it's kept in check"
+# ---------------------------------------------------------------------------
+
+def routing_statistics(probs: torch.Tensor, top1: torch.Tensor, alpha: float) -> dict:
+    """P_i, f_i and the auxiliary loss of one batch.
+
+    P_i = (1/n) sum over tokens of p_i(x)        (mean router probability)
+    f_i = (1/n) #{tokens whose argmax expert is i} (traffic share)
+    aux = alpha * E * sum_i f_i * P_i
+    ``top1`` is each token's argmax expert (rank 0 of the selection, so ties
+    go to the lower index as in ``topk_select``).
+    """
+    n, E = probs.shape
+    P = probs.sum(dim=0) / n
+    f = torch.bincount(top1.reshape(-1).to(torch.int64), minlength=E).to(F64) / n
+    aux = alpha * E * float((f * P).sum())
+    return dict(P=P, f=f, aux=aux)
+
+
 def near_ties(routing: dict, threshold: float = 1e-5) -> torch.Tensor:
     """Tokens whose top-k margin is below ``threshold`` (listed, not excused)."""
     return torch.nonzero(routing["margin"] < threshold, as_tuple=True)[0]

@@ -315,6 +315,54 @@ def test_shared_expert_added_unweighted():
     assert np.allclose(res["y"].numpy() - res0["y"].numpy(), S, rtol=1e-10, atol=1e-12)
 
 
+# -------------------------------------------------------- routing statistics
+
+def check_aux_loss_example(golden_dir):
+    g = _load(golden_dir, "aux_loss_example.json")
+    E = g["n_experts"]
+    # four token distributions whose first column averages P1 = 0.5825 and whose
+    # argmax is always expert 1 (the page's unbalanced router)
+    probs = torch.tensor([[0.70, 0.10, 0.10, 0.10],
+                          [0.55, 0.15, 0.15, 0.15],
+                          [0.48, 0.40, 0.06, 0.06],
+                          [0.60, 0.30, 0.05, 0.05]], dtype=torch.float64)
+    assert abs(probs[:, 0].mean().item() - g["unbalanced"]["P1"]) < 1e-12
+    top1 = O.topk_select(torch.log(probs), 1)[:, 0]
+    st = O.routing_statistics(probs, top1, 1.0)
+    assert st["f"].tolist() == [1.0, 0.0, 0.0, 0.0]
+    assert abs(st["aux"] - E * g["unbalanced"]["P1"]) < 1e-12
+    assert round(st["aux"], 2) == g["unbalanced"]["E_sum_fP_printed_2dp"]
+    assert round(O.routing_statistics(probs, top1, g["alpha"])["aux"], 4) == \
+        g["alpha_terms_printed"]["unbalanced"]
+    # balanced: each expert is the argmax once; any rows that sum to one give 1.0
+    bal = torch.tensor([[0.40, 0.20, 0.20, 0.20],
+                        [0.10, 0.50, 0.20, 0.20],
+                        [0.25, 0.05, 0.45, 0.25],
+                        [0.30, 0.10, 0.10, 0.50]], dtype=torch.float64)
+    t1 = O.topk_select(torch.log(bal), 1)[:, 0]
+    sb = O.routing_statistics(bal, t1, 1.0)
+    assert sb["f"].tolist() == g["balanced"]["f"]
+    assert abs(sb["aux"] - g["balanced"]["E_sum_fP"]) < 1e-12
+    assert abs(O.routing_statistics(bal, t1, g["alpha"])["aux"] -
+               g["alpha_terms_printed"]["balanced"]) < 1e-12
+
+
+def test_aux_loss_example(golden_dir):
+    check_aux_loss_example(golden_dir)
+
+
+def test_aux_loss_uniform_router_closed_form():
+    """p_i(x) = 1/E for every token: P_i = 1/E, so aux = alpha * sum_i f_i = alpha."""
+    g = torch.Generator().manual_seed(17)
+    for E in (2, 8, 128):
+        n = 97
+        probs = torch.full((n, E), 1.0 / E, dtype=torch.float64)
+        top1 = torch.randint(0, E, (n,), generator=g)
+        st = O.routing_statistics(probs, top1, 0.37)
+        assert abs(st["aux"] - 0.37) < 1e-12
+        assert abs(st["f"].sum().item() - 1.0) < 1e-12
+
+
 # ---------------------------------------------------------------- MXFP4 pins
 
 def check_mxfp4(golden_dir):
@@ -421,6 +469,13 @@ def _bad_dispatch(idx, E):                       # unstable order inside a segme
 _orig_dispatch = O.dispatch_arrays
 
 
+def _bad_stats(probs, top1, alpha):             # P_i averaged over experts, not tokens
+    n, E = probs.shape
+    P = probs.sum(dim=1)[:E] / E if n >= E else probs.sum(dim=1).mean().repeat(E)
+    f = torch.bincount(top1.reshape(-1).to(torch.int64), minlength=E).to(torch.float64) / n
+    return dict(P=P, f=f, aux=alpha * E * float((f * P).sum()))
+
+
 def _bad_softmax(logits):                        # no max subtraction and wrong axis
     ex = torch.exp(logits)
     return ex / ex.sum(dim=0, keepdim=True)
@@ -433,6 +488,7 @@ MUTANTS = [
     ("e2m1_value", _e2m1_bias0, check_mxfp4),
     ("dispatch_arrays", _bad_dispatch, check_dispatch_example),
     ("softmax_rows", _bad_softmax, check_softmax_example),
+    ("routing_statistics", _bad_stats, check_aux_loss_example),
 ]
 
 
