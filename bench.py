@@ -46,6 +46,8 @@ def parse_args(argv=None):
     p.add_argument("--n", type=int, default=None, help="override the token count")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--layers", type=int, default=1,
+                   help="MoE layers per step (independently seeded weights, run in sequence)")
     p.add_argument("--cpu-sample", type=int, default=None,
                    help="tokens in the oracle's timed sample")
     return p.parse_args(argv)
@@ -247,8 +249,24 @@ def run_ours(args):
         x = torch.randn(inputs["x"].shape, generator=g, device=device, dtype=torch.float32)
         inputs["x"] = (x * cfg.x_std).to(inputs["x"].dtype)
     w = moe.make_weights(inputs)
+    # further layers of the stack: their own seeded weights, same shapes
+    layer_inputs = [inputs] + [moe_synth.make_inputs(cfg, seed=args.seed + 101 * l, device=device)
+                               for l in range(1, args.layers)]
+    layer_w = [w] + [moe.make_weights(li) for li in layer_inputs[1:]]
     ws = moe.alloc_workspace(cfg, device)
     y = torch.empty(cfg.n, cfg.d, dtype=inputs["x"].dtype, device=device)
+    mid = [torch.empty_like(y) for _ in range(2)]
+
+    def run_layers(x_in, y_out, hook=None):
+        """Layer 0 .. L-1 in sequence; the stage hook instruments layer 0."""
+        cur = x_in
+        for l in range(args.layers):
+            out = y_out if l == args.layers - 1 else mid[l % 2]
+            if l == 0 and hook is not None:
+                moe.moe_forward_staged(cfg, cur, layer_w[l], out, ws, hook, stream)
+            else:
+                moe.moe_forward(cfg, cur, layer_w[l], out, ws, stream)
+            cur = out
     # a non-default stream: CUDA graphs cannot be captured on the legacy default stream
     stream = torch.cuda.Stream(device)
     torch.cuda.set_stream(stream)
@@ -271,7 +289,7 @@ def run_ours(args):
                 events[stage].record(stream)
             if stage == len(stage_names) - 1:
                 launches["n"] = kernels
-        moe.moe_forward_staged(cfg, x_pool[i % n_batches], w, y, ws, hook, stream)
+        run_layers(x_pool[i % n_batches], y, hook)
 
     L = moe.moe_workspace_layout_of(cfg)
     counts = ws[L["counts"]:L["counts"] + 4 * cfg.E].view(torch.int32)
@@ -338,7 +356,7 @@ def run_ours(args):
     barrier(device)
     elapsed = start.elapsed_time(stop) / 1e3
     t_job = max_over_ranks(elapsed, device)
-    kernels_per_step = launches["n"]
+    kernels_per_step = launches["n"] * args.layers
     st, detail = moe.moe_status_check(ws)
     if st != 0:
         raise RuntimeError(f"device status {moe.status_string(st)} ({detail})")
@@ -362,7 +380,7 @@ def run_ours(args):
     x_dev = torch.empty_like(inputs["x"])
     for _ in range(2):
         x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_forward(cfg, x_dev, w, y, ws, stream)
+        run_layers(x_dev, y)
         y_host.copy_(y, non_blocking=True)
     torch.cuda.synchronize(device)
     barrier(device)
@@ -370,7 +388,7 @@ def run_ours(args):
     e0.record(stream)
     for _ in range(args.steps):
         x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_forward(cfg, x_dev, w, y, ws, stream)
+        run_layers(x_dev, y)
         y_host.copy_(y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(device)
@@ -400,7 +418,8 @@ def run_ours(args):
                   else {"bytes_per_launch": dom_units, "active_experts_mean": active})
 
     out = {
-        "metric": "MoE-layer tokens/s",
+        "metric": ("MoE-layer tokens/s" if args.layers == 1 else
+                   f"MoE-stack tokens/s ({args.layers} layers per step)"),
         "value": job_throughput(cfg.n * args.steps, world, t_job),
         "unit": "tokens/s",
         "n_gpus": world,
@@ -415,6 +434,7 @@ def run_ours(args):
         "config": {
             "workload": workload_name(cfg),
             "tokens_per_rank": cfg.n,
+            "layers_per_step": args.layers,
             "parallelism": f"dp{world} (independent token batches, replicated weights)",
             "l2": l2_note,
             "timing": timing,
@@ -431,7 +451,7 @@ def run_ours(args):
         "clocks": clocks.summary(),
     }
 
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.layers == 1:
         tokens = args.cpu_sample or default_cpu_sample(cfg)
         del x_host, y_host, x_dev
         scfg, sub = oracle_sample(cfg, host_copy(inputs), tokens, args.seed)

@@ -149,6 +149,20 @@ moe_status moe_route(const moe_config *cfg, const void *x, const moe_weights *w,
                      int32_t *topk_idx, float *topk_gate, float *probs,
                      void *ws, size_t ws_bytes, void *stream);
 
+/* Routing statistics of one batch ("How Mixture of Experts Scales Model
+ * Parameters", section "Load balancing: how collapse happens, and how it's
+ * kept in check"):
+ *   P[i]  = (1/n) sum_t probs[t][i]            mean router probability
+ *   f[i]  = (1/n) #{t : topk_idx[t][0] == i}   share of tokens whose argmax is i
+ *   aux[0] = alpha * E * sum_i f[i] * P[i]      auxiliary load-balancing loss
+ * probs fp32 [n][E] and topk_idx int32 [n][K] as produced by moe_route
+ * (rank 0 of each row is the argmax).  P, f fp32 [E]; aux fp32 [1].  Sums run
+ * in a fixed order (deterministic).  A top-1 index outside [0, E) sets
+ * MOE_ERR_BAD_INDEX in the workspace status word. */
+moe_status moe_route_stats(const moe_config *cfg, const float *probs, const int32_t *topk_idx,
+                           float alpha, float *P, float *f, float *aux, void *ws,
+                           size_t ws_bytes, void *stream);
+
 /* moe_route without a workspace, for callers that cannot allocate device
  * memory: code running during CUDA graph capture under an allocator that is
  * not capture-safe, plugins handed only their input and output buffers by a

@@ -153,12 +153,22 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   if (status_failed(a.status)) return;
 
   // slot blockIdx.y -> the blockIdx.y-th expert with a non-empty segment
+  // (all offsets loaded up front: one memory latency, E <= 256)
   if (warp == 0) {
     const int slot = blockIdx.y;
+    int off_lo[8], off_hi[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = 32 * j + lane;
+      off_lo[j] = e < a.num_experts ? a.offsets[e] : 0;
+      off_hi[j] = e < a.num_experts ? a.offsets[e + 1] : 0;
+    }
     int seen = 0, found = -1;
-    for (int base = 0; base < a.num_experts && found < 0; base += 32) {
-      const int e = base + lane;
-      const bool ne = e < a.num_experts && a.offsets[e + 1] > a.offsets[e];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int base = 32 * j;
+      if (found >= 0 || base >= a.num_experts) continue;
+      const bool ne = off_hi[j] > off_lo[j];
       unsigned m = __ballot_sync(0xffffffffu, ne);
       const int c = __popc(m);
       if (seen + c > slot) {

@@ -16,6 +16,7 @@ namespace {
 
 constexpr int DP_THREADS = 1024;
 constexpr int DP_WARPS = DP_THREADS / 32;
+constexpr int DP_PREFETCH = 8;            // groups of 32 pair indices loaded ahead
 
 // One CTA.  Warp w owns the pair range [w*chunk, (w+1)*chunk) and walks it in
 // groups of 32 in increasing pair order, so a pair's rank inside its expert is
@@ -37,18 +38,28 @@ dispatch_kernel(const int32_t *__restrict__ topk_idx, int P, int E, int32_t *__r
   for (int i = threadIdx.x; i < DP_WARPS * E; i += DP_THREADS) hist[i] = 0;
   __syncthreads();
 
-  // pass 1: per-warp histogram
-  for (int base = beg; base < end; base += 32) {
-    const int p = base + lane;
-    int e = (p < end) ? topk_idx[p] : -1;
-    const bool bad = (p < end) && (e < 0 || e >= E);
-    if (bad) {
-      set_status(status, MOE_ERR_BAD_INDEX, p);
-      e = -1;
+  // pass 1: per-warp histogram (DP_PREFETCH groups of 32 loaded ahead)
+  for (int base0 = beg; base0 < end; base0 += 32 * DP_PREFETCH) {
+    int ev[DP_PREFETCH];
+#pragma unroll
+    for (int u = 0; u < DP_PREFETCH; ++u) {
+      const int p = base0 + 32 * u + lane;
+      ev[u] = (p < end) ? topk_idx[p] : -1;
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < DP_PREFETCH; ++u) {
+      const int p = base0 + 32 * u + lane;
+      int e = ev[u];
+      const bool bad = (p < end) && (e < 0 || e >= E);
+      if (bad) {
+        set_status(status, MOE_ERR_BAD_INDEX, p);
+        e = -1;
+      }
+      if (p >= end) e = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+      __syncwarp();
+    }
   }
   __syncthreads();
 
@@ -100,22 +111,31 @@ dispatch_kernel(const int32_t *__restrict__ topk_idx, int P, int E, int32_t *__r
   __syncthreads();
 
   // pass 2: scatter in pair order
-  for (int base = beg; base < end; base += 32) {
-    const int p = base + lane;
-    int e = (p < end) ? topk_idx[p] : -1;
-    if (e >= E || e < 0) e = -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    int pos = 0;
-    if (e >= 0) pos = my[e] + __popc(peers & lanemask_lt());
-    __syncwarp();
-    if (e >= 0) {
-      perm[pos] = p;
-      inv_perm[p] = pos;
-      if (lane == __ffs(peers) - 1) my[e] += __popc(peers);
-    } else if (p < end) {
-      inv_perm[p] = -1;
+  for (int base0 = beg; base0 < end; base0 += 32 * DP_PREFETCH) {
+    int ev[DP_PREFETCH];
+#pragma unroll
+    for (int u = 0; u < DP_PREFETCH; ++u) {
+      const int p = base0 + 32 * u + lane;
+      ev[u] = (p < end) ? topk_idx[p] : -1;
     }
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < DP_PREFETCH; ++u) {
+      const int p = base0 + 32 * u + lane;
+      int e = ev[u];
+      if (e >= E || e < 0 || p >= end) e = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      int pos = 0;
+      if (e >= 0) pos = my[e] + __popc(peers & lanemask_lt());
+      __syncwarp();
+      if (e >= 0) {
+        perm[pos] = p;
+        inv_perm[p] = pos;
+        if (lane == __ffs(peers) - 1) my[e] += __popc(peers);
+      } else if (p < end) {
+        inv_perm[p] = -1;
+      }
+      __syncwarp();
+    }
   }
 }
 

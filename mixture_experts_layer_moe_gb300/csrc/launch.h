@@ -22,6 +22,12 @@ cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, con
                          float *logits, int32_t *topk_idx, float *topk_gate, float *probs,
                          int *status, cudaStream_t s);
 
+// Routing statistics: P [E], f [E] and aux (one float) from probs [n][E] and
+// the top-1 column of topk_idx.
+cudaError_t launch_route_stats(const moe_config &c, const float *probs, const int32_t *topk_idx,
+                               float alpha, float *P, float *f, float *aux, int *status,
+                               cudaStream_t s);
+
 // Stable counting sort of P pairs by expert (one CTA).
 cudaError_t launch_dispatch(int P, int E, const int32_t *topk_idx, int32_t *counts,
                             int32_t *offsets, int32_t *perm, int32_t *inv_perm, int *status,

@@ -315,6 +315,20 @@ moe_status moe_route(const moe_config *cfg, const void *x, const moe_weights *w,
                                   topk_gate, probs, at<int>(ws, L.status), as_stream(stream)));
 }
 
+moe_status moe_route_stats(const moe_config *cfg, const float *probs, const int32_t *topk_idx,
+                           float alpha, float *P, float *f, float *aux, void *ws,
+                           size_t ws_bytes, void *stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config &c = *cfg;
+  if (!ok_ptr(probs) || !ok_ptr(topk_idx) || !ok_ptr(P) || !ok_ptr(f) || aux == nullptr ||
+      !aligned(aux, 4))
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  const Layout L = layout_of(c);
+  return cuda_status(launch_route_stats(c, probs, topk_idx, alpha, P, f, aux,
+                                        at<int>(ws, L.status), as_stream(stream)));
+}
+
 moe_status moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x,
                         int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
                         void *x_perm, void *ws, size_t ws_bytes, void *stream) {

@@ -249,3 +249,83 @@ cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, con
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Routing statistics ("How Mixture of Experts Scales Model Parameters",
+// section "Load balancing: how collapse happens, and how it's kept in check"):
+//   P_i = (1/n) sum_t p_i(t),  f_i = (1/n) #{t : argmax_e p_e(t) = i},
+//   aux = alpha * E * sum_i f_i P_i.
+// One CTA per 32 experts: lane = expert, warp w takes rows w, w+8, ...; each
+// run of 64 rows is summed into a fresh partial, the warp partials are added
+// in warp order, so the result does not depend on scheduling.
+namespace moe {
+namespace {
+
+constexpr int ST_WARPS = 8;
+
+__global__ void __launch_bounds__(32 * ST_WARPS)
+route_stats_kernel(const float *__restrict__ probs, const int32_t *__restrict__ topk_idx, int n,
+                   int E, int k, float *__restrict__ P, float *__restrict__ f, int *status) {
+  __shared__ float ps[ST_WARPS][32];
+  __shared__ int pc[ST_WARPS][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 32 + lane;
+  float sum = 0.f, part = 0.f;
+  int count = 0, in_part = 0;
+  for (int t = warp; t < n; t += ST_WARPS) {
+    if (e < E) part += probs[(size_t)t * E + e];
+    const int a = topk_idx[(size_t)t * k];
+    if (a < 0 || a >= E) {
+      if (lane == 0 && blockIdx.x == 0) set_status(status, MOE_ERR_BAD_INDEX, t * k);
+    } else if (a == e) {
+      ++count;
+    }
+    if (++in_part == 64) {
+      sum += part;
+      part = 0.f;
+      in_part = 0;
+    }
+  }
+  ps[warp][lane] = sum + part;
+  pc[warp][lane] = count;
+  __syncthreads();
+  if (warp == 0 && e < E) {
+    float s = 0.f;
+    int c = 0;
+    for (int w = 0; w < ST_WARPS; ++w) {
+      s += ps[w][lane];
+      c += pc[w][lane];
+    }
+    P[e] = s / (float)n;
+    f[e] = (float)c / (float)n;
+  }
+}
+
+// aux = alpha * E * sum_i f_i P_i, a fixed-order tree over one CTA.
+__global__ void __launch_bounds__(256)
+route_aux_kernel(const float *__restrict__ P, const float *__restrict__ f, int E, float alpha,
+                 float *__restrict__ aux) {
+  __shared__ float v[256];
+  v[threadIdx.x] = threadIdx.x < E ? f[threadIdx.x] * P[threadIdx.x] : 0.f;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (threadIdx.x < o) v[threadIdx.x] += v[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *aux = alpha * (float)E * v[0];
+}
+
+}  // namespace
+
+cudaError_t launch_route_stats(const moe_config &c, const float *probs, const int32_t *topk_idx,
+                               float alpha, float *P, float *f, float *aux, int *status,
+                               cudaStream_t s) {
+  route_stats_kernel<<<(c.n_experts + 31) / 32, 32 * ST_WARPS, 0, s>>>(
+      probs, topk_idx, c.n, c.n_experts, c.top_k, P, f, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  route_aux_kernel<<<1, 256, 0, s>>>(P, f, c.n_experts, alpha, aux);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -60,6 +60,7 @@ def _load() -> ctypes.CDLL:
         "moe_workspace_layout_of": [cfgp, ctypes.POINTER(moe_workspace_layout)],
         "moe_route": [cfgp, P, wp, P, P, P, P, SZ, P],
         "moe_route_noalloc": [cfgp, P, wp, P, P, P, P],
+        "moe_route_stats": [cfgp, P, P, ctypes.c_float, P, P, P, P, SZ, P],
         "moe_dispatch": [cfgp, P, P, P, P, P, P, P, P, SZ, P],
         "moe_expert_ffn": [cfgp, P, P, wp, P, P, SZ, P],
         "moe_combine": [cfgp, P, P, P, P, P, P, SZ, P],
@@ -160,6 +161,13 @@ def moe_route_noalloc(cfg, x, w: moe_weights, topk_idx, topk_gate, probs, stream
     _check(_lib.moe_route_noalloc(ctypes.byref(c), _ptr(x), ctypes.byref(w), _ptr(topk_idx),
                                   _ptr(topk_gate), _ptr(probs), _stream(stream)),
            "moe_route_noalloc")
+
+
+def moe_route_stats(cfg, probs, topk_idx, alpha, P, f, aux, ws, stream=None):
+    c = make_config(cfg)
+    _check(_lib.moe_route_stats(ctypes.byref(c), _ptr(probs), _ptr(topk_idx), float(alpha),
+                                _ptr(P), _ptr(f), _ptr(aux), _ptr(ws), ws.numel(),
+                                _stream(stream)), "moe_route_stats")
 
 
 def moe_dispatch(cfg, topk_idx, x, counts, offsets, perm, inv_perm, x_perm, ws, stream=None):

@@ -264,3 +264,45 @@ def test_expert_ffn_segments(lib, name):
         W1, W3, W2 = O.expert_weights(oin, cfg, e)
         want[off[e]:off[e + 1]] = O.expert_ffn(xp[off[e]:off[e + 1]], W1, W2, cfg.act, W3)
     parity.check_output(cfg, y_perm, want)
+
+
+# ------------------------------------------------------- routing statistics
+
+@pytest.mark.parametrize("name", ["mixtral_small", "prefill_zipf_small", "finegrained_small"])
+def test_route_stats(lib, name):
+    """P_i, f_i and the auxiliary loss against the oracle's definition; f_i is
+    compared as the exact count of the kernel's own argmax choices."""
+    cfg = SMALL[name]
+    inputs = moe_synth.make_inputs(cfg, seed=11, device="cuda")
+    ws = lib.alloc_workspace(cfg)
+    idx = torch.empty(cfg.n, cfg.k, dtype=torch.int32, device="cuda")
+    g = torch.empty(cfg.n, cfg.k, dtype=torch.float32, device="cuda")
+    pr = torch.empty(cfg.n, cfg.E, dtype=torch.float32, device="cuda")
+    lib.moe_route(cfg, inputs["x"], lib.make_weights(inputs), idx, g, pr, ws)
+    P = torch.empty(cfg.E, device="cuda")
+    f = torch.empty(cfg.E, device="cuda")
+    aux = torch.empty(1, device="cuda")
+    lib.moe_route_stats(cfg, pr, idx, 0.01, P, f, aux, ws)
+    assert lib.moe_status_check(ws)[0] == 0
+    r = O.route(cfg, parity.oracle_inputs(inputs))
+    want = O.routing_statistics(r["probs"], idx[:, 0].cpu().long(), 0.01)
+    assert (P.cpu().double() - want["P"]).abs().max().item() < 1e-6
+    assert torch.equal(torch.round(f.cpu().double() * cfg.n), torch.round(want["f"] * cfg.n))
+    assert abs(aux.item() - want["aux"]) <= 1e-5 * abs(want["aux"])
+
+
+def test_route_stats_page_example(lib):
+    """Four tokens whose argmax is always expert 1 with P1 = 0.5825: E * sum f P = 2.33."""
+    cfg = moe_synth.MoEConfig("ex", n=4, d=4, d_ff=4, E=4, k=1, act_dtype="f32",
+                              weight_dtype="f32", gate="top_prob", act="relu")
+    probs = torch.tensor([[0.70, 0.10, 0.10, 0.10], [0.55, 0.15, 0.15, 0.15],
+                          [0.48, 0.40, 0.06, 0.06], [0.60, 0.30, 0.05, 0.05]], device="cuda")
+    idx = torch.zeros(4, 1, dtype=torch.int32, device="cuda")
+    P = torch.empty(4, device="cuda")
+    f = torch.empty(4, device="cuda")
+    aux = torch.empty(1, device="cuda")
+    ws = lib.alloc_workspace(cfg)
+    lib.moe_route_stats(cfg, probs, idx, 1.0, P, f, aux, ws)
+    assert lib.moe_status_check(ws)[0] == 0
+    assert f.tolist() == [1.0, 0.0, 0.0, 0.0]
+    assert abs(aux.item() - 2.33) < 1e-6 and round(aux.item(), 2) == 2.33
