@@ -33,6 +33,11 @@ import torch  # noqa: E402
 import moe_synth  # noqa: E402
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + write) per launch of the dominant kernel from an ncu
+# capture of the same workload and kernel version (profiles/ has the summary).
+MEASURED_TRAFFIC = {
+    ("mixtral_bf16", 4096, "ffn_up"): 1.948580e9 + 0.226934e9,
+}
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -446,7 +451,8 @@ def run_ours(args):
         "roofline": {"kernel": dom_stage, "bound": bound, "achieved": achieved, "peak": peak,
                      "unit": dom_unit, "frac": achieved / peak,
                      "peak_source": f"{peak_src} ({'bf16 sustained' if bound == 'tensor' else 'hbm copy'})",
-                     "traffic": None, **per_launch},
+                     "traffic": (MEASURED_TRAFFIC.get((cfg.name, cfg.n, dom_stage))
+                                 if args.layers == 1 else None), **per_launch},
         "stages_ms": stage_ms,
         "clocks": clocks.summary(),
     }
