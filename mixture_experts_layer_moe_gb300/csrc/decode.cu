@@ -48,21 +48,42 @@ struct DecodeArgs {
   int *status;
 };
 
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t d;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(d)
-      : "r"(byte));
-  return d;
+// The four code pairs of a 32-bit word (bytes 0..3) as four f16 pairs; each
+// pair's low half is the low nibble (the even element).
+struct F16x2x4 {
+  uint32_t v[4];
+};
+__device__ __forceinline__ F16x2x4 e2m1x8_to_f16x2x4(uint32_t w) {
+  F16x2x4 r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3])
+      : "r"(w));
+  return r;
 }
 
+// d = A * B (+ c), m16n8k16, f16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_16816_first(float (&c)[4], uint32_t a0, uint32_t a1,
+                                                uint32_t a2, uint32_t a3, uint32_t b0,
+                                                uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// E8M0 byte -> 2^(s-127) (s = 0 is the fp32 subnormal 2^-127; s = 255, not a
+// valid scale, gives +inf).
+__device__ __forceinline__ float e8m0_fast(uint32_t s) {
+  return __uint_as_float(s ? (s << 23) : 0x00400000u);
 }
 
 // One MX block (32 elements) of rows g and g+8 against 8 tokens.  The block's
@@ -73,11 +94,10 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
 // reduction does not depend on the order of its terms.
 __device__ __forceinline__ void mx_block(float (&acc)[4], uint32_t wg, uint32_t wh, float sg,
                                          float sh, const uint4 &b) {
-  float p[4] = {0.f, 0.f, 0.f, 0.f};
-  mma_16816(p, e2m1x2_to_f16x2(wg), e2m1x2_to_f16x2(wh), e2m1x2_to_f16x2(wg >> 8),
-            e2m1x2_to_f16x2(wh >> 8), b.x, b.y);
-  mma_16816(p, e2m1x2_to_f16x2(wg >> 16), e2m1x2_to_f16x2(wh >> 16), e2m1x2_to_f16x2(wg >> 24),
-            e2m1x2_to_f16x2(wh >> 24), b.z, b.w);
+  const F16x2x4 ag = e2m1x8_to_f16x2x4(wg), ah = e2m1x8_to_f16x2x4(wh);
+  float p[4];
+  mma_16816_first(p, ag.v[0], ah.v[0], ag.v[1], ah.v[1], b.x, b.y);
+  mma_16816(p, ag.v[2], ah.v[2], ag.v[3], ah.v[3], b.z, b.w);
   acc[0] = fmaf(sg, p[0], acc[0]);
   acc[1] = fmaf(sg, p[1], acc[1]);
   acc[2] = fmaf(sh, p[2], acc[2]);
@@ -128,16 +148,18 @@ __global__ void rows_to_f16_kernel(const __nv_bfloat16 *__restrict__ src,
 
 // EPI: 0 none, 1 relu, 2 swiglu (tm3 / S3 hold the linear branch).
 //
-// One CTA = one selected expert x 16 * row_groups output rows.  Its DV_WARPS
-// warps form row_groups groups of DV_WARPS / row_groups warps; the warps of a
-// group split the reduction into contiguous runs of 128-byte boxes.  Each warp
-// keeps its own ring of boxes per matrix in flight (lane 0 issues TMA and
-// refills a slot once the warp has read it) and reads its fragments
-// conflict-free from the 128-byte-swizzled boxes.  The B fragments (the
-// tokens' f16 activation rows, a few KB that stay in L2) are loaded from
-// global memory a box ahead of their use.  The partial sums of a group are
-// added in warp order by its first warp, which applies the activation and
-// stores.
+// Persistent: the grid is sized to the GPU and each CTA walks its share of the
+// work units (selected expert x 16 * row_groups output rows), slot-major.  Its
+// DV_WARPS warps form row_groups groups of DV_WARPS / row_groups warps; the
+// warps of a group split the reduction into contiguous runs of 128-byte
+// boxes.  Each warp keeps its own ring of boxes per matrix in flight; lane 0
+// refills a slot as soon as the warp has read it, with the next box of the
+// warp's sequence — across token passes and units — so the weight stream
+// does not stop at unit boundaries.  Block scales of the next unit are copied
+// while the current one runs (two buffers).  B fragments (the tokens' f16
+// activation rows, a few KB in L2) are loaded a box ahead of their use.  The
+// partial sums of a group are added in warp order by its first warp, which
+// applies the activation and stores.
 template <int EPI>
 __global__ void __launch_bounds__(32 * DV_WARPS)
 decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm3,
@@ -145,17 +167,16 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   constexpr int NMAT = (EPI == 2) ? 2 : 1;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ uint64_t full[DV_WARPS][DV_STAGES_MAX];
-  __shared__ uint64_t sbar;
-  __shared__ int s_expert;
+  __shared__ uint64_t sbar[2];
   __shared__ int s_abort;
+  __shared__ int s_nactive;
+  __shared__ int s_active[257];
   __shared__ float red[DV_WARPS][32][8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (status_failed(a.status)) return;
 
-  // slot blockIdx.y -> the blockIdx.y-th expert with a non-empty segment
-  // (all offsets loaded up front: one memory latency, E <= 256)
+  // the experts with a non-empty segment, in order (E <= 256, one round of loads)
   if (warp == 0) {
-    const int slot = blockIdx.y;
     int off_lo[8], off_hi[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -163,24 +184,23 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       off_lo[j] = e < a.num_experts ? a.offsets[e] : 0;
       off_hi[j] = e < a.num_experts ? a.offsets[e + 1] : 0;
     }
-    int seen = 0, found = -1;
+    int seen = 0, bad = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int base = 32 * j;
-      if (found >= 0 || base >= a.num_experts) continue;
-      const bool ne = off_hi[j] > off_lo[j];
-      unsigned m = __ballot_sync(0xffffffffu, ne);
-      const int c = __popc(m);
-      if (seen + c > slot) {
-        for (int i = slot - seen; i > 0; --i) m &= m - 1;   // drop the lower set bits
-        found = base + __ffs(m) - 1;
-      }
-      seen += c;
+      const int e = 32 * j + lane;
+      const bool ne = e < a.num_experts && off_hi[j] > off_lo[j];
+      if (e < a.num_experts && (off_lo[j] < 0 || off_hi[j] < off_lo[j] || off_hi[j] > a.P)) bad = 1;
+      const unsigned m = __ballot_sync(0xffffffffu, ne);
+      if (ne) s_active[seen + __popc(m & lanemask_lt())] = e;
+      seen += __popc(m);
     }
+    bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
-      s_expert = found;
+      s_nactive = bad ? 0 : seen;
+      if (bad) set_status(a.status, MOE_ERR_BAD_INDEX, -1);
       s_abort = 0;
-      tc::mbar_init(&sbar, 1);
+      tc::mbar_init(&sbar[0], 1);
+      tc::mbar_init(&sbar[1], 1);
     }
   }
   if (lane == 0) {
@@ -188,13 +208,6 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     tc::fence_mbar_init();
   }
   __syncthreads();
-  const int e = s_expert;
-  if (e < 0) return;
-  const int beg = a.offsets[e], cnt = a.offsets[e + 1] - beg;
-  if (beg < 0 || cnt < 0 || beg + cnt > a.P) {
-    if (threadIdx.x == 0) set_status(a.status, MOE_ERR_BAD_INDEX, e);
-    return;
-  }
   uint8_t *smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   const int K = a.K, R = a.R, S = a.stages;
   const int RG = a.row_groups, KS = DV_WARPS / RG;
@@ -204,120 +217,177 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   const int per_warp = (NC + KS - 1) / KS;
   const int c_beg = min(NC, split * per_warp), c_end = min(NC, c_beg + per_warp);
   const int cta_rows = 16 * RG;
-  const int sc_bytes = cta_rows * KB;                   // the CTA's rows, one matrix
+  const int row_blocks = (R + cta_rows - 1) / cta_rows;
+  const int total = s_nactive * row_blocks;
+  const int sc_bytes = cta_rows * KB;                   // one unit's rows, one matrix
   const int sc_pitch = (sc_bytes + 15) & ~15;
   uint8_t *ring = smem + (size_t)warp * S * NMAT * DV_BOX;
-  uint8_t *scl = smem + (size_t)DV_WARPS * S * NMAT * DV_BOX;
-  const int cta_r0 = blockIdx.x * cta_rows;
-  const int r0 = cta_r0 + grp * 16;
-  const bool active = r0 < R;
+  uint8_t *scl_base = smem + (size_t)DV_WARPS * S * NMAT * DV_BOX;
   const int g = lane >> 2, t = lane & 3;
-  const int wrow = e * R + r0;                          // first code row of this warp
   volatile int *abort = &s_abort;
 
-  auto issue = [&](int chunk, int slot) {
-    tc::mbar_arrive_expect_tx(&full[warp][slot], NMAT * DV_BOX);
-    uint8_t *dst = ring + (size_t)slot * NMAT * DV_BOX;
-    tc::tma_load_2d(&tm1, &full[warp][slot], dst, chunk * DV_BOXB, wrow);
-    if (NMAT == 2) tc::tma_load_2d(&tm3, &full[warp][slot], dst + DV_BOX, chunk * DV_BOXB, wrow);
+  // unit i of this CTA -> (expert, first row); token passes of a unit
+  auto unit_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
+  auto expert_of = [&](int u) { return s_active[u / row_blocks]; };
+  auto row0_of = [&](int u) { return (u % row_blocks) * cta_rows; };
+  auto passes_of = [&](int u) {
+    const int e = expert_of(u);
+    return (a.offsets[e + 1] - a.offsets[e] + DV_TOK - 1) / DV_TOK;
+  };
+  // scales of unit i -> buffer i & 1 (thread 0 only; sf_phase: parity of the
+  // last copy issued into each buffer, -1 if none)
+  int sf_phase[2] = {-1, -1};
+  auto fetch_scales = [&](int i) {
+    const int u = unit_of(i);
+    if (u >= total) return;
+    sf_phase[i & 1] = (i >> 1) & 1;
+    const int e = expert_of(u), r0 = row0_of(u);
+    const int rows = min(cta_rows, R - r0);
+    const uint32_t bytes = (uint32_t)rows * KB;         // a multiple of 16 (rows % 16 == 0)
+    uint8_t *dst = scl_base + (size_t)(i & 1) * NMAT * sc_pitch;
+    tc::mbar_arrive_expect_tx(&sbar[i & 1], NMAT * bytes);
+    bulk_load(dst, a.S + ((size_t)e * R + r0) * KB, bytes, &sbar[i & 1]);
+    if (NMAT == 2) bulk_load(dst + sc_pitch, a.S3 + ((size_t)e * R + r0) * KB, bytes, &sbar[i & 1]);
+  };
+  // the producer's cursor over this warp's boxes: (unit i, pass p, box c)
+  int pi = 0, pp = 0, pc = c_beg, issued = 0;
+  bool pvalid = c_beg < c_end && unit_of(0) < total;
+  auto issue_next = [&]() {
+    if (!pvalid) return;
+    const int u = unit_of(pi);
+    const int r0 = row0_of(u) + grp * 16;
+    const int slot = issued % S;
+    if (r0 < R) {
+      tc::mbar_arrive_expect_tx(&full[warp][slot], NMAT * DV_BOX);
+      uint8_t *dst = ring + (size_t)slot * NMAT * DV_BOX;
+      const int wrow = expert_of(u) * R + r0;
+      tc::tma_load_2d(&tm1, &full[warp][slot], dst, pc * DV_BOXB, wrow);
+      if (NMAT == 2) tc::tma_load_2d(&tm3, &full[warp][slot], dst + DV_BOX, pc * DV_BOXB, wrow);
+    } else {
+      tc::mbar_arrive(&full[warp][slot]);   // a group past the last row: keep the phases in step
+    }
+    ++issued;
+    if (++pc == c_end) {
+      pc = c_beg;
+      if (++pp == passes_of(u)) {
+        pp = 0;
+        ++pi;
+        pvalid = unit_of(pi) < total;
+      }
+    }
   };
 
   if (threadIdx.x == 0) {
-    const int rows = min(cta_rows, R - cta_r0);
-    const uint32_t bytes = (uint32_t)rows * KB;         // a multiple of 16 (rows % 16 == 0)
-    tc::mbar_arrive_expect_tx(&sbar, NMAT * bytes);
-    bulk_load(scl, a.S + (size_t)(e * R + cta_r0) * KB, bytes, &sbar);
-    if (NMAT == 2) bulk_load(scl + sc_pitch, a.S3 + (size_t)(e * R + cta_r0) * KB, bytes, &sbar);
+    fetch_scales(0);
+    fetch_scales(1);
   }
-  bool scales_ready = false;
-  int issued = 0, consumed = 0;
-  const uint8_t *s1g = scl + (grp * 16 + g) * KB, *s1h = s1g + 8 * KB;
-  const uint8_t *s3g = s1g + sc_pitch, *s3h = s1h + sc_pitch;
+  if (lane == 0)
+    for (int st = 0; st < S; ++st) issue_next();
+  int consumed = 0;
 
-  for (int tg = 0; tg < cnt; tg += DV_TOK) {
-    // every thread sees the same decision: a warp that timed out stops the CTA
-    if (__syncthreads_or(*abort)) break;
-    if (active && lane == 0) {
-      for (int c = c_beg; c < c_end && c - c_beg < S; ++c) issue(c, (issued++) % S);
-    }
-    bool ok = true;
-    if (active && !scales_ready) {
-      scales_ready = __all_sync(0xffffffffu, tc::mbar_wait(&sbar, 0, abort));
-      ok = scales_ready;
-    }
-    const bool xrow_ok = g < cnt - tg;                  // token g of this pass exists
-    const uint16_t *xrow = a.act16 + (size_t)(beg + tg + (xrow_ok ? g : 0)) * K + 8 * t;
-    float acc1[4] = {0.f, 0.f, 0.f, 0.f}, acc3[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int c = c_beg; active && c < c_end && ok; ++c) {
-      const int nb = min(8, KB - c * 8);
-      uint4 bx[8];
+  for (int i = 0; unit_of(i) < total; ++i) {
+    const int u = unit_of(i);
+    const int e = expert_of(u);
+    const int r0 = row0_of(u) + grp * 16;
+    const bool active = r0 < R;
+    const int beg = a.offsets[e], cnt = a.offsets[e + 1] - beg;
+    const uint8_t *scl = scl_base + (size_t)(i & 1) * NMAT * sc_pitch;
+    const uint8_t *s1g = scl + (grp * 16 + g) * KB, *s1h = s1g + 8 * KB;
+    const uint8_t *s3g = s1g + sc_pitch, *s3h = s1h + sc_pitch;
+    bool scales_ready = false;
+    for (int tg = 0; tg < cnt; tg += DV_TOK) {
+      // every thread sees the same decision: a warp that timed out stops the CTA
+      if (__syncthreads_or(*abort)) goto done;
+      bool ok = true;
+      if (!scales_ready && c_beg < c_end) {
+        scales_ready = __all_sync(0xffffffffu, tc::mbar_wait(&sbar[i & 1], (i >> 1) & 1, abort));
+        ok = scales_ready;
+      }
+      const bool xrow_ok = g < cnt - tg;                // token g of this pass exists
+      const uint16_t *xrow = a.act16 + (size_t)(beg + tg + (xrow_ok ? g : 0)) * K + 8 * t;
+      float acc1[4] = {0.f, 0.f, 0.f, 0.f}, acc3[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int c = c_beg; c < c_end && ok; ++c) {
+        const int nb = min(8, KB - c * 8);
+        uint4 bx[8];
 #pragma unroll
-      for (int bl = 0; bl < 8; ++bl)
-        bx[bl] = (xrow_ok && bl < nb) ? __ldg(reinterpret_cast<const uint4 *>(xrow + (c * 8 + bl) * 32))
-                                      : make_uint4(0u, 0u, 0u, 0u);
-      const int slot = consumed % S;
-      const uint32_t parity = (consumed / S) & 1;
-      ++consumed;
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&full[warp][slot], parity, abort));
-      if (!ok) break;
-      const uint8_t *st = ring + (size_t)slot * NMAT * DV_BOX;
+        for (int bl = 0; bl < 8; ++bl)
+          bx[bl] = (active && xrow_ok && bl < nb)
+                       ? __ldg(reinterpret_cast<const uint4 *>(xrow + (c * 8 + bl) * 32))
+                       : make_uint4(0u, 0u, 0u, 0u);
+        const int slot = consumed % S;
+        const uint32_t parity = (consumed / S) & 1;
+        ++consumed;
+        if (active) {
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(&full[warp][slot], parity, abort));
+          if (!ok) break;
+          const uint8_t *st = ring + (size_t)slot * NMAT * DV_BOX;
+          auto block = [&](int bl) {
+            const int bg = c * 8 + bl;
+            const int off = ((bl ^ g) << 4) + 4 * t;
+            const uint32_t wg = *reinterpret_cast<const uint32_t *>(st + g * DV_BOXB + off);
+            const uint32_t wh = *reinterpret_cast<const uint32_t *>(st + (g + 8) * DV_BOXB + off);
+            mx_block(acc1, wg, wh, e8m0_fast(s1g[bg]), e8m0_fast(s1h[bg]), bx[bl]);
+            if constexpr (NMAT == 2) {
+              const uint32_t vg = *reinterpret_cast<const uint32_t *>(st + DV_BOX + g * DV_BOXB + off);
+              const uint32_t vh =
+                  *reinterpret_cast<const uint32_t *>(st + DV_BOX + (g + 8) * DV_BOXB + off);
+              mx_block(acc3, vg, vh, e8m0_fast(s3g[bg]), e8m0_fast(s3h[bg]), bx[bl]);
+            }
+          };
+          if (nb == 8) {
+            // a full box: straight-line code, so the eight blocks' independent
+            // MMA chains can be interleaved
 #pragma unroll
-      for (int bl = 0; bl < 8; ++bl) {
-        if (bl < nb) {
-          const int bg = c * 8 + bl;
-          const int off = ((bl ^ g) << 4) + 4 * t;
-          const uint32_t wg = *reinterpret_cast<const uint32_t *>(st + g * DV_BOXB + off);
-          const uint32_t wh = *reinterpret_cast<const uint32_t *>(st + (g + 8) * DV_BOXB + off);
-          mx_block(acc1, wg, wh, e8m0_to_float(s1g[bg]), e8m0_to_float(s1h[bg]), bx[bl]);
-          if constexpr (NMAT == 2) {
-            const uint32_t vg =
-                *reinterpret_cast<const uint32_t *>(st + DV_BOX + g * DV_BOXB + off);
-            const uint32_t vh =
-                *reinterpret_cast<const uint32_t *>(st + DV_BOX + (g + 8) * DV_BOXB + off);
-            mx_block(acc3, vg, vh, e8m0_to_float(s3g[bg]), e8m0_to_float(s3h[bg]), bx[bl]);
+            for (int bl = 0; bl < 8; ++bl) block(bl);
+          } else {
+            for (int bl = 0; bl < nb; ++bl) block(bl);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          // the slot was read through the generic proxy; order those reads
+          // before the TMA engine overwrites it
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          issue_next();
+        }
+      }
+      // partial sums -> the first warp of the group, added in warp order
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        red[warp][lane][q] = acc1[q];
+        red[warp][lane][4 + q] = acc3[q];
+      }
+      if (__syncthreads_or(!ok)) goto done;   // an aborted pass stores nothing
+      if (split == 0 && active) {
+        float s1[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int w = warp; w < warp + KS; ++w)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            s1[q] += red[w][lane][q];
+            s3[q] += red[w][lane][4 + q];
+          }
+        // c0, c1: row g, tokens 2t, 2t+1; c2, c3: row g+8
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float v;
+          if constexpr (EPI == 2) v = s1[q] / (1.f + __expf(-s1[q])) * s3[q];
+          else if constexpr (EPI == 1) v = fmaxf(s1[q], 0.f);
+          else v = s1[q];
+          const int tok = tg + 2 * t + (q & 1);
+          const int row = r0 + g + ((q >> 1) ? 8 : 0);
+          if (tok < cnt && row < R) {
+            const __nv_bfloat16 hb = __float2bfloat16_rn(v);
+            a.out[(size_t)(beg + tok) * R + row] = hb;
+            if (a.out16) a.out16[(size_t)(beg + tok) * R + row] = to_f16_bits(__bfloat162float(hb));
           }
         }
       }
-      __syncwarp();
-      if (lane == 0 && c + S < c_end) {
-        // the slot was read through the generic proxy; order those reads
-        // before the TMA engine overwrites it
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue(c + S, (issued++) % S);
-      }
     }
-    // partial sums -> the first warp of the group, added in warp order
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      red[warp][lane][i] = acc1[i];
-      red[warp][lane][4 + i] = acc3[i];
-    }
-    if (__syncthreads_or(!ok)) continue;   // an aborted pass stores nothing
-    if (split == 0 && active) {
-      float s1[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int w = warp; w < warp + KS; ++w)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          s1[i] += red[w][lane][i];
-          s3[i] += red[w][lane][4 + i];
-        }
-      // c0, c1: row g, tokens 2t, 2t+1; c2, c3: row g+8
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float v;
-        if constexpr (EPI == 2) v = s1[i] / (1.f + __expf(-s1[i])) * s3[i];
-        else if constexpr (EPI == 1) v = fmaxf(s1[i], 0.f);
-        else v = s1[i];
-        const int tok = tg + 2 * t + (i & 1);
-        const int row = r0 + g + ((i >> 1) ? 8 : 0);
-        if (tok < cnt && row < R) {
-          const __nv_bfloat16 hb = __float2bfloat16_rn(v);
-          a.out[(size_t)(beg + tok) * R + row] = hb;
-          if (a.out16) a.out16[(size_t)(beg + tok) * R + row] = to_f16_bits(__bfloat162float(hb));
-        }
-      }
-    }
+    // unit i is done everywhere: its scale buffer takes unit i + 2
+    __syncthreads();
+    if (threadIdx.x == 0) fetch_scales(i + 2);
   }
+done:
   if (*abort) {
     // let the copies this CTA issued land before it exits
     if (lane == 0) {
@@ -325,7 +395,9 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
         tc::mbar_wait_drain(&full[warp][j % S], (j / S) & 1, 100000000ull);
     }
     if (threadIdx.x == 0) {
-      tc::mbar_wait_drain(&sbar, 0, 100000000ull);
+      // scale copies in flight (a completed phase returns at once)
+      for (int b = 0; b < 2; ++b)
+        if (sf_phase[b] >= 0) tc::mbar_wait_drain(&sbar[b], (uint32_t)sf_phase[b], 100000000ull);
       set_status(a.status, MOE_ERR_TIMEOUT, blockIdx.x);
     }
   }
@@ -334,7 +406,7 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
 size_t decode_smem(int nmat, int K, int row_groups, int stages) {
   const int KB = K / 32;
   const size_t sc_pitch = (size_t)((16 * row_groups * KB + 15) & ~15);
-  return 1024 + (size_t)DV_WARPS * stages * nmat * DV_BOX + (size_t)nmat * sc_pitch;
+  return 1024 + (size_t)DV_WARPS * stages * nmat * DV_BOX + 2 * (size_t)nmat * sc_pitch;
 }
 
 template <int EPI>
@@ -347,11 +419,19 @@ cudaError_t launch_one(DecodeArgs a, const uint8_t *W, const uint8_t *W3, int nu
   a.stages = per_warp < DV_STAGES_MAX ? (per_warp > 0 ? per_warp : 1) : DV_STAGES_MAX;
   const size_t smem = decode_smem(NMAT, a.K, a.row_groups, a.stages);
   static size_t smem_set = 0;
-  if (smem > 48 * 1024 && smem > smem_set) {
+  static int per_sm = 0;
+  if (smem > smem_set) {
     cudaError_t e = cudaFuncSetAttribute(decode_mxfp4_kernel<EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     smem_set = smem;
+    per_sm = 0;
+  }
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mxfp4_kernel<EPI>,
+                                                      32 * DV_WARPS, smem) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
   }
   CUtensorMap m1, m3;
   const uint64_t dims[2] = {(uint64_t)a.K / 2, (uint64_t)num_experts * a.R};
@@ -366,9 +446,13 @@ cudaError_t launch_one(DecodeArgs a, const uint8_t *W, const uint8_t *W3, int nu
   } else {
     m3 = m1;
   }
+  // units: at most `slots` experts x row blocks; no more CTAs than units
   const int cta_rows = 16 * a.row_groups;
-  dim3 grid((a.R + cta_rows - 1) / cta_rows, slots);
-  decode_mxfp4_kernel<EPI><<<grid, 32 * DV_WARPS, smem, s>>>(m1, m3, a);
+  const long units = (long)slots * ((a.R + cta_rows - 1) / cta_rows);
+  long grid = (long)per_sm * num_sms();
+  if (grid > units) grid = units;
+  if (grid < 1) grid = 1;
+  decode_mxfp4_kernel<EPI><<<(unsigned)grid, 32 * DV_WARPS, smem, s>>>(m1, m3, a);
   return cudaGetLastError();
 }
 

@@ -113,12 +113,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t d;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(d)
-      : "r"(byte));
-  return d;
+// The four code pairs of a 32-bit word (bytes 0..3) as four f16 pairs, low
+// nibble (even element) in the low half.
+__device__ __forceinline__ uint4 e2m1x8_to_f16x2x4(uint32_t w) {
+  uint4 r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "r"(w));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
@@ -491,10 +495,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const uint32_t w = words[j], f = j < 4 ? f0 : f1;
-            const uint4 v = make_uint4(hmul2(e2m1x2_to_f16x2(w), f), hmul2(e2m1x2_to_f16x2(w >> 8), f),
-                                       hmul2(e2m1x2_to_f16x2(w >> 16), f),
-                                       hmul2(e2m1x2_to_f16x2(w >> 24), f));
+            const uint32_t f = j < 4 ? f0 : f1;
+            const uint4 q = e2m1x8_to_f16x2x4(words[j]);
+            const uint4 v = make_uint4(hmul2(q.x, f), hmul2(q.y, f), hmul2(q.z, f), hmul2(q.w, f));
             *reinterpret_cast<uint4 *>(brow + ((j ^ (r & 7)) << 4)) = v;
           }
         } else {
