@@ -8,16 +8,16 @@
 // MXFP4?": 4-bit elements in blocks of 32 sharing one scale; E2M1 elements and
 // E8M0 scales per the OCP MX v1.0 format).
 //
-// Work unit: one CTA = one selected expert x 16 output rows (one MMA M tile);
-// its warps split the reduction.  Codes arrive by TMA (128-byte boxes of 16
-// rows, 128-byte swizzle).  16 bytes of a row are exactly one MX block (32
-// elements, one scale); lane (g = lane/4, t = lane%4) reads word t of the block
-// for rows g and g+8 and converts its bytes with cvt.rn.f16x2.e2m1x2 straight
-// into the A fragment of mma.sync.m16n8k16.  The expert's tokens (up to 8 per
-// pass, N = 8) sit in shared memory as f16 and form the B fragment.  Each
-// 32-element block is multiplied with unscaled E2M1 values into a fresh fp32
-// partial, which is then scaled by the block's E8M0 scale and added to the
-// fp32 accumulator.
+// Work unit: one selected expert x 16 * RG output rows (RG MMA M tiles); the
+// warps of a 16-row group split the reduction.  Codes arrive by TMA (128-byte
+// boxes of 16 rows, 128-byte swizzle).  16 bytes of a row are exactly one MX
+// block (32 elements, one scale); lane (g = lane/4, t = lane%4) reads word t of
+// the block for rows g and g+8 and converts its bytes with
+// cvt.rn.f16x2.e2m1x2 straight into the A fragment of mma.sync.m16n8k16.  The
+// expert's tokens (up to 8 per pass, N = 8) are f16 rows read from L2 into
+// the B fragment.  Each 32-element block is multiplied with unscaled E2M1
+// values into a fresh fp32 partial, which is then scaled by the block's E8M0
+// scale and added to the fp32 accumulator.
 //
 // Activations enter the tensor core as f16 (E2M1 values are exact in f16);
 // an activation beyond the f16 range (|v| > 65504) is clamped to it.
@@ -31,7 +31,7 @@ namespace {
 constexpr int DV_WARPS = 8;                 // warps per CTA = row groups x reduction splits
 constexpr int DV_BOXB = 128;                // bytes of a row per TMA box: 8 MX blocks
 constexpr int DV_BOX = 16 * DV_BOXB;        // one box: 16 rows x 128 bytes (128-byte swizzle)
-constexpr int DV_STAGES_MAX = 2;            // boxes in flight per warp and matrix
+constexpr int DV_STAGES = 2;                // boxes in flight per warp and matrix (a power of 2)
 constexpr int DV_TOK = 8;                   // tokens per pass (MMA N)
 
 struct DecodeArgs {
@@ -39,8 +39,6 @@ struct DecodeArgs {
   int num_experts;
   int P;
   const uint16_t *act16;          // f16 activation rows in segment order [P][K]
-  int row_groups;                 // 16-row groups per CTA (1 or 4); DV_WARPS / row_groups splits
-  int stages;                     // ring depth per warp (<= DV_STAGES_MAX)
   const uint8_t *S, *S3;          // scales [E][R][K/32] (S3: SwiGLU linear branch or nullptr)
   int R, K;
   __nv_bfloat16 *out;             // [P][R]
@@ -78,12 +76,6 @@ __device__ __forceinline__ void mma_16816_first(float (&c)[4], uint32_t a0, uint
       "{%8,%9}, {%10,%10,%10,%10};"
       : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
-}
-
-// E8M0 byte -> 2^(s-127) (s = 0 is the fp32 subnormal 2^-127; s = 255, not a
-// valid scale, gives +inf).
-__device__ __forceinline__ float e8m0_fast(uint32_t s) {
-  return __uint_as_float(s ? (s << 23) : 0x00400000u);
 }
 
 // One MX block (32 elements) of rows g and g+8 against 8 tokens.  The block's
@@ -146,32 +138,78 @@ __global__ void rows_to_f16_kernel(const __nv_bfloat16 *__restrict__ src,
   }
 }
 
-// EPI: 0 none, 1 relu, 2 swiglu (tm3 / S3 hold the linear branch).
+// Group barrier on named barrier 1 + id over n threads: returns the OR of
+// pred over the group (every thread gets the same answer).
+__device__ __forceinline__ bool group_sync_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(1 + id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// Shared-memory plan of the decode kernel (bytes from the 1024-aligned base).
+struct DecodePlan {
+  int KB;          // MX blocks per row
+  int bps;         // blocks per reduction split
+  int PP;          // decoded-scale row pitch (u32) of one warp
+  int sc_pitch;    // raw scale bytes of one unit and matrix, padded to 16
+  size_t raw_off, pairs_off, red_off, bytes;
+};
+
+__host__ __device__ inline DecodePlan decode_plan(int nmat, int K, int rg) {
+  DecodePlan p;
+  const int ks = DV_WARPS / rg;
+  p.KB = K / 32;
+  // an even split point keeps every warp's first raw scale byte 2-byte aligned
+  p.bps = (((p.KB + ks - 1) / ks) + 1) & ~1;
+  p.PP = (p.bps + 7) & ~7;
+  if (p.PP % 32 == 0) p.PP += 8;   // rows g and g + 1 of a quarter-warp on other banks
+  p.sc_pitch = (16 * rg * p.KB + 15) & ~15;
+  p.raw_off = (size_t)DV_WARPS * DV_STAGES * nmat * DV_BOX;
+  p.pairs_off = p.raw_off + (size_t)nmat * p.sc_pitch;
+  p.red_off = p.pairs_off + (size_t)DV_WARPS * nmat * 8 * p.PP * 4;
+  const int red_vals = ks == 2 ? 4 : 8;
+  p.bytes = p.red_off + (size_t)2 * DV_WARPS * red_vals * 32 * 4;
+  return p;
+}
+
+// EPI: 0 none, 1 relu, 2 swiglu (tm3 / S3 hold the linear branch).  RG: 16-row
+// groups per CTA; the KS = DV_WARPS / RG warps of a group split the reduction
+// into contiguous, equal runs of MX blocks.
 //
 // Persistent: the grid is sized to the GPU and each CTA walks its share of the
-// work units (selected expert x 16 * row_groups output rows), slot-major.  Its
-// DV_WARPS warps form row_groups groups of DV_WARPS / row_groups warps; the
-// warps of a group split the reduction into contiguous runs of 128-byte
-// boxes.  Each warp keeps its own ring of boxes per matrix in flight; lane 0
+// work units (selected expert x 16 * RG output rows), slot-major.  The groups
+// of a CTA run independently: the warps of a group meet only on their own
+// named barrier, once per token pass, to add their partial sums.  Each warp
+// keeps its own ring of 128-byte code boxes per matrix in flight; lane 0
 // refills a slot as soon as the warp has read it, with the next box of the
-// warp's sequence — across token passes and units — so the weight stream
-// does not stop at unit boundaries.  Block scales of the next unit are copied
-// while the current one runs (two buffers).  B fragments (the tokens' f16
-// activation rows, a few KB in L2) are loaded a box ahead of their use.  The
-// partial sums of a group are added in warp order by its first warp, which
-// applies the activation and stores.
-template <int EPI>
-__global__ void __launch_bounds__(32 * DV_WARPS)
+// warp's sequence (across token passes and units), so the weight stream does
+// not stop at unit boundaries.  A unit's E8M0 bytes are bulk-copied into
+// shared memory one unit ahead; each warp decodes the part it reads into bf16
+// pairs (row g | row g + 8), so that the inner loop takes eight blocks' scales
+// with two 16-byte loads, and the last warp done with the raw bytes issues the
+// next unit's copy.  B fragments (the tokens' f16 activation rows, a few KB in
+// L2) are loaded at the top of each box, and the next box's lines are
+// prefetched into L1.
+template <int EPI, int RG>
+__global__ void __launch_bounds__(32 * DV_WARPS, 2)
 decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm3,
                     DecodeArgs a) {
   constexpr int NMAT = (EPI == 2) ? 2 : 1;
+  constexpr int KS = DV_WARPS / RG;
+  constexpr int CTA_ROWS = 16 * RG;
+  constexpr int RV = KS == 2 ? 4 : 8;   // partial sums a warp hands over per lane
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  __shared__ uint64_t full[DV_WARPS][DV_STAGES_MAX];
-  __shared__ uint64_t sbar[2];
+  __shared__ uint64_t full[DV_WARPS][DV_STAGES];
+  __shared__ uint64_t sbar;
   __shared__ int s_abort;
   __shared__ int s_nactive;
-  __shared__ int s_active[257];
-  __shared__ float red[DV_WARPS][32][8];
+  __shared__ unsigned s_raw_done;
+  __shared__ int s_active[256], s_beg[256], s_cnt[256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (status_failed(a.status)) return;
 
@@ -191,7 +229,12 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       const bool ne = e < a.num_experts && off_hi[j] > off_lo[j];
       if (e < a.num_experts && (off_lo[j] < 0 || off_hi[j] < off_lo[j] || off_hi[j] > a.P)) bad = 1;
       const unsigned m = __ballot_sync(0xffffffffu, ne);
-      if (ne) s_active[seen + __popc(m & lanemask_lt())] = e;
+      if (ne) {
+        const int q = seen + __popc(m & lanemask_lt());
+        s_active[q] = e;
+        s_beg[q] = off_lo[j];
+        s_cnt[q] = off_hi[j] - off_lo[j];
+      }
       seen += __popc(m);
     }
     bad = __any_sync(0xffffffffu, bad);
@@ -199,139 +242,194 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       s_nactive = bad ? 0 : seen;
       if (bad) set_status(a.status, MOE_ERR_BAD_INDEX, -1);
       s_abort = 0;
-      tc::mbar_init(&sbar[0], 1);
-      tc::mbar_init(&sbar[1], 1);
+      s_raw_done = 0;
+      tc::mbar_init(&sbar, 1);
     }
   }
   if (lane == 0) {
-    for (int st = 0; st < DV_STAGES_MAX; ++st) tc::mbar_init(&full[warp][st], 1);
+    for (int st = 0; st < DV_STAGES; ++st) tc::mbar_init(&full[warp][st], 1);
     tc::fence_mbar_init();
   }
   __syncthreads();
   uint8_t *smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
-  const int K = a.K, R = a.R, S = a.stages;
-  const int RG = a.row_groups, KS = DV_WARPS / RG;
+  const DecodePlan plan = decode_plan(NMAT, a.K, RG);
+  const int K = a.K, R = a.R, KB = plan.KB, PP = plan.PP, sc_pitch = plan.sc_pitch;
   const int grp = warp / KS, split = warp - grp * KS;
-  const int KB = K / 32;                                // MX blocks per row
-  const int NC = (K / 2 + DV_BOXB - 1) / DV_BOXB;       // boxes per row
-  const int per_warp = (NC + KS - 1) / KS;
-  const int c_beg = min(NC, split * per_warp), c_end = min(NC, c_beg + per_warp);
-  const int cta_rows = 16 * RG;
-  const int row_blocks = (R + cta_rows - 1) / cta_rows;
+  const int b_beg = min(KB, split * plan.bps), b_end = min(KB, b_beg + plan.bps);
+  const int nbl = b_end - b_beg;                        // this warp's MX blocks per row
+  const int nbox = (nbl + 7) / 8;
+  const int row_blocks = (R + CTA_ROWS - 1) / CTA_ROWS;
   const int total = s_nactive * row_blocks;
-  const int sc_bytes = cta_rows * KB;                   // one unit's rows, one matrix
-  const int sc_pitch = (sc_bytes + 15) & ~15;
-  uint8_t *ring = smem + (size_t)warp * S * NMAT * DV_BOX;
-  uint8_t *scl_base = smem + (size_t)DV_WARPS * S * NMAT * DV_BOX;
+  uint8_t *ring = smem + (size_t)warp * DV_STAGES * NMAT * DV_BOX;
+  const uint8_t *raw = smem + plan.raw_off;
+  uint32_t *pw = reinterpret_cast<uint32_t *>(smem + plan.pairs_off) + (size_t)warp * NMAT * 8 * PP;
+  float *red = reinterpret_cast<float *>(smem + plan.red_off);   // [2][DV_WARPS][RV][32]
   const int g = lane >> 2, t = lane & 3;
+  // byte offset of word t of 16-byte chunk (bl ^ g) in row g of a box with
+  // the 128-byte swizzle: lane_off ^ (bl << 4)
+  const uint32_t lane_off = (uint32_t)(g * DV_BOXB + (g << 4) + 4 * t);
   volatile int *abort = &s_abort;
 
-  // unit i of this CTA -> (expert, first row); token passes of a unit
-  auto unit_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
-  auto expert_of = [&](int u) { return s_active[u / row_blocks]; };
-  auto row0_of = [&](int u) { return (u % row_blocks) * cta_rows; };
-  auto passes_of = [&](int u) {
-    const int e = expert_of(u);
-    return (a.offsets[e + 1] - a.offsets[e] + DV_TOK - 1) / DV_TOK;
-  };
-  // scales of unit i -> buffer i & 1 (thread 0 only; sf_phase: parity of the
-  // last copy issued into each buffer, -1 if none)
-  int sf_phase[2] = {-1, -1};
-  auto fetch_scales = [&](int i) {
-    const int u = unit_of(i);
+  // raw E8M0 bytes of this CTA's unit i (one buffer, one copy in flight; the
+  // thread that issued the last copy drains it on abort)
+  int raw_mine = -1;
+  auto fetch_raw = [&](int i) {
+    const int u = (int)blockIdx.x + i * (int)gridDim.x;
     if (u >= total) return;
-    sf_phase[i & 1] = (i >> 1) & 1;
-    const int e = expert_of(u), r0 = row0_of(u);
-    const int rows = min(cta_rows, R - r0);
-    const uint32_t bytes = (uint32_t)rows * KB;         // a multiple of 16 (rows % 16 == 0)
-    uint8_t *dst = scl_base + (size_t)(i & 1) * NMAT * sc_pitch;
-    tc::mbar_arrive_expect_tx(&sbar[i & 1], NMAT * bytes);
-    bulk_load(dst, a.S + ((size_t)e * R + r0) * KB, bytes, &sbar[i & 1]);
-    if (NMAT == 2) bulk_load(dst + sc_pitch, a.S3 + ((size_t)e * R + r0) * KB, bytes, &sbar[i & 1]);
+    const int sl = u / row_blocks;
+    const int e = s_active[sl], r0 = (u - sl * row_blocks) * CTA_ROWS;
+    const uint32_t bytes = (uint32_t)min(CTA_ROWS, R - r0) * KB;   // rows % 16 == 0
+    tc::mbar_arrive_expect_tx(&sbar, NMAT * bytes);
+    uint8_t *dst = smem + plan.raw_off;
+    bulk_load(dst, a.S + ((size_t)e * R + r0) * KB, bytes, &sbar);
+    if (NMAT == 2) bulk_load(dst + sc_pitch, a.S3 + ((size_t)e * R + r0) * KB, bytes, &sbar);
+    raw_mine = i;
   };
-  // the producer's cursor over this warp's boxes: (unit i, pass p, box c)
-  int pi = 0, pp = 0, pc = c_beg, issued = 0;
-  bool pvalid = c_beg < c_end && unit_of(0) < total;
+
+  // the producer's cursor over this warp's boxes (lane 0): unit p_i, pass
+  // p_pass, box p_c; p_wrow is the first weight row of the warp's group
+  int p_i = 0, p_pass = 0, p_c = 0, p_passes = 0, p_wrow = 0, issued = 0;
+  bool p_valid = false, p_active = false;
+  auto p_load_unit = [&]() {
+    const int u = (int)blockIdx.x + p_i * (int)gridDim.x;
+    p_valid = nbox > 0 && u < total;
+    if (!p_valid) return;
+    const int sl = u / row_blocks;
+    const int r = (u - sl * row_blocks) * CTA_ROWS + grp * 16;
+    p_active = r < R;
+    p_wrow = s_active[sl] * R + r;
+    p_passes = (s_cnt[sl] + DV_TOK - 1) / DV_TOK;
+  };
   auto issue_next = [&]() {
-    if (!pvalid) return;
-    const int u = unit_of(pi);
-    const int r0 = row0_of(u) + grp * 16;
-    const int slot = issued % S;
-    if (r0 < R) {
-      tc::mbar_arrive_expect_tx(&full[warp][slot], NMAT * DV_BOX);
-      uint8_t *dst = ring + (size_t)slot * NMAT * DV_BOX;
-      const int wrow = expert_of(u) * R + r0;
-      tc::tma_load_2d(&tm1, &full[warp][slot], dst, pc * DV_BOXB, wrow);
-      if (NMAT == 2) tc::tma_load_2d(&tm3, &full[warp][slot], dst + DV_BOX, pc * DV_BOXB, wrow);
+    if (!p_valid) return;
+    const int sl = issued & (DV_STAGES - 1);
+    if (p_active) {
+      tc::mbar_arrive_expect_tx(&full[warp][sl], NMAT * DV_BOX);
+      uint8_t *dst = ring + (size_t)sl * NMAT * DV_BOX;
+      const int x = (b_beg + 8 * p_c) * 16;             // a multiple of 16 bytes
+      tc::tma_load_2d(&tm1, &full[warp][sl], dst, x, p_wrow);
+      if (NMAT == 2) tc::tma_load_2d(&tm3, &full[warp][sl], dst + DV_BOX, x, p_wrow);
     } else {
-      tc::mbar_arrive(&full[warp][slot]);   // a group past the last row: keep the phases in step
+      tc::mbar_arrive(&full[warp][sl]);   // a group past the last row: keep the phases in step
     }
     ++issued;
-    if (++pc == c_end) {
-      pc = c_beg;
-      if (++pp == passes_of(u)) {
-        pp = 0;
-        ++pi;
-        pvalid = unit_of(pi) < total;
+    if (++p_c == nbox) {
+      p_c = 0;
+      if (++p_pass == p_passes) {
+        p_pass = 0;
+        ++p_i;
+        p_load_unit();
       }
     }
   };
 
-  if (threadIdx.x == 0) {
-    fetch_scales(0);
-    fetch_scales(1);
+  if (threadIdx.x == 0) fetch_raw(0);
+  if (lane == 0) {
+    p_load_unit();
+    for (int st = 0; st < DV_STAGES; ++st) issue_next();
   }
-  if (lane == 0)
-    for (int st = 0; st < S; ++st) issue_next();
-  int consumed = 0;
+  int consumed = 0, npass = 0;
+  bool ok = true;
 
-  for (int i = 0; unit_of(i) < total; ++i) {
-    const int u = unit_of(i);
-    const int e = expert_of(u);
-    const int r0 = row0_of(u) + grp * 16;
+  for (int i = 0;; ++i) {
+    const int u = (int)blockIdx.x + i * (int)gridDim.x;
+    if (u >= total) break;
+    const int sl = u / row_blocks;
+    const int r0 = (u - sl * row_blocks) * CTA_ROWS + grp * 16;
     const bool active = r0 < R;
-    const int beg = a.offsets[e], cnt = a.offsets[e + 1] - beg;
-    const uint8_t *scl = scl_base + (size_t)(i & 1) * NMAT * sc_pitch;
-    const uint8_t *s1g = scl + (grp * 16 + g) * KB, *s1h = s1g + 8 * KB;
-    const uint8_t *s3g = s1g + sc_pitch, *s3h = s1h + sc_pitch;
-    bool scales_ready = false;
-    for (int tg = 0; tg < cnt; tg += DV_TOK) {
-      // every thread sees the same decision: a warp that timed out stops the CTA
-      if (__syncthreads_or(*abort)) goto done;
-      bool ok = true;
-      if (!scales_ready && c_beg < c_end) {
-        scales_ready = __all_sync(0xffffffffu, tc::mbar_wait(&sbar[i & 1], (i >> 1) & 1, abort));
-        ok = scales_ready;
-      }
-      const bool xrow_ok = g < cnt - tg;                // token g of this pass exists
-      const uint16_t *xrow = a.act16 + (size_t)(beg + tg + (xrow_ok ? g : 0)) * K + 8 * t;
-      float acc1[4] = {0.f, 0.f, 0.f, 0.f}, acc3[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int c = c_beg; c < c_end && ok; ++c) {
-        const int nb = min(8, KB - c * 8);
-        uint4 bx[8];
+    const int beg = s_beg[sl], cnt = s_cnt[sl];
+
+    // this unit's scales: wait for the raw bytes, decode this warp's part into
+    // pairs; the last warp to finish issues the next unit's copy
+    ok = __all_sync(0xffffffffu, tc::mbar_wait(&sbar, (uint32_t)(i & 1), abort));
+    // the warps of a group leave together, so none waits on a barrier alone
+    if (group_sync_or(grp, 32 * KS, !ok)) { ok = false; break; }
+    {
+      // lane (gg = lane / 4, q = lane % 4) takes blocks 2q, 2q + 1, 2q + 8, ...
+      // of row pair gg: two raw bytes of row gg and two of row gg + 8 per step
+      // (16-bit loads where the row pitch is even: the split point always is)
+      const int gg = lane >> 2, q = lane & 3;
+      const bool even = (KB & 1) == 0;
 #pragma unroll
-        for (int bl = 0; bl < 8; ++bl)
-          bx[bl] = (active && xrow_ok && bl < nb)
-                       ? __ldg(reinterpret_cast<const uint4 *>(xrow + (c * 8 + bl) * 32))
-                       : make_uint4(0u, 0u, 0u, 0u);
-        const int slot = consumed % S;
-        const uint32_t parity = (consumed / S) & 1;
+      for (int m = 0; m < NMAT; ++m) {
+        const uint8_t *src = raw + m * sc_pitch + (grp * 16 + gg) * KB + b_beg;
+        uint32_t *dst = pw + (m * 8 + gg) * PP;
+        for (int b = 2 * q; b < nbl; b += 8) {
+          const bool two = b + 1 < nbl;
+          uint32_t x, y;
+          if (even) {
+            x = *reinterpret_cast<const uint16_t *>(src + b);
+            y = *reinterpret_cast<const uint16_t *>(src + b + 8 * KB);
+          } else {
+            x = src[b] | (two ? (uint32_t)src[b + 1] << 8 : 0u);
+            y = src[b + 8 * KB] | (two ? (uint32_t)src[b + 1 + 8 * KB] << 8 : 0u);
+          }
+          // bf16 of 2^(s-127): s << 7, and 0x0040 (2^-127, a subnormal) for s = 0
+          const uint32_t p0 = __vmaxu2(__byte_perm(x, y, 0x7460) << 7, 0x00400040u);
+          const uint32_t p1 = __vmaxu2(__byte_perm(x, y, 0x7561) << 7, 0x00400040u);
+          if (two) *reinterpret_cast<uint2 *>(dst + b) = make_uint2(p0, p1);
+          else dst[b] = p0;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&s_raw_done, 1u) == (unsigned)((i + 1) * DV_WARPS - 1)) {
+        __threadfence_block();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        fetch_raw(i + 1);
+      }
+    }
+    const uint32_t *pr1 = pw + g * PP;
+    const uint32_t *pr3 = pr1 + 8 * PP;
+
+    for (int tg = 0; tg < cnt; tg += DV_TOK, ++npass) {
+      // token g of this pass, or the pass's last token where g is past it (its
+      // results are not stored)
+      const int tok = tg + min(g, cnt - tg - 1);
+      const uint16_t *xrow = a.act16 + (size_t)(beg + tok) * K + (size_t)b_beg * 32 + 8 * t;
+      const uint16_t *xpf = a.act16 + (size_t)(beg + tg + min(lane >> 2, cnt - tg - 1)) * K +
+                            (size_t)b_beg * 32 + (lane & 3) * 64;
+      float acc1[4] = {0.f, 0.f, 0.f, 0.f}, acc3[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int c = 0; c < nbox; ++c) {
+        const int nb = min(8, nbl - c * 8);
+        const int slot = consumed & (DV_STAGES - 1);
+        const uint32_t parity = (uint32_t)(consumed / DV_STAGES) & 1u;
         ++consumed;
         if (active) {
+          const uint16_t *xb = xrow + c * 256;
+          uint4 bx[8];
+#pragma unroll
+          for (int bl = 0; bl < 8; ++bl)
+            bx[bl] = (bl < nb) ? __ldg(reinterpret_cast<const uint4 *>(xb + bl * 32))
+                               : make_uint4(0u, 0u, 0u, 0u);
+          // the next box's activation lines: one 128-byte line (two blocks) per lane
+          if (c + 1 < nbox && (lane & 3) * 2 < nbl - (c + 1) * 8)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(xpf + (c + 1) * 256));
           ok = __all_sync(0xffffffffu, tc::mbar_wait(&full[warp][slot], parity, abort));
           if (!ok) break;
           const uint8_t *st = ring + (size_t)slot * NMAT * DV_BOX;
+          const uint4 s1a = *reinterpret_cast<const uint4 *>(pr1 + c * 8);
+          const uint4 s1b = *reinterpret_cast<const uint4 *>(pr1 + c * 8 + 4);
+          uint4 s3a = s1a, s3b = s1b;
+          if constexpr (NMAT == 2) {
+            s3a = *reinterpret_cast<const uint4 *>(pr3 + c * 8);
+            s3b = *reinterpret_cast<const uint4 *>(pr3 + c * 8 + 4);
+          }
+          const uint32_t sp1[8] = {s1a.x, s1a.y, s1a.z, s1a.w, s1b.x, s1b.y, s1b.z, s1b.w};
+          const uint32_t sp3[8] = {s3a.x, s3a.y, s3a.z, s3a.w, s3b.x, s3b.y, s3b.z, s3b.w};
           auto block = [&](int bl) {
-            const int bg = c * 8 + bl;
-            const int off = ((bl ^ g) << 4) + 4 * t;
-            const uint32_t wg = *reinterpret_cast<const uint32_t *>(st + g * DV_BOXB + off);
-            const uint32_t wh = *reinterpret_cast<const uint32_t *>(st + (g + 8) * DV_BOXB + off);
-            mx_block(acc1, wg, wh, e8m0_fast(s1g[bg]), e8m0_fast(s1h[bg]), bx[bl]);
+            const uint8_t *w = st + (lane_off ^ (uint32_t)(bl << 4));
+            const uint32_t wg = *reinterpret_cast<const uint32_t *>(w);
+            const uint32_t wh = *reinterpret_cast<const uint32_t *>(w + 8 * DV_BOXB);
+            mx_block(acc1, wg, wh, __uint_as_float(sp1[bl] << 16),
+                     __uint_as_float(sp1[bl] & 0xffff0000u), bx[bl]);
             if constexpr (NMAT == 2) {
-              const uint32_t vg = *reinterpret_cast<const uint32_t *>(st + DV_BOX + g * DV_BOXB + off);
-              const uint32_t vh =
-                  *reinterpret_cast<const uint32_t *>(st + DV_BOX + (g + 8) * DV_BOXB + off);
-              mx_block(acc3, vg, vh, e8m0_fast(s3g[bg]), e8m0_fast(s3h[bg]), bx[bl]);
+              const uint32_t vg = *reinterpret_cast<const uint32_t *>(w + DV_BOX);
+              const uint32_t vh = *reinterpret_cast<const uint32_t *>(w + DV_BOX + 8 * DV_BOXB);
+              mx_block(acc3, vg, vh, __uint_as_float(sp3[bl] << 16),
+                       __uint_as_float(sp3[bl] & 0xffff0000u), bx[bl]);
             }
           };
           if (nb == 8) {
@@ -340,8 +438,14 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
 #pragma unroll
             for (int bl = 0; bl < 8; ++bl) block(bl);
           } else {
-            for (int bl = 0; bl < nb; ++bl) block(bl);
+#pragma unroll
+            for (int bl = 0; bl < 8; ++bl)
+              if (bl < nb) block(bl);
           }
+        } else {
+          // a group past the last row: its slots were arrived on without data
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(&full[warp][slot], parity, abort));
+          if (!ok) break;
         }
         __syncwarp();
         if (lane == 0) {
@@ -351,84 +455,105 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
           issue_next();
         }
       }
-      // partial sums -> the first warp of the group, added in warp order
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        red[warp][lane][q] = acc1[q];
-        red[warp][lane][4 + q] = acc3[q];
-      }
-      if (__syncthreads_or(!ok)) goto done;   // an aborted pass stores nothing
-      if (split == 0 && active) {
-        float s1[4] = {0.f, 0.f, 0.f, 0.f}, s3[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int w = warp; w < warp + KS; ++w)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            s1[q] += red[w][lane][q];
-            s3[q] += red[w][lane][4 + q];
-          }
-        // c0, c1: row g, tokens 2t, 2t+1; c2, c3: row g+8
+      // partial sums of the group's warps, added in warp order.  Two splits:
+      // each warp finishes one row (split 0 row g, split 1 row g + 8) and hands
+      // the other row's sums to its partner.  More splits: the first warp
+      // finishes both rows.
+      float *rb = red + (size_t)(npass & 1) * DV_WARPS * RV * 32;
+      float f1[2], f3[2];   // this warp's finished values: tokens 2t, 2t+1 of its row
+      int frow;
+      bool fin;
+      if constexpr (KS == 2) {
+        const bool s0 = split == 0;
+        // kept: this warp's row; given: the partner's row
+        const float k10 = s0 ? acc1[0] : acc1[2], k11 = s0 ? acc1[1] : acc1[3];
+        const float k30 = s0 ? acc3[0] : acc3[2], k31 = s0 ? acc3[1] : acc3[3];
+        rb[(warp * RV + 0) * 32 + lane] = s0 ? acc1[2] : acc1[0];
+        rb[(warp * RV + 1) * 32 + lane] = s0 ? acc1[3] : acc1[1];
+        rb[(warp * RV + 2) * 32 + lane] = s0 ? acc3[2] : acc3[0];
+        rb[(warp * RV + 3) * 32 + lane] = s0 ? acc3[3] : acc3[1];
+        if (group_sync_or(grp, 32 * KS, !ok)) { ok = false; break; }
+        const int pw_ = warp ^ 1;
+        // warp order: split 0's sum first
+        const float o10 = rb[(pw_ * RV + 0) * 32 + lane], o11 = rb[(pw_ * RV + 1) * 32 + lane];
+        const float o30 = rb[(pw_ * RV + 2) * 32 + lane], o31 = rb[(pw_ * RV + 3) * 32 + lane];
+        f1[0] = s0 ? k10 + o10 : o10 + k10;
+        f1[1] = s0 ? k11 + o11 : o11 + k11;
+        f3[0] = s0 ? k30 + o30 : o30 + k30;
+        f3[1] = s0 ? k31 + o31 : o31 + k31;
+        frow = s0 ? g : g + 8;
+        fin = active;
+      } else {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
+          rb[(warp * RV + q) * 32 + lane] = acc1[q];
+          rb[(warp * RV + 4 + q) * 32 + lane] = acc3[q];
+        }
+        if (group_sync_or(grp, 32 * KS, !ok)) { ok = false; break; }
+        // the first warp finishes row g, the second row g + 8
+        fin = active && split < 2;
+        const int q0 = split == 1 ? 2 : 0;
+        f1[0] = f1[1] = f3[0] = f3[1] = 0.f;
+        if (fin) {
+#pragma unroll
+          for (int w = 0; w < KS; ++w) {
+            const int ww = grp * KS + w;
+            f1[0] += rb[(ww * RV + q0) * 32 + lane];
+            f1[1] += rb[(ww * RV + q0 + 1) * 32 + lane];
+            f3[0] += rb[(ww * RV + 4 + q0) * 32 + lane];
+            f3[1] += rb[(ww * RV + 4 + q0 + 1) * 32 + lane];
+          }
+        }
+        frow = split == 1 ? g + 8 : g;
+      }
+      if (fin) {
+        const int row = r0 + frow;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
           float v;
-          if constexpr (EPI == 2) v = s1[q] / (1.f + __expf(-s1[q])) * s3[q];
-          else if constexpr (EPI == 1) v = fmaxf(s1[q], 0.f);
-          else v = s1[q];
-          const int tok = tg + 2 * t + (q & 1);
-          const int row = r0 + g + ((q >> 1) ? 8 : 0);
-          if (tok < cnt && row < R) {
+          if constexpr (EPI == 2) v = f1[q] / (1.f + __expf(-f1[q])) * f3[q];
+          else if constexpr (EPI == 1) v = fmaxf(f1[q], 0.f);
+          else v = f1[q];
+          const int tk = tg + 2 * t + q;
+          if (tk < cnt && row < R) {
             const __nv_bfloat16 hb = __float2bfloat16_rn(v);
-            a.out[(size_t)(beg + tok) * R + row] = hb;
-            if (a.out16) a.out16[(size_t)(beg + tok) * R + row] = to_f16_bits(__bfloat162float(hb));
+            a.out[(size_t)(beg + tk) * R + row] = hb;
+            if (a.out16) a.out16[(size_t)(beg + tk) * R + row] = to_f16_bits(__bfloat162float(hb));
           }
         }
       }
     }
-    // unit i is done everywhere: its scale buffer takes unit i + 2
-    __syncthreads();
-    if (threadIdx.x == 0) fetch_scales(i + 2);
+    if (!ok) break;
   }
-done:
-  if (*abort) {
-    // let the copies this CTA issued land before it exits
+  if (!ok) {
+    // let the copies this warp issued land before it exits
     if (lane == 0) {
       for (int j = consumed; j < issued; ++j)
-        tc::mbar_wait_drain(&full[warp][j % S], (j / S) & 1, 100000000ull);
-    }
-    if (threadIdx.x == 0) {
-      // scale copies in flight (a completed phase returns at once)
-      for (int b = 0; b < 2; ++b)
-        if (sf_phase[b] >= 0) tc::mbar_wait_drain(&sbar[b], (uint32_t)sf_phase[b], 100000000ull);
+        tc::mbar_wait_drain(&full[warp][j % DV_STAGES], (uint32_t)(j / DV_STAGES) & 1u,
+                            100000000ull);
+      if (raw_mine >= 0)
+        tc::mbar_wait_drain(&sbar, (uint32_t)(raw_mine & 1), 100000000ull);
       set_status(a.status, MOE_ERR_TIMEOUT, blockIdx.x);
     }
   }
 }
 
-size_t decode_smem(int nmat, int K, int row_groups, int stages) {
-  const int KB = K / 32;
-  const size_t sc_pitch = (size_t)((16 * row_groups * KB + 15) & ~15);
-  return 1024 + (size_t)DV_WARPS * stages * nmat * DV_BOX + 2 * (size_t)nmat * sc_pitch;
-}
-
-template <int EPI>
+template <int EPI, int RG>
 cudaError_t launch_one(DecodeArgs a, const uint8_t *W, const uint8_t *W3, int num_experts,
                        int slots, cudaStream_t s) {
   constexpr int NMAT = (EPI == 2) ? 2 : 1;
-  const int KS = DV_WARPS / a.row_groups;
-  const int NC = (a.K / 2 + DV_BOXB - 1) / DV_BOXB;
-  const int per_warp = (NC + KS - 1) / KS;
-  a.stages = per_warp < DV_STAGES_MAX ? (per_warp > 0 ? per_warp : 1) : DV_STAGES_MAX;
-  const size_t smem = decode_smem(NMAT, a.K, a.row_groups, a.stages);
+  const size_t smem = 1024 + decode_plan(NMAT, a.K, RG).bytes;
   static size_t smem_set = 0;
   static int per_sm = 0;
   if (smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mxfp4_kernel<EPI>,
+    cudaError_t e = cudaFuncSetAttribute(decode_mxfp4_kernel<EPI, RG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     smem_set = smem;
     per_sm = 0;
   }
   if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mxfp4_kernel<EPI>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mxfp4_kernel<EPI, RG>,
                                                       32 * DV_WARPS, smem) != cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
@@ -447,13 +572,19 @@ cudaError_t launch_one(DecodeArgs a, const uint8_t *W, const uint8_t *W3, int nu
     m3 = m1;
   }
   // units: at most `slots` experts x row blocks; no more CTAs than units
-  const int cta_rows = 16 * a.row_groups;
-  const long units = (long)slots * ((a.R + cta_rows - 1) / cta_rows);
+  const long units = (long)slots * ((a.R + 16 * RG - 1) / (16 * RG));
   long grid = (long)per_sm * num_sms();
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
-  decode_mxfp4_kernel<EPI><<<(unsigned)grid, 32 * DV_WARPS, smem, s>>>(m1, m3, a);
+  decode_mxfp4_kernel<EPI, RG><<<(unsigned)grid, 32 * DV_WARPS, smem, s>>>(m1, m3, a);
   return cudaGetLastError();
+}
+
+template <int EPI>
+cudaError_t launch_rg(DecodeArgs a, int row_groups, const uint8_t *W, const uint8_t *W3,
+                      int num_experts, int slots, cudaStream_t s) {
+  return row_groups == 1 ? launch_one<EPI, 1>(a, W, W3, num_experts, slots, s)
+                         : launch_one<EPI, 4>(a, W, W3, num_experts, slots, s);
 }
 
 }  // namespace
@@ -494,7 +625,7 @@ cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
   a.status = status;
   // few tokens per expert: eight reduction splits per 16 rows for parallelism;
   // more tokens: 64 rows per CTA, each staged B fragment serving more weights
-  a.row_groups = c.n <= 2 ? 1 : 4;
+  const int row_groups = c.n <= 2 ? 1 : 4;
   if (part == 0) {
     cudaError_t e = launch_rows_to_f16(act, perm, c.top_k, P, c.d, x16, status, s);
     if (e != cudaSuccess) return e;
@@ -506,8 +637,8 @@ cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
     a.out = static_cast<__nv_bfloat16 *>(h);
     a.out16 = h16;
     const uint8_t *W1 = static_cast<const uint8_t *>(w.W1), *W3 = static_cast<const uint8_t *>(w.W3);
-    return c.act == MOE_ACT_SWIGLU ? launch_one<2>(a, W1, W3, c.n_experts, slots, s)
-                                   : launch_one<1>(a, W1, nullptr, c.n_experts, slots, s);
+    return c.act == MOE_ACT_SWIGLU ? launch_rg<2>(a, row_groups, W1, W3, c.n_experts, slots, s)
+                                   : launch_rg<1>(a, row_groups, W1, nullptr, c.n_experts, slots, s);
   }
   a.act16 = h16;
   a.S = w.S2;
@@ -516,7 +647,8 @@ cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
   a.K = c.d_ff;
   a.out = static_cast<__nv_bfloat16 *>(y_perm);
   a.out16 = nullptr;
-  return launch_one<0>(a, static_cast<const uint8_t *>(w.W2), nullptr, c.n_experts, slots, s);
+  return launch_rg<0>(a, row_groups, static_cast<const uint8_t *>(w.W2), nullptr, c.n_experts,
+                      slots, s);
 }
 
 }  // namespace moe

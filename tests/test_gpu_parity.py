@@ -39,6 +39,8 @@ SMALL = {
     "decode_many_tokens_per_expert": C["gptoss_decode_mxfp4"].scaled(n=64, d=256, d_ff=320, E=4),
     "decode_relu_small": C["gptoss_decode_mxfp4"].scaled(n=16, d=128, d_ff=192, E=8, k=2,
                                                          act="relu"),
+    # an odd number of MX blocks per row (3 and 5) on both projections
+    "decode_odd_blocks": C["gptoss_decode_mxfp4"].scaled(n=4, d=96, d_ff=160, E=8, k=2),
     "prefill_zipf_small": C["gptoss_prefill_zipf_mxfp4"].scaled(n=600, d=256, d_ff=320, E=16),
     "finegrained_small": C["finegrained_shared_bf16"].scaled(n=500, d=256, d_ff=128, E=32,
                                                              d_ff_shared=192),
@@ -242,7 +244,7 @@ def test_combine_bad_inverse_reported(lib):
 
 @pytest.mark.parametrize("name", ["tiny_switch_fp32", "mixtral_small", "prefill_zipf_small",
                                   "decode_n4", "decode_many_tokens_per_expert",
-                                  "decode_relu_small"])
+                                  "decode_relu_small", "decode_odd_blocks"])
 def test_expert_ffn_segments(lib, name):
     cfg = SMALL[name]
     inputs = moe_synth.make_inputs(cfg, seed=8, device="cuda")
