@@ -169,7 +169,7 @@ __host__ __device__ inline DecodePlan decode_plan(int nmat, int K, int rg) {
   p.PP = (p.bps + 7) & ~7;
   if (p.PP % 32 == 0) p.PP += 8;   // rows g and g + 1 of a quarter-warp on other banks
   p.sc_pitch = (16 * rg * p.KB + 15) & ~15;
-  p.raw_off = (size_t)DV_WARPS * DV_STAGES * nmat * DV_BOX;
+  p.raw_off = (size_t)DV_WARPS * DV_STAGES * 2 * DV_BOX;
   p.pairs_off = p.raw_off + (size_t)nmat * p.sc_pitch;
   p.red_off = p.pairs_off + (size_t)DV_WARPS * nmat * 8 * p.PP * 4;
   const int red_vals = ks == 2 ? 4 : 8;
@@ -257,10 +257,14 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   const int grp = warp / KS, split = warp - grp * KS;
   const int b_beg = min(KB, split * plan.bps), b_end = min(KB, b_beg + plan.bps);
   const int nbl = b_end - b_beg;                        // this warp's MX blocks per row
-  const int nbox = (nbl + 7) / 8;
+  // a ring slot holds two 16 x 128-byte boxes: the same 8 MX blocks of both
+  // matrices (SwiGLU), or 16 consecutive blocks of the one matrix
+  constexpr int SUB = (NMAT == 2) ? 1 : 2;              // 8-block groups per slot
+  constexpr int SB = 8 * SUB;                           // MX blocks per slot
+  const int nslot = (nbl + SB - 1) / SB;
   const int row_blocks = (R + CTA_ROWS - 1) / CTA_ROWS;
   const int total = s_nactive * row_blocks;
-  uint8_t *ring = smem + (size_t)warp * DV_STAGES * NMAT * DV_BOX;
+  uint8_t *ring = smem + (size_t)warp * DV_STAGES * 2 * DV_BOX;
   const uint8_t *raw = smem + plan.raw_off;
   uint32_t *pw = reinterpret_cast<uint32_t *>(smem + plan.pairs_off) + (size_t)warp * NMAT * 8 * PP;
   float *red = reinterpret_cast<float *>(smem + plan.red_off);   // [2][DV_WARPS][RV][32]
@@ -292,7 +296,7 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   bool p_valid = false, p_active = false;
   auto p_load_unit = [&]() {
     const int u = (int)blockIdx.x + p_i * (int)gridDim.x;
-    p_valid = nbox > 0 && u < total;
+    p_valid = nslot > 0 && u < total;
     if (!p_valid) return;
     const int sl = u / row_blocks;
     const int r = (u - sl * row_blocks) * CTA_ROWS + grp * 16;
@@ -304,16 +308,18 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     if (!p_valid) return;
     const int sl = issued & (DV_STAGES - 1);
     if (p_active) {
-      tc::mbar_arrive_expect_tx(&full[warp][sl], NMAT * DV_BOX);
-      uint8_t *dst = ring + (size_t)sl * NMAT * DV_BOX;
-      const int x = (b_beg + 8 * p_c) * 16;             // a multiple of 16 bytes
+      tc::mbar_arrive_expect_tx(&full[warp][sl], 2 * DV_BOX);
+      uint8_t *dst = ring + (size_t)sl * 2 * DV_BOX;
+      const int x = (b_beg + SB * p_c) * 16;            // a multiple of 16 bytes
       tc::tma_load_2d(&tm1, &full[warp][sl], dst, x, p_wrow);
+      // (a box past the end of the row reads zeros)
       if (NMAT == 2) tc::tma_load_2d(&tm3, &full[warp][sl], dst + DV_BOX, x, p_wrow);
+      else tc::tma_load_2d(&tm1, &full[warp][sl], dst + DV_BOX, x + DV_BOXB, p_wrow);
     } else {
       tc::mbar_arrive(&full[warp][sl]);   // a group past the last row: keep the phases in step
     }
     ++issued;
-    if (++p_c == nbox) {
+    if (++p_c == nslot) {
       p_c = 0;
       if (++p_pass == p_passes) {
         p_pass = 0;
@@ -392,55 +398,73 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       const uint16_t *xpf = a.act16 + (size_t)(beg + tg + min(lane >> 2, cnt - tg - 1)) * K +
                             (size_t)b_beg * 32 + (lane & 3) * 64;
       float acc1[4] = {0.f, 0.f, 0.f, 0.f}, acc3[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int c = 0; c < nbox; ++c) {
-        const int nb = min(8, nbl - c * 8);
+      uint4 bx[8];
+      // B fragments of the 8-block group starting at local block cb
+      auto load_bx = [&](int cb, int nb) {
+        const uint16_t *xb = xrow + cb * 32;
+#pragma unroll
+        for (int bl = 0; bl < 8; ++bl)
+          bx[bl] = (bl < nb) ? __ldg(reinterpret_cast<const uint4 *>(xb + bl * 32))
+                             : make_uint4(0u, 0u, 0u, 0u);
+      };
+      // the 8-block group at local block cb: matrix 1 in box sw (matrix 3,
+      // SwiGLU, in the box after it)
+      auto compute8 = [&](const uint8_t *sw, int cb, int nb) {
+        const uint4 s1a = *reinterpret_cast<const uint4 *>(pr1 + cb);
+        const uint4 s1b = *reinterpret_cast<const uint4 *>(pr1 + cb + 4);
+        uint4 s3a = s1a, s3b = s1b;
+        if constexpr (NMAT == 2) {
+          s3a = *reinterpret_cast<const uint4 *>(pr3 + cb);
+          s3b = *reinterpret_cast<const uint4 *>(pr3 + cb + 4);
+        }
+        const uint32_t sp1[8] = {s1a.x, s1a.y, s1a.z, s1a.w, s1b.x, s1b.y, s1b.z, s1b.w};
+        const uint32_t sp3[8] = {s3a.x, s3a.y, s3a.z, s3a.w, s3b.x, s3b.y, s3b.z, s3b.w};
+        auto block = [&](int bl) {
+          const uint8_t *w = sw + (lane_off ^ (uint32_t)(bl << 4));
+          const uint32_t wg = *reinterpret_cast<const uint32_t *>(w);
+          const uint32_t wh = *reinterpret_cast<const uint32_t *>(w + 8 * DV_BOXB);
+          mx_block(acc1, wg, wh, __uint_as_float(sp1[bl] << 16),
+                   __uint_as_float(sp1[bl] & 0xffff0000u), bx[bl]);
+          if constexpr (NMAT == 2) {
+            const uint32_t vg = *reinterpret_cast<const uint32_t *>(w + DV_BOX);
+            const uint32_t vh = *reinterpret_cast<const uint32_t *>(w + DV_BOX + 8 * DV_BOXB);
+            mx_block(acc3, vg, vh, __uint_as_float(sp3[bl] << 16),
+                     __uint_as_float(sp3[bl] & 0xffff0000u), bx[bl]);
+          }
+        };
+        if (nb == 8) {
+          // a full group: straight-line code, so the eight blocks' independent
+          // MMA chains can be interleaved
+#pragma unroll
+          for (int bl = 0; bl < 8; ++bl) block(bl);
+        } else {
+#pragma unroll
+          for (int bl = 0; bl < 8; ++bl)
+            if (bl < nb) block(bl);
+        }
+      };
+      for (int c = 0; c < nslot; ++c) {
+        const int cb = c * SB;
         const int slot = consumed & (DV_STAGES - 1);
         const uint32_t parity = (uint32_t)(consumed / DV_STAGES) & 1u;
         ++consumed;
         if (active) {
-          const uint16_t *xb = xrow + c * 256;
-          uint4 bx[8];
+          load_bx(cb, min(8, nbl - cb));
+          // the next slot's activation lines: one 128-byte line (two blocks)
+          // per lane and 8-block group
 #pragma unroll
-          for (int bl = 0; bl < 8; ++bl)
-            bx[bl] = (bl < nb) ? __ldg(reinterpret_cast<const uint4 *>(xb + bl * 32))
-                               : make_uint4(0u, 0u, 0u, 0u);
-          // the next box's activation lines: one 128-byte line (two blocks) per lane
-          if (c + 1 < nbox && (lane & 3) * 2 < nbl - (c + 1) * 8)
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(xpf + (c + 1) * 256));
+          for (int h = 0; h < SUB; ++h)
+            if (c + 1 < nslot && (lane & 3) * 2 < nbl - (cb + SB + 8 * h))
+              asm volatile("prefetch.global.L1 [%0];" ::"l"(xpf + (cb + SB + 8 * h) * 32));
           ok = __all_sync(0xffffffffu, tc::mbar_wait(&full[warp][slot], parity, abort));
           if (!ok) break;
-          const uint8_t *st = ring + (size_t)slot * NMAT * DV_BOX;
-          const uint4 s1a = *reinterpret_cast<const uint4 *>(pr1 + c * 8);
-          const uint4 s1b = *reinterpret_cast<const uint4 *>(pr1 + c * 8 + 4);
-          uint4 s3a = s1a, s3b = s1b;
-          if constexpr (NMAT == 2) {
-            s3a = *reinterpret_cast<const uint4 *>(pr3 + c * 8);
-            s3b = *reinterpret_cast<const uint4 *>(pr3 + c * 8 + 4);
-          }
-          const uint32_t sp1[8] = {s1a.x, s1a.y, s1a.z, s1a.w, s1b.x, s1b.y, s1b.z, s1b.w};
-          const uint32_t sp3[8] = {s3a.x, s3a.y, s3a.z, s3a.w, s3b.x, s3b.y, s3b.z, s3b.w};
-          auto block = [&](int bl) {
-            const uint8_t *w = st + (lane_off ^ (uint32_t)(bl << 4));
-            const uint32_t wg = *reinterpret_cast<const uint32_t *>(w);
-            const uint32_t wh = *reinterpret_cast<const uint32_t *>(w + 8 * DV_BOXB);
-            mx_block(acc1, wg, wh, __uint_as_float(sp1[bl] << 16),
-                     __uint_as_float(sp1[bl] & 0xffff0000u), bx[bl]);
-            if constexpr (NMAT == 2) {
-              const uint32_t vg = *reinterpret_cast<const uint32_t *>(w + DV_BOX);
-              const uint32_t vh = *reinterpret_cast<const uint32_t *>(w + DV_BOX + 8 * DV_BOXB);
-              mx_block(acc3, vg, vh, __uint_as_float(sp3[bl] << 16),
-                       __uint_as_float(sp3[bl] & 0xffff0000u), bx[bl]);
+          const uint8_t *st = ring + (size_t)slot * 2 * DV_BOX;
+          compute8(st, cb, min(8, nbl - cb));
+          if constexpr (SUB == 2) {
+            if (nbl - cb > 8) {
+              load_bx(cb + 8, min(8, nbl - cb - 8));
+              compute8(st + DV_BOX, cb + 8, min(8, nbl - cb - 8));
             }
-          };
-          if (nb == 8) {
-            // a full box: straight-line code, so the eight blocks' independent
-            // MMA chains can be interleaved
-#pragma unroll
-            for (int bl = 0; bl < 8; ++bl) block(bl);
-          } else {
-#pragma unroll
-            for (int bl = 0; bl < 8; ++bl)
-              if (bl < nb) block(bl);
           }
         } else {
           // a group past the last row: its slots were arrived on without data
