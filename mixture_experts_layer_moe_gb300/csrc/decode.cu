@@ -38,7 +38,9 @@ struct DecodeArgs {
   const int32_t *offsets;
   int num_experts;
   int P;
-  const uint16_t *act16;          // f16 activation rows in segment order [P][K]
+  const uint16_t *act16;          // f16 activation rows: segment order [P][K], or token order
+  const int32_t *perm;            // (token order) segment position -> pair t*top_k + j, else nullptr
+  int top_k;
   const uint8_t *S, *S3;          // scales [E][R][K/32] (S3: SwiGLU linear branch or nullptr)
   int R, K;
   __nv_bfloat16 *out;             // [P][R]
@@ -157,6 +159,7 @@ struct DecodePlan {
   int bps;         // blocks per reduction split
   int PP;          // decoded-scale row pitch (u32) of one warp
   int sc_pitch;    // raw scale bytes of one unit and matrix, padded to 16
+  int nraw;        // raw scale buffers (two for short units: copies run two units ahead)
   size_t raw_off, pairs_off, red_off, bytes;
 };
 
@@ -169,8 +172,9 @@ __host__ __device__ inline DecodePlan decode_plan(int nmat, int K, int rg) {
   p.PP = (p.bps + 7) & ~7;
   if (p.PP % 32 == 0) p.PP += 8;   // rows g and g + 1 of a quarter-warp on other banks
   p.sc_pitch = (16 * rg * p.KB + 15) & ~15;
+  p.nraw = rg == 1 ? 2 : 1;
   p.raw_off = (size_t)DV_WARPS * DV_STAGES * 2 * DV_BOX;
-  p.pairs_off = p.raw_off + (size_t)nmat * p.sc_pitch;
+  p.pairs_off = p.raw_off + (size_t)p.nraw * nmat * p.sc_pitch;
   p.red_off = p.pairs_off + (size_t)DV_WARPS * nmat * 8 * p.PP * 4;
   const int red_vals = ks == 2 ? 4 : 8;
   p.bytes = p.red_off + (size_t)2 * DV_WARPS * red_vals * 32 * 4;
@@ -189,12 +193,13 @@ __host__ __device__ inline DecodePlan decode_plan(int nmat, int K, int rg) {
 // refills a slot as soon as the warp has read it, with the next box of the
 // warp's sequence (across token passes and units), so the weight stream does
 // not stop at unit boundaries.  A unit's E8M0 bytes are bulk-copied into
-// shared memory one unit ahead; each warp decodes the part it reads into bf16
-// pairs (row g | row g + 8), so that the inner loop takes eight blocks' scales
-// with two 16-byte loads, and the last warp done with the raw bytes issues the
-// next unit's copy.  B fragments (the tokens' f16 activation rows, a few KB in
-// L2) are loaded at the top of each box, and the next box's lines are
-// prefetched into L1.
+// shared memory ahead of it (one unit ahead, two for short 16-row units);
+// each warp decodes the part it reads into bf16 pairs (row g | row g + 8), so
+// that the inner loop takes eight blocks' scales with two 16-byte loads, and
+// the last warp done with a raw buffer issues the copy for the unit that uses
+// it next.  B fragments (the tokens' f16 activation rows, a few KB in L2) are
+// loaded at the top of each slot, and the next slot's lines are prefetched
+// into L1.
 template <int EPI, int RG>
 __global__ void __launch_bounds__(32 * DV_WARPS, 2)
 decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm3,
@@ -205,11 +210,12 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   constexpr int RV = KS == 2 ? 4 : 8;   // partial sums a warp hands over per lane
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ uint64_t full[DV_WARPS][DV_STAGES];
-  __shared__ uint64_t sbar;
+  __shared__ uint64_t sbar[2];
   __shared__ int s_abort;
   __shared__ int s_nactive;
   __shared__ unsigned s_raw_done;
   __shared__ int s_active[256], s_beg[256], s_cnt[256];
+  __shared__ int s_row[kDecodeMaxPairs];          // activation row of each segment position
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (status_failed(a.status)) return;
 
@@ -243,7 +249,19 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       if (bad) set_status(a.status, MOE_ERR_BAD_INDEX, -1);
       s_abort = 0;
       s_raw_done = 0;
-      tc::mbar_init(&sbar, 1);
+      tc::mbar_init(&sbar[0], 1);
+      tc::mbar_init(&sbar[1], 1);
+    }
+  }
+  if (warp == 1) {
+    for (int q = lane; q < a.P; q += 32) {
+      int row = q;
+      if (a.perm) {
+        const int p = a.perm[q];
+        row = (p >= 0 && p < a.P) ? p / a.top_k : 0;
+        if (p < 0 || p >= a.P) set_status(a.status, MOE_ERR_BAD_INDEX, q);
+      }
+      s_row[q] = row;
     }
   }
   if (lane == 0) {
@@ -265,7 +283,7 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   const int row_blocks = (R + CTA_ROWS - 1) / CTA_ROWS;
   const int total = s_nactive * row_blocks;
   uint8_t *ring = smem + (size_t)warp * DV_STAGES * 2 * DV_BOX;
-  const uint8_t *raw = smem + plan.raw_off;
+  const int NRAW = plan.nraw;
   uint32_t *pw = reinterpret_cast<uint32_t *>(smem + plan.pairs_off) + (size_t)warp * NMAT * 8 * PP;
   float *red = reinterpret_cast<float *>(smem + plan.red_off);   // [2][DV_WARPS][RV][32]
   const int g = lane >> 2, t = lane & 3;
@@ -274,20 +292,22 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   const uint32_t lane_off = (uint32_t)(g * DV_BOXB + (g << 4) + 4 * t);
   volatile int *abort = &s_abort;
 
-  // raw E8M0 bytes of this CTA's unit i (one buffer, one copy in flight; the
-  // thread that issued the last copy drains it on abort)
-  int raw_mine = -1;
+  // raw E8M0 bytes of this CTA's unit i into buffer i % NRAW (NRAW copies in
+  // flight at most; a thread drains the copies it issued on abort)
+  int raw_mine0 = -1, raw_mine1 = -1;   // last unit copied into buffer 0 / 1
   auto fetch_raw = [&](int i) {
     const int u = (int)blockIdx.x + i * (int)gridDim.x;
     if (u >= total) return;
     const int sl = u / row_blocks;
     const int e = s_active[sl], r0 = (u - sl * row_blocks) * CTA_ROWS;
     const uint32_t bytes = (uint32_t)min(CTA_ROWS, R - r0) * KB;   // rows % 16 == 0
-    tc::mbar_arrive_expect_tx(&sbar, NMAT * bytes);
-    uint8_t *dst = smem + plan.raw_off;
-    bulk_load(dst, a.S + ((size_t)e * R + r0) * KB, bytes, &sbar);
-    if (NMAT == 2) bulk_load(dst + sc_pitch, a.S3 + ((size_t)e * R + r0) * KB, bytes, &sbar);
-    raw_mine = i;
+    const int b = i % NRAW;
+    tc::mbar_arrive_expect_tx(&sbar[b], NMAT * bytes);
+    uint8_t *dst = smem + plan.raw_off + (size_t)b * NMAT * sc_pitch;
+    bulk_load(dst, a.S + ((size_t)e * R + r0) * KB, bytes, &sbar[b]);
+    if (NMAT == 2) bulk_load(dst + sc_pitch, a.S3 + ((size_t)e * R + r0) * KB, bytes, &sbar[b]);
+    if (b) raw_mine1 = i;
+    else raw_mine0 = i;
   };
 
   // the producer's cursor over this warp's boxes (lane 0): unit p_i, pass
@@ -329,7 +349,8 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     }
   };
 
-  if (threadIdx.x == 0) fetch_raw(0);
+  if (threadIdx.x == 0)
+    for (int i = 0; i < NRAW; ++i) fetch_raw(i);
   if (lane == 0) {
     p_load_unit();
     for (int st = 0; st < DV_STAGES; ++st) issue_next();
@@ -347,7 +368,8 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
 
     // this unit's scales: wait for the raw bytes, decode this warp's part into
     // pairs; the last warp to finish issues the next unit's copy
-    ok = __all_sync(0xffffffffu, tc::mbar_wait(&sbar, (uint32_t)(i & 1), abort));
+    ok = __all_sync(0xffffffffu,
+                    tc::mbar_wait(&sbar[i % NRAW], (uint32_t)((i / NRAW) & 1), abort));
     // the warps of a group leave together, so none waits on a barrier alone
     if (group_sync_or(grp, 32 * KS, !ok)) { ok = false; break; }
     {
@@ -358,7 +380,8 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       const bool even = (KB & 1) == 0;
 #pragma unroll
       for (int m = 0; m < NMAT; ++m) {
-        const uint8_t *src = raw + m * sc_pitch + (grp * 16 + gg) * KB + b_beg;
+        const uint8_t *src = smem + plan.raw_off + (size_t)((i % NRAW) * NMAT + m) * sc_pitch +
+                             (grp * 16 + gg) * KB + b_beg;
         uint32_t *dst = pw + (m * 8 + gg) * PP;
         for (int b = 2 * q; b < nbl; b += 8) {
           const bool two = b + 1 < nbl;
@@ -384,7 +407,7 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       if (atomicAdd(&s_raw_done, 1u) == (unsigned)((i + 1) * DV_WARPS - 1)) {
         __threadfence_block();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        fetch_raw(i + 1);
+        fetch_raw(i + NRAW);
       }
     }
     const uint32_t *pr1 = pw + g * PP;
@@ -394,8 +417,8 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       // token g of this pass, or the pass's last token where g is past it (its
       // results are not stored)
       const int tok = tg + min(g, cnt - tg - 1);
-      const uint16_t *xrow = a.act16 + (size_t)(beg + tok) * K + (size_t)b_beg * 32 + 8 * t;
-      const uint16_t *xpf = a.act16 + (size_t)(beg + tg + min(lane >> 2, cnt - tg - 1)) * K +
+      const uint16_t *xrow = a.act16 + (size_t)s_row[beg + tok] * K + (size_t)b_beg * 32 + 8 * t;
+      const uint16_t *xpf = a.act16 + (size_t)s_row[beg + tg + min(lane >> 2, cnt - tg - 1)] * K +
                             (size_t)b_beg * 32 + (lane & 3) * 64;
       float acc1[4] = {0.f, 0.f, 0.f, 0.f}, acc3[4] = {0.f, 0.f, 0.f, 0.f};
       uint4 bx[8];
@@ -555,8 +578,10 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       for (int j = consumed; j < issued; ++j)
         tc::mbar_wait_drain(&full[warp][j % DV_STAGES], (uint32_t)(j / DV_STAGES) & 1u,
                             100000000ull);
-      if (raw_mine >= 0)
-        tc::mbar_wait_drain(&sbar, (uint32_t)(raw_mine & 1), 100000000ull);
+      if (raw_mine0 >= 0)
+        tc::mbar_wait_drain(&sbar[0], (uint32_t)((raw_mine0 / NRAW) & 1), 100000000ull);
+      if (raw_mine1 >= 0)
+        tc::mbar_wait_drain(&sbar[1], (uint32_t)((raw_mine1 / NRAW) & 1), 100000000ull);
       set_status(a.status, MOE_ERR_TIMEOUT, blockIdx.x);
     }
   }
@@ -604,11 +629,18 @@ cudaError_t launch_one(DecodeArgs a, const uint8_t *W, const uint8_t *W3, int nu
   return cudaGetLastError();
 }
 
+// Rows per work unit: 64 (four 16-row groups, two reduction splits each)
+// where that still gives every resident CTA a unit, else 32, else 16.  Longer
+// units spread the per-unit costs (scale decoding, the partial-sum exchange,
+// the epilogue) over more weight bytes.
 template <int EPI>
-cudaError_t launch_rg(DecodeArgs a, int row_groups, const uint8_t *W, const uint8_t *W3,
-                      int num_experts, int slots, cudaStream_t s) {
-  return row_groups == 1 ? launch_one<EPI, 1>(a, W, W3, num_experts, slots, s)
-                         : launch_one<EPI, 4>(a, W, W3, num_experts, slots, s);
+cudaError_t launch_rg(DecodeArgs a, const uint8_t *W, const uint8_t *W3, int num_experts,
+                      int slots, cudaStream_t s) {
+  const long ctas = 2L * num_sms();
+  auto units = [&](int rg) { return (long)slots * ((a.R + 16 * rg - 1) / (16 * rg)); };
+  if (units(4) >= ctas) return launch_one<EPI, 4>(a, W, W3, num_experts, slots, s);
+  if (units(2) >= ctas) return launch_one<EPI, 2>(a, W, W3, num_experts, slots, s);
+  return launch_one<EPI, 1>(a, W, W3, num_experts, slots, s);
 }
 
 }  // namespace
@@ -647,12 +679,14 @@ cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
   a.num_experts = c.n_experts;
   a.P = P;
   a.status = status;
-  // few tokens per expert: eight reduction splits per 16 rows for parallelism;
-  // more tokens: 64 rows per CTA, each staged B fragment serving more weights
-  const int row_groups = c.n <= 2 ? 1 : 4;
+  a.top_k = c.top_k;
   if (part == 0) {
-    cudaError_t e = launch_rows_to_f16(act, perm, c.top_k, P, c.d, x16, status, s);
-    if (e != cudaSuccess) return e;
+    if (act != nullptr) {
+      cudaError_t e = launch_rows_to_f16(act, perm, c.top_k, P, c.d, x16, status, s);
+      if (e != cudaSuccess) return e;
+    } else {
+      a.perm = perm;   // x16 holds the x rows in token order
+    }
     a.act16 = x16;
     a.S = w.S1;
     a.S3 = w.S3;
@@ -661,8 +695,8 @@ cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
     a.out = static_cast<__nv_bfloat16 *>(h);
     a.out16 = h16;
     const uint8_t *W1 = static_cast<const uint8_t *>(w.W1), *W3 = static_cast<const uint8_t *>(w.W3);
-    return c.act == MOE_ACT_SWIGLU ? launch_rg<2>(a, row_groups, W1, W3, c.n_experts, slots, s)
-                                   : launch_rg<1>(a, row_groups, W1, nullptr, c.n_experts, slots, s);
+    return c.act == MOE_ACT_SWIGLU ? launch_rg<2>(a, W1, W3, c.n_experts, slots, s)
+                                   : launch_rg<1>(a, W1, nullptr, c.n_experts, slots, s);
   }
   a.act16 = h16;
   a.S = w.S2;
@@ -671,8 +705,7 @@ cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
   a.K = c.d_ff;
   a.out = static_cast<__nv_bfloat16 *>(y_perm);
   a.out16 = nullptr;
-  return launch_rg<0>(a, row_groups, static_cast<const uint8_t *>(w.W2), nullptr, c.n_experts,
-                      slots, s);
+  return launch_rg<0>(a, static_cast<const uint8_t *>(w.W2), nullptr, c.n_experts, slots, s);
 }
 
 }  // namespace moe

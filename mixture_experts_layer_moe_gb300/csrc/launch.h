@@ -21,6 +21,9 @@ int num_sms();
 cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, const float *bias,
                          float *logits, int32_t *topk_idx, float *topk_gate, float *probs,
                          int *status, cudaStream_t s);
+// The router's linear layer alone: logits [n][E] fp32.
+cudaError_t launch_route_logits(const moe_config &c, const void *x, const void *Wg,
+                                const float *bias, float *logits, int *status, cudaStream_t s);
 
 // Routing statistics: P [E], f [E] and aux (one float) from probs [n][E] and
 // the top-1 column of topk_idx.
@@ -95,8 +98,19 @@ size_t mx_act16_bytes(const moe_config &c);
 // dst[q] = f16(src[perm[q] / top_k]) (perm given) or f16(src[q]); rows of K.
 cudaError_t launch_rows_to_f16(const void *src, const int32_t *perm, int top_k, int P, int K,
                                void *dst, int *status, cudaStream_t s);
+// part 0 with act == nullptr: act16 already holds the f16 x rows in token order
+// (as launch_decode_route writes them), read through perm.
 cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
                               const int32_t *perm, const int32_t *offsets, const moe_weights &w,
                               void *h, void *y_perm, void *act16, int *status, cudaStream_t s);
+// Small-batch routing in one launch (decode_supported configurations with a
+// bf16 x): selection and gates from the logits, counts / offsets / perm /
+// inv_perm of the stable dispatch, and the f16 x rows in token order (act16,
+// as launch_decode_ffn part 0 reads them with act == nullptr).
+bool decode_route_supported(const moe_config &c);
+cudaError_t launch_decode_route(const moe_config &c, const float *logits, const void *x,
+                                int32_t *topk_idx, float *topk_gate, int32_t *counts,
+                                int32_t *offsets, int32_t *perm, int32_t *inv_perm, void *act16,
+                                int *status, cudaStream_t s);
 
 }  // namespace moe

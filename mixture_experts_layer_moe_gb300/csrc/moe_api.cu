@@ -410,11 +410,35 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
   int32_t *offsets = at<int32_t>(ws, L.offsets);
   int32_t *perm = at<int32_t>(ws, L.perm);
   int32_t *inv_perm = at<int32_t>(ws, L.inv_perm);
+  const bool decode = decode_supported(c);
+  const bool mx_tc = mx_tc_path(c);
+  if (decode && decode_route_supported(c)) {
+    // small batch: the router's linear layer, then selection, dispatch and the
+    // f16 activation rows in one launch; the FFN streams the chosen experts
+    stage(MOE_STAGE_ROUTE, 1);
+    MOE_TRY(cuda_status(launch_route_logits(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits),
+                                            status, s)));
+    stage(MOE_STAGE_DISPATCH, 1);
+    MOE_TRY(cuda_status(launch_decode_route(c, at<float>(ws, L.logits), x, topk_idx, gates,
+                                            at<int32_t>(ws, L.counts), offsets, perm, inv_perm,
+                                            at<void>(ws, L.act16), status, s)));
+    stage(MOE_STAGE_FFN_UP, 1);
+    MOE_TRY(cuda_status(launch_decode_ffn(c, 0, nullptr, perm, offsets, *w, at<void>(ws, L.h),
+                                          at<void>(ws, L.y_perm), at<void>(ws, L.act16), status,
+                                          s)));
+    stage(MOE_STAGE_FFN_DOWN, 1);
+    MOE_TRY(cuda_status(launch_decode_ffn(c, 1, nullptr, perm, offsets, *w, at<void>(ws, L.h),
+                                          at<void>(ws, L.y_perm), at<void>(ws, L.act16), status,
+                                          s)));
+    stage(MOE_STAGE_COMBINE, 1);
+    MOE_TRY(cuda_status(launch_combine(c.act_dtype, at<void>(ws, L.y_perm), inv_perm, gates,
+                                       nullptr, y, c.n, c.top_k, c.d, status, s)));
+    stage(MOE_STAGE_END, 0);
+    return MOE_OK;
+  }
   stage(MOE_STAGE_ROUTE, 2);
   MOE_TRY(cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits), topk_idx,
                                    gates, nullptr, status, s)));
-  const bool decode = decode_supported(c);
-  const bool mx_tc = mx_tc_path(c);
   stage(MOE_STAGE_DISPATCH, (decode || mx_tc) ? 1 : 2);
   MOE_TRY(cuda_status(launch_dispatch(P, c.n_experts, topk_idx, at<int32_t>(ws, L.counts), offsets,
                                       perm, inv_perm, status, s)));

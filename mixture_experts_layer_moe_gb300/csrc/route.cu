@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "select.cuh"
 
 namespace moe {
 namespace {
@@ -78,62 +79,83 @@ route_logits_kernel(const T *__restrict__ x, const T *__restrict__ Wg,
 // Small batches (decode): one warp per expert, RS_TOK tokens per CTA row.
 // Lane l walks the row in 8-element pieces (l*8, l*8 + 256, ...); each piece
 // is a fresh fp32 partial added to the token's sum, and the 32 lane sums are
-// combined by a shuffle tree.  Wg is read once per token group.
-constexpr int RS_WARPS = 8, RS_TOK = 16, RS_MAXV = 12;   // d <= 32 * 8 * RS_MAXV = 3072
+// combined by a shuffle tree.  A lane's Wg pieces are loaded into registers
+// while the CTA copies its tokens' x rows into shared memory, so the whole
+// CTA waits on one round of memory latency; the dot products then read x
+// from shared memory.
+constexpr int RS_WARPS = 8, RS_TOK = 4, RS_MAXV = 12;    // d <= 32 * 8 * RS_MAXV = 3072
 
-// All of a lane's Wg pieces are loaded before any arithmetic, and a token's
-// pieces before its dot product, so a warp waits on about two memory
-// latencies instead of one per piece.
 __global__ void __launch_bounds__(32 * RS_WARPS)
 route_logits_small_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat16 *__restrict__ Wg,
                           const float *__restrict__ bias, float *__restrict__ logits, int n, int d,
                           int E) {
+  extern __shared__ __align__(16) uint4 xs[];             // [RS_TOK][d / 8]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * RS_WARPS + warp;
   const int t0 = blockIdx.y * RS_TOK;
-  if (e >= E) return;
   const int nt = min(RS_TOK, n - t0);
-  const int nv = (d / 8 - lane + 31) / 32;          // pieces of this lane: k0 = (lane + 32 v) * 8
-  const __nv_bfloat16 *wrow = Wg + (size_t)e * d;
+  const int vpr = d / 8;
+  const int nv = (vpr - lane + 31) / 32;                  // pieces of this lane: k0 = (lane + 32 v) * 8
   uint4 wv[RS_MAXV];
-#pragma unroll
-  for (int v = 0; v < RS_MAXV; ++v)
-    if (v < nv) wv[v] = *reinterpret_cast<const uint4 *>(wrow + (size_t)(lane + 32 * v) * 8);
-  float mine = 0.f;
-  for (int j = 0; j < nt; ++j) {
-    const __nv_bfloat16 *xrow = x + (size_t)(t0 + j) * d;
-    uint4 xv[RS_MAXV];
+  if (e < E) {
+    const __nv_bfloat16 *wrow = Wg + (size_t)e * d;
 #pragma unroll
     for (int v = 0; v < RS_MAXV; ++v)
-      if (v < nv) xv[v] = *reinterpret_cast<const uint4 *>(xrow + (size_t)(lane + 32 * v) * 8);
-    float acc = 0.f;
+      if (v < nv) wv[v] = *reinterpret_cast<const uint4 *>(wrow + (size_t)(lane + 32 * v) * 8);
+  }
+  // all of a thread's x pieces in flight at once (at most RS_TOK * d / 8 /
+  // threads = 12), then stored
+  const uint4 *xsrc = reinterpret_cast<const uint4 *>(x + (size_t)t0 * d);
+  constexpr int RS_STAGE = RS_TOK * 32 * 8 * RS_MAXV / 8 / (32 * RS_WARPS);
+  uint4 xv_st[RS_STAGE];
 #pragma unroll
-    for (int v = 0; v < RS_MAXV; ++v) {
-      if (v < nv) {
-        const uint32_t ww[4] = {wv[v].x, wv[v].y, wv[v].z, wv[v].w};
-        const uint32_t xx[4] = {xv[v].x, xv[v].y, xv[v].z, xv[v].w};
-        float part = 0.f;
+  for (int j = 0; j < RS_STAGE; ++j) {
+    const int i = threadIdx.x + j * 32 * RS_WARPS;
+    if (i < nt * vpr) xv_st[j] = xsrc[i];
+  }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          part = fmaf(__uint_as_float(ww[i] << 16), __uint_as_float(xx[i] << 16), part);
-          part = fmaf(__uint_as_float(ww[i] & 0xffff0000u), __uint_as_float(xx[i] & 0xffff0000u),
-                      part);
+  for (int j = 0; j < RS_STAGE; ++j) {
+    const int i = threadIdx.x + j * 32 * RS_WARPS;
+    if (i < nt * vpr) xs[i] = xv_st[j];
+  }
+  __syncthreads();
+  if (e >= E) return;
+  // the RS_TOK tokens' sums side by side, so their shuffle trees interleave
+  float acc[RS_TOK];
+#pragma unroll
+  for (int j = 0; j < RS_TOK; ++j) acc[j] = 0.f;
+#pragma unroll
+  for (int v = 0; v < RS_MAXV; ++v) {
+    if (v < nv) {
+      const uint32_t ww[4] = {wv[v].x, wv[v].y, wv[v].z, wv[v].w};
+#pragma unroll
+      for (int j = 0; j < RS_TOK; ++j) {
+        if (j < nt) {
+          const uint4 xv = xs[j * vpr + lane + 32 * v];
+          const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+          float part = 0.f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            part = fmaf(__uint_as_float(ww[i] << 16), __uint_as_float(xx[i] << 16), part);
+            part = fmaf(__uint_as_float(ww[i] & 0xffff0000u), __uint_as_float(xx[i] & 0xffff0000u),
+                        part);
+          }
+          acc[j] += part;
         }
-        acc += part;
       }
     }
+  }
+  float mine = 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == j) mine = acc;
+  for (int j = 0; j < RS_TOK; ++j) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
+    if (lane == j) mine = acc[j];
   }
   if (lane < nt) logits[(size_t)(t0 + lane) * E + e] = mine + (bias ? bias[e] : 0.f);
 }
 
-// One warp per token.  Lane l holds experts l, l+32, ... (E <= 256).
-// Selection works on the fp32 logits: larger first, lower index on equal
-// values; NaN scores rank below everything.  Gates:
-//   top_prob: g_j = exp(l_j - m) / sum_e exp(l_e - m)
-//   renorm:   g_j = exp(l_j - m) / sum_{chosen} exp(l_c - m)
+// One warp per token (selection and gates as in select_topk_warp).
 __global__ void __launch_bounds__(256)
 route_select_kernel(const float *__restrict__ logits, int n, int E, int k, int gate_mode,
                     int32_t *__restrict__ topk_idx, float *__restrict__ topk_gate,
@@ -141,73 +163,14 @@ route_select_kernel(const float *__restrict__ logits, int n, int E, int k, int g
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= n) return;
-  const float *l = logits + (size_t)warp * E;
-  float v[8];
-  float mx = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = lane + 32 * i;
-    float t = (e < E) ? l[e] : -INFINITY;
-    if (isnan(t)) t = -INFINITY;
-    v[i] = t;
-    mx = fmaxf(mx, t);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float sum = 0.f;
-  float ex[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    ex[i] = (lane + 32 * i < E) ? expf(v[i] - mx) : 0.f;
-    sum += ex[i];
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (probs) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) probs[(size_t)warp * E + e] = ex[i] / sum;
-    }
-  }
-  unsigned taken = 0;
-  float sel_ex[8];   // slot j kept by lane j % 32 at [j / 32]
-  float sel_sum = 0.f;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u)) {
-        if (v[i] > bv || (v[i] == bv && e < bi)) { bv = v[i]; bi = e; }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    const float exj = expf(bv - mx);
-    sel_sum += exj;
-    if ((j & 31) == lane) sel_ex[j >> 5] = exj;
-    if (lane == 0) topk_idx[(size_t)warp * k + j] = bi;
-  }
-  const float denom = (gate_mode == MOE_GATE_RENORM) ? sel_sum : sum;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int j = lane + 32 * i;
-    if (j < k) topk_gate[(size_t)warp * k + j] = sel_ex[i] / denom;
-  }
+  select_topk_warp(logits + (size_t)warp * E, E, k, gate_mode, lane, topk_idx + (size_t)warp * k,
+                   topk_gate + (size_t)warp * k, probs ? probs + (size_t)warp * E : nullptr);
 }
 
 }  // namespace
 
-cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, const float *bias,
-                         float *logits, int32_t *topk_idx, float *topk_gate, float *probs,
-                         int *status, cudaStream_t s) {
+cudaError_t launch_route_logits(const moe_config &c, const void *x, const void *Wg,
+                                const float *bias, float *logits, int *status, cudaStream_t s) {
   cudaError_t err = cudaSuccess;
   GemmStage g{};
   g.a_dtype = c.act_dtype;
@@ -229,7 +192,7 @@ cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, con
   else if (c.act_dtype == MOE_BF16 && c.n <= kSmallRouterMaxTokens && c.d <= 32 * 8 * RS_MAXV)
     route_logits_small_kernel<<<dim3((c.n_experts + RS_WARPS - 1) / RS_WARPS,
                                      (c.n + RS_TOK - 1) / RS_TOK),
-                                32 * RS_WARPS, 0, s>>>((const __nv_bfloat16 *)x,
+                                32 * RS_WARPS, (size_t)RS_TOK * c.d * 2, s>>>((const __nv_bfloat16 *)x,
                                                        (const __nv_bfloat16 *)Wg, bias, logits,
                                                        c.n, c.d, c.n_experts);
   else if (c.act_dtype == MOE_F32)
@@ -240,6 +203,13 @@ cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, con
         (const __nv_bfloat16 *)x, (const __nv_bfloat16 *)Wg, bias, logits, c.n, c.d,
         c.n_experts);
   if (err == cudaSuccess) err = cudaGetLastError();
+  return err;
+}
+
+cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, const float *bias,
+                         float *logits, int32_t *topk_idx, float *topk_gate, float *probs,
+                         int *status, cudaStream_t s) {
+  cudaError_t err = launch_route_logits(c, x, Wg, bias, logits, status, s);
   if (err != cudaSuccess) return err;
   const int warps_per_block = 8;
   route_select_kernel<<<(c.n + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0,
