@@ -53,13 +53,19 @@ __device__ __forceinline__ uint4 pack16<__nv_bfloat16>(const float *f) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// One CTA per token row block; thread handles 16-byte vectors of the row.
+// Thread = one 16-byte vector of an output row.  The slots are taken eight at
+// a time: their indices and gates, then their rows, are all loaded before the
+// sum, which runs in slot order.
+constexpr int CB_SLOTS = 8;
+
 template <typename T>
 __global__ void __launch_bounds__(256)
 combine_kernel(const uint4 *__restrict__ y_perm, const int32_t *__restrict__ inv_perm,
                const float *__restrict__ gates, const uint4 *__restrict__ y_shared,
                uint4 *__restrict__ y, int n, int k, int vec_per_row, int *status) {
   constexpr int V = Vec16<T>::N;
+  pdl_launch_dependents();
+  pdl_wait();
   const int P = n * k;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)n * vec_per_row;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -68,17 +74,33 @@ combine_kernel(const uint4 *__restrict__ y_perm, const int32_t *__restrict__ inv
     float acc[V];
 #pragma unroll
     for (int c = 0; c < V; ++c) acc[c] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int q = inv_perm[(int64_t)t * k + j];
-      if (q < 0 || q >= P) {
-        if (v == 0) set_status(status, MOE_ERR_BAD_INDEX, t * k + j);
-        continue;
-      }
-      const float g = gates[(int64_t)t * k + j];
-      float f[V];
-      unpack16<T>(y_perm[(int64_t)q * vec_per_row + v], f);
+    for (int j0 = 0; j0 < k; j0 += CB_SLOTS) {
+      int q[CB_SLOTS];
+      float g[CB_SLOTS];
+      uint4 r[CB_SLOTS];
 #pragma unroll
-      for (int c = 0; c < V; ++c) acc[c] = fmaf(g, f[c], acc[c]);
+      for (int u = 0; u < CB_SLOTS; ++u) {
+        q[u] = -1;
+        if (j0 + u < k) {
+          q[u] = inv_perm[(int64_t)t * k + j0 + u];
+          g[u] = gates[(int64_t)t * k + j0 + u];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < CB_SLOTS; ++u)
+        if (q[u] >= 0 && q[u] < P) r[u] = y_perm[(int64_t)q[u] * vec_per_row + v];
+#pragma unroll
+      for (int u = 0; u < CB_SLOTS; ++u) {
+        if (j0 + u >= k) continue;
+        if (q[u] < 0 || q[u] >= P) {
+          if (v == 0) set_status(status, MOE_ERR_BAD_INDEX, t * k + j0 + u);
+          continue;
+        }
+        float f[V];
+        unpack16<T>(r[u], f);
+#pragma unroll
+        for (int c = 0; c < V; ++c) acc[c] = fmaf(g[u], f[c], acc[c]);
+      }
     }
     if (y_shared) {
       float f[V];
@@ -102,14 +124,12 @@ cudaError_t launch_combine(int act_dtype, const void *y_perm, const int32_t *inv
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
   if (act_dtype == MOE_F32)
-    combine_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
-        (const uint4 *)y_perm, inv_perm, gates, (const uint4 *)y_shared, (uint4 *)y, n, k, vpr,
-        status);
-  else
-    combine_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
-        (const uint4 *)y_perm, inv_perm, gates, (const uint4 *)y_shared, (uint4 *)y, n, k, vpr,
-        status);
-  return cudaGetLastError();
+    return launch_pdl(combine_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, s,
+                      (const uint4 *)y_perm, inv_perm, gates, (const uint4 *)y_shared, (uint4 *)y,
+                      n, k, vpr, status);
+  return launch_pdl(combine_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0, s,
+                    (const uint4 *)y_perm, inv_perm, gates, (const uint4 *)y_shared, (uint4 *)y, n,
+                    k, vpr, status);
 }
 
 }  // namespace moe

@@ -27,6 +27,18 @@ __device__ __forceinline__ bool status_failed(const int *st) {
   return st != nullptr && *reinterpret_cast<const volatile int *>(st) != 0;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// A kernel launched with launch_pdl may start while the previous kernel in the
+// stream is still running: it calls pdl_launch_dependents() to let the next
+// kernel start in turn, and pdl_wait() before touching any global memory that
+// an earlier kernel writes or reads (the wait returns once the previous grid
+// has completed and its writes are visible).  Both are no-ops in a kernel
+// launched without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------- element types
 template <typename T> struct Elem;
 template <> struct Elem<float> {

@@ -217,6 +217,12 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   __shared__ int s_active[256], s_beg[256], s_cnt[256];
   __shared__ int s_row[kDecodeMaxPairs];          // activation row of each segment position
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    tc::prefetch_tmap(&tm1);
+    if (NMAT == 2) tc::prefetch_tmap(&tm3);
+  }
+  pdl_wait();
   if (status_failed(a.status)) return;
 
   // the experts with a non-empty segment, in order (E <= 256, one round of loads)
@@ -625,8 +631,8 @@ cudaError_t launch_one(DecodeArgs a, const uint8_t *W, const uint8_t *W3, int nu
   long grid = (long)per_sm * num_sms();
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
-  decode_mxfp4_kernel<EPI, RG><<<(unsigned)grid, 32 * DV_WARPS, smem, s>>>(m1, m3, a);
-  return cudaGetLastError();
+  return launch_pdl(decode_mxfp4_kernel<EPI, RG>, dim3((unsigned)grid), dim3(32 * DV_WARPS), smem,
+                    s, m1, m3, a);
 }
 
 // Rows per work unit: 64 (four 16-row groups, two reduction splits each)

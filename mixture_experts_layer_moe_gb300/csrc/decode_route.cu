@@ -54,6 +54,8 @@ decode_route_kernel(const float *__restrict__ logits, int n, int E, int k, int g
   __shared__ int s_off[256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int P = n * k;
+  pdl_launch_dependents();
+  pdl_wait();
   // the same answer in every CTA: nothing writes the status word meanwhile
   const bool failed = status_failed(status);
   const bool router = blockIdx.x < DR_CLUSTER;
@@ -153,11 +155,10 @@ cudaError_t launch_decode_route(const moe_config &c, const float *logits, const 
   const long max_clusters = num_sms() / DR_CLUSTER;
   if (clusters > max_clusters) clusters = max_clusters;
   if (clusters < 1) clusters = 1;
-  decode_route_kernel<<<(unsigned)(clusters * DR_CLUSTER), DR_THREADS, 0, s>>>(
-      logits, c.n, c.n_experts, c.top_k, c.gate, static_cast<const __nv_bfloat16 *>(x), c.d,
-      topk_idx, topk_gate, counts, offsets, perm, inv_perm, static_cast<uint16_t *>(act16),
-      status);
-  return cudaGetLastError();
+  return launch_pdl(decode_route_kernel, dim3((unsigned)(clusters * DR_CLUSTER)), dim3(DR_THREADS),
+                    0, s, logits, c.n, c.n_experts, c.top_k, (int)c.gate,
+                    static_cast<const __nv_bfloat16 *>(x), c.d, topk_idx, topk_gate, counts,
+                    offsets, perm, inv_perm, static_cast<uint16_t *>(act16), status);
 }
 
 }  // namespace moe

@@ -1,6 +1,8 @@
 // Host-side launchers of the MoE kernels (internal; the public ABI is moe.h).
 #pragma once
 
+#include <utility>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -8,6 +10,25 @@
 #include "moe.h"
 
 namespace moe {
+
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// before the previous kernel in the stream completes (it must call pdl_wait()
+// before touching memory that earlier kernels use).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Tensor-map encoding (cuTensorMapEncodeTiled through the runtime's driver
 // entry point), innermost dimension first, dense strides; and the SM count.

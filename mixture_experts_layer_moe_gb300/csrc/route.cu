@@ -90,6 +90,8 @@ route_logits_small_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat
                           const float *__restrict__ bias, float *__restrict__ logits, int n, int d,
                           int E) {
   extern __shared__ __align__(16) uint4 xs[];             // [RS_TOK][d / 8]
+  pdl_launch_dependents();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * RS_WARPS + warp;
   const int t0 = blockIdx.y * RS_TOK;
@@ -190,11 +192,10 @@ cudaError_t launch_route_logits(const moe_config &c, const void *x, const void *
   if (c.n >= kTensorCoreRouterMinTokens && gemm_tc_supported(g))
     err = launch_gemm_tc(g, status, s);
   else if (c.act_dtype == MOE_BF16 && c.n <= kSmallRouterMaxTokens && c.d <= 32 * 8 * RS_MAXV)
-    route_logits_small_kernel<<<dim3((c.n_experts + RS_WARPS - 1) / RS_WARPS,
-                                     (c.n + RS_TOK - 1) / RS_TOK),
-                                32 * RS_WARPS, (size_t)RS_TOK * c.d * 2, s>>>((const __nv_bfloat16 *)x,
-                                                       (const __nv_bfloat16 *)Wg, bias, logits,
-                                                       c.n, c.d, c.n_experts);
+    err = launch_pdl(route_logits_small_kernel,
+                     dim3((c.n_experts + RS_WARPS - 1) / RS_WARPS, (c.n + RS_TOK - 1) / RS_TOK),
+                     dim3(32 * RS_WARPS), (size_t)RS_TOK * c.d * 2, s, (const __nv_bfloat16 *)x,
+                     (const __nv_bfloat16 *)Wg, bias, logits, c.n, c.d, c.n_experts);
   else if (c.act_dtype == MOE_F32)
     route_logits_kernel<float><<<grid, RT_THREADS, 0, s>>>(
         (const float *)x, (const float *)Wg, bias, logits, c.n, c.d, c.n_experts);
