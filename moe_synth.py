@@ -211,3 +211,36 @@ def describe(cfg: MoEConfig) -> str:
             + (f" shared d_ff={cfg.d_ff_shared}" if cfg.d_ff_shared else "")
             + (f" bias={cfg.router_bias}" if cfg.router_bias != "none" else ""))
 
+
+
+# ---------------------------------------------------------------------------
+# Resident expert pool (expert-slot indirection inputs)
+# ---------------------------------------------------------------------------
+
+def make_slot_table(E: int, n_slots: int, resident: int, seed: int = 0) -> torch.Tensor:
+    """A seeded resident set: ``resident`` distinct experts, each mapped to a
+    distinct slot in [0, n_slots) (both drawn at random); -1 elsewhere."""
+    assert 0 <= resident <= min(E, n_slots)
+    g = torch.Generator().manual_seed(seed)
+    experts = torch.randperm(E, generator=g)[:resident]
+    slots = torch.randperm(n_slots, generator=g)[:resident]
+    table = torch.full((E,), -1, dtype=torch.int32)
+    table[experts] = slots.to(torch.int32)
+    return table
+
+
+def make_pool(inputs: dict, slot_of: torch.Tensor, n_slots: int, device="cpu") -> dict:
+    """The resident pool for ``slot_of``: slot s holds a byte-for-byte copy of
+    the weights (MXFP4 codes and scales) of the expert mapped to it; unused
+    slots are zero.  Keys as in ``make_inputs``."""
+    out = {}
+    for key in ("W1q", "W3q", "W2q", "S1", "S3", "S2"):
+        src = inputs.get(key)
+        if src is None:
+            continue
+        pool = torch.zeros((n_slots,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+        for e, s in enumerate(slot_of.tolist()):
+            if s >= 0:
+                pool[s].copy_(src[e])
+        out[key] = pool.to(device)
+    return out

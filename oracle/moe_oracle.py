@@ -323,3 +323,41 @@ def routing_statistics(probs: torch.Tensor, top1: torch.Tensor, alpha: float) ->
 def near_ties(routing: dict, threshold: float = 1e-5) -> torch.Tensor:
     """Tokens whose top-k margin is below ``threshold`` (listed, not excused)."""
     return torch.nonzero(routing["margin"] < threshold, as_tuple=True)[0]
+
+
+# ---------------------------------------------------------------------------
+# Expert-slot indirection   [Feed] FreeToken paper summary post, section
+# "3. Decode: Exploit Expert Locality" (a selected expert that is resident in
+# GPU memory is a hit and runs from there; one that is not is a miss) and
+# section "10. Dynamic Scheduling Without Giving Up CUDA Graphs" (hit/miss
+# classification and the rewrite of logical expert ids to physical cache
+# slots happen on the GPU).  The benchmark post's section "5. Why llama.cpp
+# Still Hits a Ceiling" counts lookups served by the resident experts.
+# ---------------------------------------------------------------------------
+
+def classify_experts(idx: torch.Tensor, E: int, slot_of: torch.Tensor) -> dict:
+    """Hit/miss classification of one batch's expert lookups.
+
+    ``idx`` [n, k] holds the selected experts, ``slot_of`` [E] the physical
+    slot of each resident expert and -1 for the others.
+
+    * ``state[e]``: -1 if no token selected expert e, 1 if it was selected and
+      is resident (hit), 0 if it was selected and is not (miss).
+    * ``miss_list``: the missed experts in ascending order.
+    * ``selected`` / ``resident``: distinct experts selected / of those, hits.
+    * ``lookups`` / ``served``: (token, slot) selections n*k / of those, the
+      ones whose expert is resident.
+    """
+    flat = idx.reshape(-1).to(torch.int64)
+    slot_of = slot_of.reshape(-1).to(torch.int64)
+    uses = torch.bincount(flat, minlength=E)
+    chosen = uses > 0
+    hit = slot_of >= 0
+    state = torch.full((E,), -1, dtype=torch.int64)
+    state[chosen & hit] = 1
+    state[chosen & ~hit] = 0
+    miss_list = torch.nonzero(chosen & ~hit, as_tuple=True)[0]
+    return dict(state=state, miss_list=miss_list,
+                selected=int(chosen.sum()), resident=int((chosen & hit).sum()),
+                lookups=int(flat.numel()), served=int(uses[hit].sum()))
+

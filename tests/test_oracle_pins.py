@@ -429,6 +429,88 @@ def test_mxfp4_expert_bruteforce():
         assert np.allclose(res["y"][t].numpy(), W2 @ h, rtol=1e-12, atol=1e-12)
 
 
+# ------------------------------------------------- expert-slot classification
+
+def check_expert_cache_example(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "expert_cache_example.json")))
+    E = g["n_experts"]
+    slot_of = torch.full((E,), -1, dtype=torch.int32)
+    for e, s in g["slot_of"].items():
+        slot_of[int(e)] = s
+    r = O.classify_experts(torch.tensor(g["selections"]), E, slot_of)
+    want = g["expected"]
+    assert r["miss_list"].tolist() == want["miss_list"]
+    assert torch.nonzero(r["state"] == 1, as_tuple=True)[0].tolist() == want["hits"]
+    assert (r["state"] == -1).sum().item() == E - want["selected"]
+    for key in ("selected", "resident", "lookups", "served"):
+        assert r[key] == want[key], key
+
+
+def test_expert_cache_example(golden_dir):
+    check_expert_cache_example(golden_dir)
+
+
+def _classify_bruteforce(idx, E, slot_of):
+    """Loop over the (token, slot) lookups with a set of seen experts."""
+    seen, served = set(), 0
+    for row in idx.tolist():
+        for e in row:
+            seen.add(e)
+            served += int(slot_of[e]) >= 0
+    misses = sorted(e for e in seen if int(slot_of[e]) < 0)
+    return seen, misses, served
+
+
+def check_classify_bruteforce():
+    g = torch.Generator().manual_seed(23)
+    for _ in range(40):
+        E = int(torch.randint(1, 40, (1,), generator=g))
+        k = int(torch.randint(1, E + 1, (1,), generator=g))
+        n = int(torch.randint(1, 12, (1,), generator=g))
+        idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(n)])
+        n_slots = int(torch.randint(1, E + 1, (1,), generator=g))
+        resident = int(torch.randint(0, n_slots + 1, (1,), generator=g))
+        slot_of = moe_synth.make_slot_table(E, n_slots, resident,
+                                            seed=int(torch.randint(0, 1 << 30, (1,), generator=g)))
+        r = O.classify_experts(idx, E, slot_of)
+        seen, misses, served = _classify_bruteforce(idx, E, slot_of)
+        assert r["miss_list"].tolist() == misses
+        assert r["selected"] == len(seen)
+        assert r["resident"] == len(seen) - len(misses)
+        assert r["lookups"] == n * k and r["served"] == served
+        for e in range(E):
+            want = -1 if e not in seen else (1 if int(slot_of[e]) >= 0 else 0)
+            assert int(r["state"][e]) == want
+
+
+def test_classify_bruteforce():
+    check_classify_bruteforce()
+
+
+def test_classify_all_or_none_resident():
+    idx = torch.tensor([[5, 1], [1, 2], [7, 5]])
+    everyone = torch.arange(8, dtype=torch.int32)
+    r = O.classify_experts(idx, 8, everyone)
+    assert r["miss_list"].numel() == 0 and r["served"] == r["lookups"] == 6
+    assert r["selected"] == r["resident"] == 4
+    nobody = torch.full((8,), -1, dtype=torch.int32)
+    r = O.classify_experts(idx, 8, nobody)
+    assert r["miss_list"].tolist() == [1, 2, 5, 7] and r["served"] == 0 and r["resident"] == 0
+
+
+def test_classify_random_router_serves_resident_fraction(golden_dir):
+    """Uniformly random selections: the served share of lookups approaches the
+    resident share of experts."""
+    g = json.load(open(os.path.join(golden_dir, "expert_cache_example.json")))["random_router"]
+    E, n, k = 4608, 4096, 4
+    gen = torch.Generator().manual_seed(5)
+    idx = torch.stack([torch.randperm(E, generator=gen)[:k] for _ in range(n)])
+    resident = round(g["resident_fraction"] * E)
+    slot_of = moe_synth.make_slot_table(E, resident, resident, seed=9)
+    r = O.classify_experts(idx, E, slot_of)
+    assert abs(r["served"] / r["lookups"] - g["resident_fraction"]) < 0.01
+
+
 # ------------------------------------------------------------ mutation tests
 
 def _bad_topk(logits, k):                        # ties go to the higher index
@@ -476,6 +558,19 @@ def _bad_stats(probs, top1, alpha):             # P_i averaged over experts, not
     return dict(P=P, f=f, aux=alpha * E * float((f * P).sum()))
 
 
+def _bad_classify(idx, E, slot_of):              # counts distinct experts as lookups served
+    r = _orig_classify(idx, E, slot_of)
+    return dict(r, served=r["resident"])
+
+
+_orig_classify = O.classify_experts
+
+
+def _bad_classify_slot0(idx, E, slot_of):        # slot 0 taken for "not resident"
+    return _orig_classify(idx, E, torch.where(slot_of.to(torch.int64) > 0, slot_of.to(torch.int64),
+                                              torch.full_like(slot_of.to(torch.int64), -1)))
+
+
 def _bad_softmax(logits):                        # no max subtraction and wrong axis
     ex = torch.exp(logits)
     return ex / ex.sum(dim=0, keepdim=True)
@@ -489,10 +584,12 @@ MUTANTS = [
     ("dispatch_arrays", _bad_dispatch, check_dispatch_example),
     ("softmax_rows", _bad_softmax, check_softmax_example),
     ("routing_statistics", _bad_stats, check_aux_loss_example),
+    ("classify_experts", _bad_classify, check_expert_cache_example),
+    ("classify_experts", _bad_classify_slot0, lambda gd: check_classify_bruteforce()),
 ]
 
 
-@pytest.mark.parametrize("name,mutant,pin", MUTANTS, ids=[m[0] for m in MUTANTS])
+@pytest.mark.parametrize("name,mutant,pin", MUTANTS, ids=[m[1].__name__ for m in MUTANTS])
 def test_planted_mistake_is_caught(monkeypatch, golden_dir, name, mutant, pin):
     pin(golden_dir)                               # passes on the real oracle
     monkeypatch.setattr(O, name, mutant)
