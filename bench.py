@@ -55,6 +55,10 @@ def parse_args(argv=None):
                    help="MoE layers per step (independently seeded weights, run in sequence)")
     p.add_argument("--cpu-sample", type=int, default=None,
                    help="tokens in the oracle's timed sample")
+    p.add_argument("--pool-fraction", type=float, default=None,
+                   help="small-batch MXFP4 workloads: run moe_forward_pooled with this share of "
+                        "each layer's experts resident in a slot pool (the rest read from the "
+                        "backing arrays)")
     return p.parse_args(argv)
 
 
@@ -262,12 +266,37 @@ def run_ours(args):
     y = torch.empty(cfg.n, cfg.d, dtype=inputs["x"].dtype, device=device)
     mid = [torch.empty_like(y) for _ in range(2)]
 
+    # expert-slot indirection: a seeded resident set per layer, copied into a
+    # slot pool; the classification of every layer lands in its own counts
+    pools, pool_keep, pool_counts = [], [], []
+    if args.pool_fraction is not None:
+        if not is_decode(cfg):
+            raise SystemExit("--pool-fraction applies to small-batch MXFP4 workloads")
+        resident = round(args.pool_fraction * cfg.E)
+        n_slots = max(1, resident)
+        for l, li in enumerate(layer_inputs):
+            table = moe_synth.make_slot_table(cfg.E, n_slots, resident, seed=args.seed + 31 * l)
+            tensors = moe_synth.make_pool(li, table, n_slots, device=device)
+            table_dev = table.to(device)
+            pool_keep.append((tensors, table_dev))
+            pools.append(moe.make_pool(table_dev, tensors))
+            pool_counts.append(torch.zeros(4, dtype=torch.int32, device=device))
+        pool_state = torch.empty(cfg.E, dtype=torch.int32, device=device)
+        pool_miss = torch.empty(cfg.E, dtype=torch.int32, device=device)
+
     def run_layers(x_in, y_out, hook=None):
         """Layer 0 .. L-1 in sequence; the stage hook instruments layer 0."""
         cur = x_in
         for l in range(args.layers):
             out = y_out if l == args.layers - 1 else mid[l % 2]
-            if l == 0 and hook is not None:
+            if pools:
+                if l == 0 and hook is not None:
+                    moe.moe_forward_pooled_staged(cfg, cur, layer_w[l], pools[l], out, pool_state,
+                                                  pool_miss, pool_counts[l], ws, hook, stream)
+                else:
+                    moe.moe_forward_pooled(cfg, cur, layer_w[l], pools[l], out, pool_state,
+                                           pool_miss, pool_counts[l], ws, stream)
+            elif l == 0 and hook is not None:
                 moe.moe_forward_staged(cfg, cur, layer_w[l], out, ws, hook, stream)
             else:
                 moe.moe_forward(cfg, cur, layer_w[l], out, ws, stream)
@@ -298,12 +327,15 @@ def run_ours(args):
 
     L = moe.moe_workspace_layout_of(cfg)
     counts = ws[L["counts"]:L["counts"] + 4 * cfg.E].view(torch.int32)
-    active_per_batch = []
+    active_per_batch, served = [], []
     for i in range(max(args.warmup, n_batches)):
         step(i)
         if i < n_batches:
             torch.cuda.synchronize(device)
             active_per_batch.append(int((counts > 0).sum().item()))
+            for pc in pool_counts:
+                c4 = pc.tolist()
+                served.append(c4[moe.POOL_SERVED] / c4[moe.POOL_LOOKUPS])
     torch.cuda.synchronize(device)
     st, detail = moe.moe_status_check(ws)
     if st != 0:
@@ -443,6 +475,12 @@ def run_ours(args):
             "parallelism": f"dp{world} (independent token batches, replicated weights)",
             "l2": l2_note,
             "timing": timing,
+            **({"expert_pool": {
+                "resident_fraction": args.pool_fraction,
+                "resident_experts_per_layer": round(args.pool_fraction * cfg.E),
+                "lookups_served_fraction": statistics.mean(served),
+                "path": "moe_forward_pooled (resident experts read from their pool slots, the "
+                        "others from the backing arrays)"}} if pools else {}),
         },
         "e2e": {"value": job_throughput(cfg.n * args.steps, world, t_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),

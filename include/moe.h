@@ -237,6 +237,68 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
                               void *ws, size_t ws_bytes, void *stream, moe_stage_hook hook,
                               void *user);
 
+/* ------------------------------------------------------------------------
+ * Expert-slot indirection for the small-batch path.  FreeToken paper summary
+ * post on the minseoc03.com feed, section "3. Decode: Exploit Expert
+ * Locality" (a selected expert held in GPU memory is a hit and runs from
+ * there; one that is not is a miss) and section "10. Dynamic Scheduling
+ * Without Giving Up CUDA Graphs" (hit/miss classification and the rewrite of
+ * logical expert ids to physical slots happen on the GPU, no host round
+ * trip).  A pool of n_slots physical slots holds copies of some experts'
+ * MXFP4 weights; slot_of maps each logical expert to its slot or to -1.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  const int32_t *slot_of;      /* [E] device: slot of expert e in [0, n_slots), or -1 */
+  int32_t n_slots;             /* >= 1 */
+  const void *W1, *W3, *W2;    /* MXFP4 codes [n_slots][d_ff][d/2], [n_slots][d_ff][d/2]
+                                  (W3: SwiGLU only, else NULL), [n_slots][d][d_ff/2] */
+  const uint8_t *S1, *S3, *S2; /* E8M0 scales [n_slots][d_ff][d/32], ..., [n_slots][d][d_ff/32] */
+} moe_expert_pool;
+
+/* Indices of the counts written by moe_classify_experts / moe_forward_pooled. */
+enum {
+  MOE_POOL_SELECTED = 0,  /* distinct experts selected by the batch */
+  MOE_POOL_RESIDENT = 1,  /* of those, resident (hits) */
+  MOE_POOL_LOOKUPS = 2,   /* (token, slot) selections: n * K */
+  MOE_POOL_SERVED = 3     /* of those, selections of a resident expert */
+};
+
+/* Hit/miss classification of a batch's expert selections (device, async):
+ *   topk_idx int32 [n][K] as moe_route writes it; slot_of int32 [E] device.
+ *   state int32 [E]: -1 expert not selected, 1 selected and resident (hit),
+ *     0 selected and not resident (miss).
+ *   miss_list int32 [E]: the missed experts in ascending order, then -1.
+ *   counts int32 [4], indexed by MOE_POOL_*.
+ * Bit-exact.  A topk_idx value outside [0, E) or a slot_of value outside
+ * [-1, n_slots) sets MOE_ERR_BAD_INDEX in the status word (detail: the pair
+ * index or the expert; a bad slot counts as a miss). */
+moe_status moe_classify_experts(const moe_config *cfg, const int32_t *topk_idx,
+                                const int32_t *slot_of, int32_t n_slots, int32_t *state,
+                                int32_t *miss_list, int32_t *counts, void *ws, size_t ws_bytes,
+                                void *stream);
+
+/* moe_forward for a small batch (MXFP4 experts, bf16 activations, n*K <= 256,
+ * no shared expert; else MOE_ERR_UNSUPPORTED) whose expert FFNs read each
+ * selected expert from its pool slot when it is resident and from w (which
+ * holds all E experts and the router) when it is not.  The result equals
+ * moe_forward's bit for bit whatever the resident set, as long as the pool's
+ * slots hold byte copies of their experts.  state, miss_list and counts
+ * (each nullable) receive the classification of moe_classify_experts.  A
+ * slot outside [-1, n_slots) sets MOE_ERR_BAD_INDEX; as after any device-side
+ * error, the layer's later kernels then do nothing and y is undefined.
+ * Graph-capturable: replays follow the slot table's contents at replay time. */
+moe_status moe_forward_pooled(const moe_config *cfg, const void *x, const moe_weights *w,
+                              const moe_expert_pool *pool, void *y, int32_t *state,
+                              int32_t *miss_list, int32_t *counts, void *ws, size_t ws_bytes,
+                              void *stream);
+
+/* moe_forward_pooled with a stage hook (as moe_forward_staged; hook may be NULL). */
+moe_status moe_forward_pooled_staged(const moe_config *cfg, const void *x, const moe_weights *w,
+                                     const moe_expert_pool *pool, void *y, int32_t *state,
+                                     int32_t *miss_list, int32_t *counts, void *ws,
+                                     size_t ws_bytes, void *stream, moe_stage_hook hook,
+                                     void *user);
+
 /* Synchronises `stream`, then returns the workspace's device status word
  * (MOE_OK if no device-side fault was recorded).  detail, if not NULL,
  * receives the detail word (e.g. the offending pair index). */

@@ -1,117 +1,10 @@
-// Small-batch (decode) expert FFN over MXFP4 weights: stream only the
-// selected experts' weights, once, and dequantise them in registers.
-//
-// The decode step touches a few experts per token, so its time is the time
-// to read those experts' weight bytes from HBM ("Inference Optimization: The
-// Bandwidth Wall, PagedAttention, and FlashAttention": decode is bound by the
-// bytes of weights read per token).  Weights are MXFP4 (feed post "What is
-// MXFP4?": 4-bit elements in blocks of 32 sharing one scale; E2M1 elements and
-// E8M0 scales per the OCP MX v1.0 format).
-//
-// Work unit: one selected expert x 16 * RG output rows (RG MMA M tiles); the
-// warps of a 16-row group split the reduction.  Codes arrive by TMA (128-byte
-// boxes of 16 rows, 128-byte swizzle).  16 bytes of a row are exactly one MX
-// block (32 elements, one scale); lane (g = lane/4, t = lane%4) reads word t of
-// the block for rows g and g+8 and converts its bytes with
-// cvt.rn.f16x2.e2m1x2 straight into the A fragment of mma.sync.m16n8k16.  The
-// expert's tokens (up to 8 per pass, N = 8) are f16 rows read from L2 into
-// the B fragment.  Each 32-element block is multiplied with unscaled E2M1
-// values into a fresh fp32 partial, which is then scaled by the block's E8M0
-// scale and added to the fp32 accumulator.
-//
-// Activations enter the tensor core as f16 (E2M1 values are exact in f16);
-// an activation beyond the f16 range (|v| > 65504) is clamped to it.
-#include "common.cuh"
-#include "launch.h"
-#include "tc_common.cuh"
+// Small-batch (decode) expert FFN over MXFP4 weights: the launches without a
+// resident pool, and the f16 staging of activation rows.  The kernel itself
+// is in decode_kernel.cuh.
+#include "decode_kernel.cuh"
 
 namespace moe {
 namespace {
-
-constexpr int DV_WARPS = 8;                 // warps per CTA = row groups x reduction splits
-constexpr int DV_BOXB = 128;                // bytes of a row per TMA box: 8 MX blocks
-constexpr int DV_BOX = 16 * DV_BOXB;        // one box: 16 rows x 128 bytes (128-byte swizzle)
-constexpr int DV_STAGES = 2;                // boxes in flight per warp and matrix (a power of 2)
-constexpr int DV_TOK = 8;                   // tokens per pass (MMA N)
-
-struct DecodeArgs {
-  const int32_t *offsets;
-  int num_experts;
-  int P;
-  const uint16_t *act16;          // f16 activation rows: segment order [P][K], or token order
-  const int32_t *perm;            // (token order) segment position -> pair t*top_k + j, else nullptr
-  int top_k;
-  const uint8_t *S, *S3;          // scales [E][R][K/32] (S3: SwiGLU linear branch or nullptr)
-  int R, K;
-  __nv_bfloat16 *out;             // [P][R]
-  uint16_t *out16;                // f16 copy of out (the next projection's input), or nullptr
-  int *status;
-};
-
-// The four code pairs of a 32-bit word (bytes 0..3) as four f16 pairs; each
-// pair's low half is the low nibble (the even element).
-struct F16x2x4 {
-  uint32_t v[4];
-};
-__device__ __forceinline__ F16x2x4 e2m1x8_to_f16x2x4(uint32_t w) {
-  F16x2x4 r;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3])
-      : "r"(w));
-  return r;
-}
-
-// d = A * B (+ c), m16n8k16, f16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void mma_16816_first(float (&c)[4], uint32_t a0, uint32_t a1,
-                                                uint32_t a2, uint32_t a3, uint32_t b0,
-                                                uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%10,%10,%10,%10};"
-      : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
-}
-
-// One MX block (32 elements) of rows g and g+8 against 8 tokens.  The block's
-// 32 elements are fed to the two K=16 MMAs in a permuted order that both
-// operands share: lane (g, t) owns word t of each row (elements 8t..8t+7) and
-// the same 8 elements of its token's activation row.  MMA 1 takes bytes 0, 1
-// of the word (elements 8t..8t+3), MMA 2 bytes 2, 3 (8t+4..8t+7).  A
-// reduction does not depend on the order of its terms.
-__device__ __forceinline__ void mx_block(float (&acc)[4], uint32_t wg, uint32_t wh, float sg,
-                                         float sh, const uint4 &b) {
-  const F16x2x4 ag = e2m1x8_to_f16x2x4(wg), ah = e2m1x8_to_f16x2x4(wh);
-  float p[4];
-  mma_16816_first(p, ag.v[0], ah.v[0], ag.v[1], ah.v[1], b.x, b.y);
-  mma_16816(p, ag.v[2], ah.v[2], ag.v[3], ah.v[3], b.z, b.w);
-  acc[0] = fmaf(sg, p[0], acc[0]);
-  acc[1] = fmaf(sg, p[1], acc[1]);
-  acc[2] = fmaf(sh, p[2], acc[2]);
-  acc[3] = fmaf(sh, p[3], acc[3]);
-}
-
-__device__ __forceinline__ uint16_t to_f16_bits(float v) {
-  v = fminf(fmaxf(v, -65504.f), 65504.f);
-  const __half h = __float2half_rn(v);
-  return *reinterpret_cast<const uint16_t *>(&h);
-}
-
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
-                                          uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(tc::smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(tc::smem_u32(bar))
-      : "memory");
-}
 
 // Expert-ordered activation rows as f16: dst[q] = src[perm[q] / top_k] (perm
 // given) or src[q], values clamped to the f16 range.
@@ -140,515 +33,6 @@ __global__ void rows_to_f16_kernel(const __nv_bfloat16 *__restrict__ src,
   }
 }
 
-// Group barrier on named barrier 1 + id over n threads: returns the OR of
-// pred over the group (every thread gets the same answer).
-__device__ __forceinline__ bool group_sync_or(int id, int n, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(1 + id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-
-// Shared-memory plan of the decode kernel (bytes from the 1024-aligned base).
-struct DecodePlan {
-  int KB;          // MX blocks per row
-  int bps;         // blocks per reduction split
-  int PP;          // decoded-scale row pitch (u32) of one warp
-  int sc_pitch;    // raw scale bytes of one unit and matrix, padded to 16
-  int nraw;        // raw scale buffers (two for short units: copies run two units ahead)
-  size_t raw_off, pairs_off, red_off, bytes;
-};
-
-__host__ __device__ inline DecodePlan decode_plan(int nmat, int K, int rg) {
-  DecodePlan p;
-  const int ks = DV_WARPS / rg;
-  p.KB = K / 32;
-  // an even split point keeps every warp's first raw scale byte 2-byte aligned
-  p.bps = (((p.KB + ks - 1) / ks) + 1) & ~1;
-  p.PP = (p.bps + 7) & ~7;
-  if (p.PP % 32 == 0) p.PP += 8;   // rows g and g + 1 of a quarter-warp on other banks
-  p.sc_pitch = (16 * rg * p.KB + 15) & ~15;
-  p.nraw = rg == 1 ? 2 : 1;
-  p.raw_off = (size_t)DV_WARPS * DV_STAGES * 2 * DV_BOX;
-  p.pairs_off = p.raw_off + (size_t)p.nraw * nmat * p.sc_pitch;
-  p.red_off = p.pairs_off + (size_t)DV_WARPS * nmat * 8 * p.PP * 4;
-  const int red_vals = ks == 2 ? 4 : 8;
-  p.bytes = p.red_off + (size_t)2 * DV_WARPS * red_vals * 32 * 4;
-  return p;
-}
-
-// EPI: 0 none, 1 relu, 2 swiglu (tm3 / S3 hold the linear branch).  RG: 16-row
-// groups per CTA; the KS = DV_WARPS / RG warps of a group split the reduction
-// into contiguous, equal runs of MX blocks.
-//
-// Persistent: the grid is sized to the GPU and each CTA walks its share of the
-// work units (selected expert x 16 * RG output rows), slot-major.  The groups
-// of a CTA run independently: the warps of a group meet only on their own
-// named barrier, once per token pass, to add their partial sums.  Each warp
-// keeps its own ring of 128-byte code boxes per matrix in flight; lane 0
-// refills a slot as soon as the warp has read it, with the next box of the
-// warp's sequence (across token passes and units), so the weight stream does
-// not stop at unit boundaries.  A unit's E8M0 bytes are bulk-copied into
-// shared memory ahead of it (one unit ahead, two for short 16-row units);
-// each warp decodes the part it reads into bf16 pairs (row g | row g + 8), so
-// that the inner loop takes eight blocks' scales with two 16-byte loads, and
-// the last warp done with a raw buffer issues the copy for the unit that uses
-// it next.  B fragments (the tokens' f16 activation rows, a few KB in L2) are
-// loaded at the top of each slot, and the next slot's lines are prefetched
-// into L1.
-template <int EPI, int RG>
-__global__ void __launch_bounds__(32 * DV_WARPS, 2)
-decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm3,
-                    DecodeArgs a) {
-  constexpr int NMAT = (EPI == 2) ? 2 : 1;
-  constexpr int KS = DV_WARPS / RG;
-  constexpr int CTA_ROWS = 16 * RG;
-  constexpr int RV = KS == 2 ? 4 : 8;   // partial sums a warp hands over per lane
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  __shared__ uint64_t full[DV_WARPS][DV_STAGES];
-  __shared__ uint64_t sbar[2];
-  __shared__ int s_abort;
-  __shared__ int s_nactive;
-  __shared__ unsigned s_raw_done;
-  __shared__ int s_active[256], s_beg[256], s_cnt[256];
-  __shared__ int s_row[kDecodeMaxPairs];          // activation row of each segment position
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_launch_dependents();
-  if (threadIdx.x == 0) {
-    tc::prefetch_tmap(&tm1);
-    if (NMAT == 2) tc::prefetch_tmap(&tm3);
-  }
-  pdl_wait();
-  if (status_failed(a.status)) return;
-
-  // the experts with a non-empty segment, in order (E <= 256, one round of loads)
-  if (warp == 0) {
-    int off_lo[8], off_hi[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = 32 * j + lane;
-      off_lo[j] = e < a.num_experts ? a.offsets[e] : 0;
-      off_hi[j] = e < a.num_experts ? a.offsets[e + 1] : 0;
-    }
-    int seen = 0, bad = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = 32 * j + lane;
-      const bool ne = e < a.num_experts && off_hi[j] > off_lo[j];
-      if (e < a.num_experts && (off_lo[j] < 0 || off_hi[j] < off_lo[j] || off_hi[j] > a.P)) bad = 1;
-      const unsigned m = __ballot_sync(0xffffffffu, ne);
-      if (ne) {
-        const int q = seen + __popc(m & lanemask_lt());
-        s_active[q] = e;
-        s_beg[q] = off_lo[j];
-        s_cnt[q] = off_hi[j] - off_lo[j];
-      }
-      seen += __popc(m);
-    }
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) {
-      s_nactive = bad ? 0 : seen;
-      if (bad) set_status(a.status, MOE_ERR_BAD_INDEX, -1);
-      s_abort = 0;
-      s_raw_done = 0;
-      tc::mbar_init(&sbar[0], 1);
-      tc::mbar_init(&sbar[1], 1);
-    }
-  }
-  if (warp == 1) {
-    for (int q = lane; q < a.P; q += 32) {
-      int row = q;
-      if (a.perm) {
-        const int p = a.perm[q];
-        row = (p >= 0 && p < a.P) ? p / a.top_k : 0;
-        if (p < 0 || p >= a.P) set_status(a.status, MOE_ERR_BAD_INDEX, q);
-      }
-      s_row[q] = row;
-    }
-  }
-  if (lane == 0) {
-    for (int st = 0; st < DV_STAGES; ++st) tc::mbar_init(&full[warp][st], 1);
-    tc::fence_mbar_init();
-  }
-  __syncthreads();
-  uint8_t *smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
-  const DecodePlan plan = decode_plan(NMAT, a.K, RG);
-  const int K = a.K, R = a.R, KB = plan.KB, PP = plan.PP, sc_pitch = plan.sc_pitch;
-  const int grp = warp / KS, split = warp - grp * KS;
-  const int b_beg = min(KB, split * plan.bps), b_end = min(KB, b_beg + plan.bps);
-  const int nbl = b_end - b_beg;                        // this warp's MX blocks per row
-  // a ring slot holds two 16 x 128-byte boxes: the same 8 MX blocks of both
-  // matrices (SwiGLU), or 16 consecutive blocks of the one matrix
-  constexpr int SUB = (NMAT == 2) ? 1 : 2;              // 8-block groups per slot
-  constexpr int SB = 8 * SUB;                           // MX blocks per slot
-  const int nslot = (nbl + SB - 1) / SB;
-  const int row_blocks = (R + CTA_ROWS - 1) / CTA_ROWS;
-  const int total = s_nactive * row_blocks;
-  uint8_t *ring = smem + (size_t)warp * DV_STAGES * 2 * DV_BOX;
-  const int NRAW = plan.nraw;
-  uint32_t *pw = reinterpret_cast<uint32_t *>(smem + plan.pairs_off) + (size_t)warp * NMAT * 8 * PP;
-  float *red = reinterpret_cast<float *>(smem + plan.red_off);   // [2][DV_WARPS][RV][32]
-  const int g = lane >> 2, t = lane & 3;
-  // byte offset of word t of 16-byte chunk (bl ^ g) in row g of a box with
-  // the 128-byte swizzle: lane_off ^ (bl << 4)
-  const uint32_t lane_off = (uint32_t)(g * DV_BOXB + (g << 4) + 4 * t);
-  volatile int *abort = &s_abort;
-
-  // raw E8M0 bytes of this CTA's unit i into buffer i % NRAW (NRAW copies in
-  // flight at most; a thread drains the copies it issued on abort)
-  int raw_mine0 = -1, raw_mine1 = -1;   // last unit copied into buffer 0 / 1
-  auto fetch_raw = [&](int i) {
-    const int u = (int)blockIdx.x + i * (int)gridDim.x;
-    if (u >= total) return;
-    const int sl = u / row_blocks;
-    const int e = s_active[sl], r0 = (u - sl * row_blocks) * CTA_ROWS;
-    const uint32_t bytes = (uint32_t)min(CTA_ROWS, R - r0) * KB;   // rows % 16 == 0
-    const int b = i % NRAW;
-    tc::mbar_arrive_expect_tx(&sbar[b], NMAT * bytes);
-    uint8_t *dst = smem + plan.raw_off + (size_t)b * NMAT * sc_pitch;
-    bulk_load(dst, a.S + ((size_t)e * R + r0) * KB, bytes, &sbar[b]);
-    if (NMAT == 2) bulk_load(dst + sc_pitch, a.S3 + ((size_t)e * R + r0) * KB, bytes, &sbar[b]);
-    if (b) raw_mine1 = i;
-    else raw_mine0 = i;
-  };
-
-  // the producer's cursor over this warp's boxes (lane 0): unit p_i, pass
-  // p_pass, box p_c; p_wrow is the first weight row of the warp's group
-  int p_i = 0, p_pass = 0, p_c = 0, p_passes = 0, p_wrow = 0, issued = 0;
-  bool p_valid = false, p_active = false;
-  auto p_load_unit = [&]() {
-    const int u = (int)blockIdx.x + p_i * (int)gridDim.x;
-    p_valid = nslot > 0 && u < total;
-    if (!p_valid) return;
-    const int sl = u / row_blocks;
-    const int r = (u - sl * row_blocks) * CTA_ROWS + grp * 16;
-    p_active = r < R;
-    p_wrow = s_active[sl] * R + r;
-    p_passes = (s_cnt[sl] + DV_TOK - 1) / DV_TOK;
-  };
-  auto issue_next = [&]() {
-    if (!p_valid) return;
-    const int sl = issued & (DV_STAGES - 1);
-    if (p_active) {
-      tc::mbar_arrive_expect_tx(&full[warp][sl], 2 * DV_BOX);
-      uint8_t *dst = ring + (size_t)sl * 2 * DV_BOX;
-      const int x = (b_beg + SB * p_c) * 16;            // a multiple of 16 bytes
-      tc::tma_load_2d(&tm1, &full[warp][sl], dst, x, p_wrow);
-      // (a box past the end of the row reads zeros)
-      if (NMAT == 2) tc::tma_load_2d(&tm3, &full[warp][sl], dst + DV_BOX, x, p_wrow);
-      else tc::tma_load_2d(&tm1, &full[warp][sl], dst + DV_BOX, x + DV_BOXB, p_wrow);
-    } else {
-      tc::mbar_arrive(&full[warp][sl]);   // a group past the last row: keep the phases in step
-    }
-    ++issued;
-    if (++p_c == nslot) {
-      p_c = 0;
-      if (++p_pass == p_passes) {
-        p_pass = 0;
-        ++p_i;
-        p_load_unit();
-      }
-    }
-  };
-
-  if (threadIdx.x == 0)
-    for (int i = 0; i < NRAW; ++i) fetch_raw(i);
-  if (lane == 0) {
-    p_load_unit();
-    for (int st = 0; st < DV_STAGES; ++st) issue_next();
-  }
-  int consumed = 0, npass = 0;
-  bool ok = true;
-
-  for (int i = 0;; ++i) {
-    const int u = (int)blockIdx.x + i * (int)gridDim.x;
-    if (u >= total) break;
-    const int sl = u / row_blocks;
-    const int r0 = (u - sl * row_blocks) * CTA_ROWS + grp * 16;
-    const bool active = r0 < R;
-    const int beg = s_beg[sl], cnt = s_cnt[sl];
-
-    // this unit's scales: wait for the raw bytes, decode this warp's part into
-    // pairs; the last warp to finish issues the next unit's copy
-    ok = __all_sync(0xffffffffu,
-                    tc::mbar_wait(&sbar[i % NRAW], (uint32_t)((i / NRAW) & 1), abort));
-    // the warps of a group leave together, so none waits on a barrier alone
-    if (group_sync_or(grp, 32 * KS, !ok)) { ok = false; break; }
-    {
-      // lane (gg = lane / 4, q = lane % 4) takes blocks 2q, 2q + 1, 2q + 8, ...
-      // of row pair gg: two raw bytes of row gg and two of row gg + 8 per step
-      // (16-bit loads where the row pitch is even: the split point always is)
-      const int gg = lane >> 2, q = lane & 3;
-      const bool even = (KB & 1) == 0;
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m) {
-        const uint8_t *src = smem + plan.raw_off + (size_t)((i % NRAW) * NMAT + m) * sc_pitch +
-                             (grp * 16 + gg) * KB + b_beg;
-        uint32_t *dst = pw + (m * 8 + gg) * PP;
-        for (int b = 2 * q; b < nbl; b += 8) {
-          const bool two = b + 1 < nbl;
-          uint32_t x, y;
-          if (even) {
-            x = *reinterpret_cast<const uint16_t *>(src + b);
-            y = *reinterpret_cast<const uint16_t *>(src + b + 8 * KB);
-          } else {
-            x = src[b] | (two ? (uint32_t)src[b + 1] << 8 : 0u);
-            y = src[b + 8 * KB] | (two ? (uint32_t)src[b + 1 + 8 * KB] << 8 : 0u);
-          }
-          // bf16 of 2^(s-127): s << 7, and 0x0040 (2^-127, a subnormal) for s = 0
-          const uint32_t p0 = __vmaxu2(__byte_perm(x, y, 0x7460) << 7, 0x00400040u);
-          const uint32_t p1 = __vmaxu2(__byte_perm(x, y, 0x7561) << 7, 0x00400040u);
-          if (two) *reinterpret_cast<uint2 *>(dst + b) = make_uint2(p0, p1);
-          else dst[b] = p0;
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) {
-      __threadfence_block();
-      if (atomicAdd(&s_raw_done, 1u) == (unsigned)((i + 1) * DV_WARPS - 1)) {
-        __threadfence_block();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        fetch_raw(i + NRAW);
-      }
-    }
-    const uint32_t *pr1 = pw + g * PP;
-    const uint32_t *pr3 = pr1 + 8 * PP;
-
-    for (int tg = 0; tg < cnt; tg += DV_TOK, ++npass) {
-      // token g of this pass, or the pass's last token where g is past it (its
-      // results are not stored)
-      const int tok = tg + min(g, cnt - tg - 1);
-      const uint16_t *xrow = a.act16 + (size_t)s_row[beg + tok] * K + (size_t)b_beg * 32 + 8 * t;
-      const uint16_t *xpf = a.act16 + (size_t)s_row[beg + tg + min(lane >> 2, cnt - tg - 1)] * K +
-                            (size_t)b_beg * 32 + (lane & 3) * 64;
-      float acc1[4] = {0.f, 0.f, 0.f, 0.f}, acc3[4] = {0.f, 0.f, 0.f, 0.f};
-      uint4 bx[8];
-      // B fragments of the 8-block group starting at local block cb
-      auto load_bx = [&](int cb, int nb) {
-        const uint16_t *xb = xrow + cb * 32;
-#pragma unroll
-        for (int bl = 0; bl < 8; ++bl)
-          bx[bl] = (bl < nb) ? __ldg(reinterpret_cast<const uint4 *>(xb + bl * 32))
-                             : make_uint4(0u, 0u, 0u, 0u);
-      };
-      // the 8-block group at local block cb: matrix 1 in box sw (matrix 3,
-      // SwiGLU, in the box after it)
-      auto compute8 = [&](const uint8_t *sw, int cb, int nb) {
-        const uint4 s1a = *reinterpret_cast<const uint4 *>(pr1 + cb);
-        const uint4 s1b = *reinterpret_cast<const uint4 *>(pr1 + cb + 4);
-        uint4 s3a = s1a, s3b = s1b;
-        if constexpr (NMAT == 2) {
-          s3a = *reinterpret_cast<const uint4 *>(pr3 + cb);
-          s3b = *reinterpret_cast<const uint4 *>(pr3 + cb + 4);
-        }
-        const uint32_t sp1[8] = {s1a.x, s1a.y, s1a.z, s1a.w, s1b.x, s1b.y, s1b.z, s1b.w};
-        const uint32_t sp3[8] = {s3a.x, s3a.y, s3a.z, s3a.w, s3b.x, s3b.y, s3b.z, s3b.w};
-        auto block = [&](int bl) {
-          const uint8_t *w = sw + (lane_off ^ (uint32_t)(bl << 4));
-          const uint32_t wg = *reinterpret_cast<const uint32_t *>(w);
-          const uint32_t wh = *reinterpret_cast<const uint32_t *>(w + 8 * DV_BOXB);
-          mx_block(acc1, wg, wh, __uint_as_float(sp1[bl] << 16),
-                   __uint_as_float(sp1[bl] & 0xffff0000u), bx[bl]);
-          if constexpr (NMAT == 2) {
-            const uint32_t vg = *reinterpret_cast<const uint32_t *>(w + DV_BOX);
-            const uint32_t vh = *reinterpret_cast<const uint32_t *>(w + DV_BOX + 8 * DV_BOXB);
-            mx_block(acc3, vg, vh, __uint_as_float(sp3[bl] << 16),
-                     __uint_as_float(sp3[bl] & 0xffff0000u), bx[bl]);
-          }
-        };
-        if (nb == 8) {
-          // a full group: straight-line code, so the eight blocks' independent
-          // MMA chains can be interleaved
-#pragma unroll
-          for (int bl = 0; bl < 8; ++bl) block(bl);
-        } else {
-#pragma unroll
-          for (int bl = 0; bl < 8; ++bl)
-            if (bl < nb) block(bl);
-        }
-      };
-      for (int c = 0; c < nslot; ++c) {
-        const int cb = c * SB;
-        const int slot = consumed & (DV_STAGES - 1);
-        const uint32_t parity = (uint32_t)(consumed / DV_STAGES) & 1u;
-        ++consumed;
-        if (active) {
-          load_bx(cb, min(8, nbl - cb));
-          // the next slot's activation lines: one 128-byte line (two blocks)
-          // per lane and 8-block group
-#pragma unroll
-          for (int h = 0; h < SUB; ++h)
-            if (c + 1 < nslot && (lane & 3) * 2 < nbl - (cb + SB + 8 * h))
-              asm volatile("prefetch.global.L1 [%0];" ::"l"(xpf + (cb + SB + 8 * h) * 32));
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(&full[warp][slot], parity, abort));
-          if (!ok) break;
-          const uint8_t *st = ring + (size_t)slot * 2 * DV_BOX;
-          compute8(st, cb, min(8, nbl - cb));
-          if constexpr (SUB == 2) {
-            if (nbl - cb > 8) {
-              load_bx(cb + 8, min(8, nbl - cb - 8));
-              compute8(st + DV_BOX, cb + 8, min(8, nbl - cb - 8));
-            }
-          }
-        } else {
-          // a group past the last row: its slots were arrived on without data
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(&full[warp][slot], parity, abort));
-          if (!ok) break;
-        }
-        __syncwarp();
-        if (lane == 0) {
-          // the slot was read through the generic proxy; order those reads
-          // before the TMA engine overwrites it
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          issue_next();
-        }
-      }
-      // partial sums of the group's warps, added in warp order.  Two splits:
-      // each warp finishes one row (split 0 row g, split 1 row g + 8) and hands
-      // the other row's sums to its partner.  More splits: the first warp
-      // finishes both rows.
-      float *rb = red + (size_t)(npass & 1) * DV_WARPS * RV * 32;
-      float f1[2], f3[2];   // this warp's finished values: tokens 2t, 2t+1 of its row
-      int frow;
-      bool fin;
-      if constexpr (KS == 2) {
-        const bool s0 = split == 0;
-        // kept: this warp's row; given: the partner's row
-        const float k10 = s0 ? acc1[0] : acc1[2], k11 = s0 ? acc1[1] : acc1[3];
-        const float k30 = s0 ? acc3[0] : acc3[2], k31 = s0 ? acc3[1] : acc3[3];
-        rb[(warp * RV + 0) * 32 + lane] = s0 ? acc1[2] : acc1[0];
-        rb[(warp * RV + 1) * 32 + lane] = s0 ? acc1[3] : acc1[1];
-        rb[(warp * RV + 2) * 32 + lane] = s0 ? acc3[2] : acc3[0];
-        rb[(warp * RV + 3) * 32 + lane] = s0 ? acc3[3] : acc3[1];
-        if (group_sync_or(grp, 32 * KS, !ok)) { ok = false; break; }
-        const int pw_ = warp ^ 1;
-        // warp order: split 0's sum first
-        const float o10 = rb[(pw_ * RV + 0) * 32 + lane], o11 = rb[(pw_ * RV + 1) * 32 + lane];
-        const float o30 = rb[(pw_ * RV + 2) * 32 + lane], o31 = rb[(pw_ * RV + 3) * 32 + lane];
-        f1[0] = s0 ? k10 + o10 : o10 + k10;
-        f1[1] = s0 ? k11 + o11 : o11 + k11;
-        f3[0] = s0 ? k30 + o30 : o30 + k30;
-        f3[1] = s0 ? k31 + o31 : o31 + k31;
-        frow = s0 ? g : g + 8;
-        fin = active;
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          rb[(warp * RV + q) * 32 + lane] = acc1[q];
-          rb[(warp * RV + 4 + q) * 32 + lane] = acc3[q];
-        }
-        if (group_sync_or(grp, 32 * KS, !ok)) { ok = false; break; }
-        // the first warp finishes row g, the second row g + 8
-        fin = active && split < 2;
-        const int q0 = split == 1 ? 2 : 0;
-        f1[0] = f1[1] = f3[0] = f3[1] = 0.f;
-        if (fin) {
-#pragma unroll
-          for (int w = 0; w < KS; ++w) {
-            const int ww = grp * KS + w;
-            f1[0] += rb[(ww * RV + q0) * 32 + lane];
-            f1[1] += rb[(ww * RV + q0 + 1) * 32 + lane];
-            f3[0] += rb[(ww * RV + 4 + q0) * 32 + lane];
-            f3[1] += rb[(ww * RV + 4 + q0 + 1) * 32 + lane];
-          }
-        }
-        frow = split == 1 ? g + 8 : g;
-      }
-      if (fin) {
-        const int row = r0 + frow;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          float v;
-          if constexpr (EPI == 2) v = f1[q] / (1.f + __expf(-f1[q])) * f3[q];
-          else if constexpr (EPI == 1) v = fmaxf(f1[q], 0.f);
-          else v = f1[q];
-          const int tk = tg + 2 * t + q;
-          if (tk < cnt && row < R) {
-            const __nv_bfloat16 hb = __float2bfloat16_rn(v);
-            a.out[(size_t)(beg + tk) * R + row] = hb;
-            if (a.out16) a.out16[(size_t)(beg + tk) * R + row] = to_f16_bits(__bfloat162float(hb));
-          }
-        }
-      }
-    }
-    if (!ok) break;
-  }
-  if (!ok) {
-    // let the copies this warp issued land before it exits
-    if (lane == 0) {
-      for (int j = consumed; j < issued; ++j)
-        tc::mbar_wait_drain(&full[warp][j % DV_STAGES], (uint32_t)(j / DV_STAGES) & 1u,
-                            100000000ull);
-      if (raw_mine0 >= 0)
-        tc::mbar_wait_drain(&sbar[0], (uint32_t)((raw_mine0 / NRAW) & 1), 100000000ull);
-      if (raw_mine1 >= 0)
-        tc::mbar_wait_drain(&sbar[1], (uint32_t)((raw_mine1 / NRAW) & 1), 100000000ull);
-      set_status(a.status, MOE_ERR_TIMEOUT, blockIdx.x);
-    }
-  }
-}
-
-template <int EPI, int RG>
-cudaError_t launch_one(DecodeArgs a, const uint8_t *W, const uint8_t *W3, int num_experts,
-                       int slots, cudaStream_t s) {
-  constexpr int NMAT = (EPI == 2) ? 2 : 1;
-  const size_t smem = 1024 + decode_plan(NMAT, a.K, RG).bytes;
-  static size_t smem_set = 0;
-  static int per_sm = 0;
-  if (smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mxfp4_kernel<EPI, RG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    smem_set = smem;
-    per_sm = 0;
-  }
-  if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mxfp4_kernel<EPI, RG>,
-                                                      32 * DV_WARPS, smem) != cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1;
-  }
-  CUtensorMap m1, m3;
-  const uint64_t dims[2] = {(uint64_t)a.K / 2, (uint64_t)num_experts * a.R};
-  const uint32_t box[2] = {DV_BOXB, 16};
-  if (!make_tensor_map(&m1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, 2, dims, box,
-                       CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
-  if (NMAT == 2) {
-    if (!make_tensor_map(&m3, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W3, 2, dims, box,
-                         CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  } else {
-    m3 = m1;
-  }
-  // units: at most `slots` experts x row blocks; no more CTAs than units
-  const long units = (long)slots * ((a.R + 16 * RG - 1) / (16 * RG));
-  long grid = (long)per_sm * num_sms();
-  if (grid > units) grid = units;
-  if (grid < 1) grid = 1;
-  return launch_pdl(decode_mxfp4_kernel<EPI, RG>, dim3((unsigned)grid), dim3(32 * DV_WARPS), smem,
-                    s, m1, m3, a);
-}
-
-// Rows per work unit: 64 (four 16-row groups, two reduction splits each)
-// where that still gives every resident CTA a unit, else 32, else 16.  Longer
-// units spread the per-unit costs (scale decoding, the partial-sum exchange,
-// the epilogue) over more weight bytes.
-template <int EPI>
-cudaError_t launch_rg(DecodeArgs a, const uint8_t *W, const uint8_t *W3, int num_experts,
-                      int slots, cudaStream_t s) {
-  const long ctas = 2L * num_sms();
-  auto units = [&](int rg) { return (long)slots * ((a.R + 16 * rg - 1) / (16 * rg)); };
-  if (units(4) >= ctas) return launch_one<EPI, 4>(a, W, W3, num_experts, slots, s);
-  if (units(2) >= ctas) return launch_one<EPI, 2>(a, W, W3, num_experts, slots, s);
-  return launch_one<EPI, 1>(a, W, W3, num_experts, slots, s);
-}
-
 }  // namespace
 
 bool decode_supported(const moe_config &c) {
@@ -675,43 +59,12 @@ cudaError_t launch_rows_to_f16(const void *src, const int32_t *perm, int top_k, 
 
 cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
                               const int32_t *perm, const int32_t *offsets, const moe_weights &w,
-                              void *h, void *y_perm, void *act16, int *status, cudaStream_t s) {
-  const int P = c.n * c.top_k;
-  const int slots = P < c.n_experts ? P : c.n_experts;
-  uint16_t *x16 = static_cast<uint16_t *>(act16);
-  uint16_t *h16 = x16 + (size_t)P * c.d;
-  DecodeArgs a{};
-  a.offsets = offsets;
-  a.num_experts = c.n_experts;
-  a.P = P;
-  a.status = status;
-  a.top_k = c.top_k;
-  if (part == 0) {
-    if (act != nullptr) {
-      cudaError_t e = launch_rows_to_f16(act, perm, c.top_k, P, c.d, x16, status, s);
-      if (e != cudaSuccess) return e;
-    } else {
-      a.perm = perm;   // x16 holds the x rows in token order
-    }
-    a.act16 = x16;
-    a.S = w.S1;
-    a.S3 = w.S3;
-    a.R = c.d_ff;
-    a.K = c.d;
-    a.out = static_cast<__nv_bfloat16 *>(h);
-    a.out16 = h16;
-    const uint8_t *W1 = static_cast<const uint8_t *>(w.W1), *W3 = static_cast<const uint8_t *>(w.W3);
-    return c.act == MOE_ACT_SWIGLU ? launch_rg<2>(a, W1, W3, c.n_experts, slots, s)
-                                   : launch_rg<1>(a, W1, nullptr, c.n_experts, slots, s);
-  }
-  a.act16 = h16;
-  a.S = w.S2;
-  a.S3 = nullptr;
-  a.R = c.d;
-  a.K = c.d_ff;
-  a.out = static_cast<__nv_bfloat16 *>(y_perm);
-  a.out16 = nullptr;
-  return launch_rg<0>(a, static_cast<const uint8_t *>(w.W2), nullptr, c.n_experts, slots, s);
+                              void *h, void *y_perm, void *act16, int *status, cudaStream_t s,
+                              const moe_expert_pool *pool) {
+  if (pool) return launch_decode_ffn_pooled(c, part, act, perm, offsets, w, h, y_perm, act16,
+                                            status, s, *pool);
+  return run_decode_ffn<false>(c, part, act, perm, offsets, w, h, y_perm, act16, status, s,
+                               nullptr);
 }
 
 }  // namespace moe

@@ -38,17 +38,85 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 raw) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Hit/miss classification by one warp from the per-expert selection counts
+// (FreeToken paper summary post, section "3. Decode: Exploit Expert
+// Locality": a selected expert in GPU memory is a hit, otherwise a miss).
+// Experts are visited in ascending order, 32 at a time, so the miss list is
+// sorted.  A slot outside [-1, n_slots) is reported and counted as a miss.
+__device__ void classify_warp(const int *cnt, int E, const int32_t *__restrict__ slot_of,
+                              int n_slots, int lookups, int32_t *state, int32_t *miss_list,
+                              int32_t *counts, int *status) {
+  const int lane = threadIdx.x & 31;
+  int misses = 0, selected = 0, resident = 0, served = 0;
+  for (int e0 = 0; e0 < E; e0 += 32) {
+    const int e = e0 + lane;
+    const int c = e < E ? cnt[e] : 0;
+    int slot = -1;
+    if (e < E) {
+      slot = slot_of[e];
+      if (slot < -1 || slot >= n_slots) {
+        set_status(status, MOE_ERR_BAD_INDEX, e);
+        slot = -1;
+      }
+    }
+    const bool chosen = c > 0, hit = chosen && slot >= 0, miss = chosen && slot < 0;
+    if (state && e < E) state[e] = chosen ? (hit ? 1 : 0) : -1;
+    const unsigned mm = __ballot_sync(0xffffffffu, miss);
+    if (miss && miss_list) miss_list[misses + __popc(mm & lanemask_lt())] = e;
+    misses += __popc(mm);
+    selected += __popc(__ballot_sync(0xffffffffu, chosen));
+    resident += __popc(__ballot_sync(0xffffffffu, hit));
+    served += hit ? c : 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) served += __shfl_xor_sync(0xffffffffu, served, o);
+  if (miss_list)
+    for (int i = misses + lane; i < E; i += 32) miss_list[i] = -1;
+  if (counts && lane == 0) {
+    counts[MOE_POOL_SELECTED] = selected;
+    counts[MOE_POOL_RESIDENT] = resident;
+    counts[MOE_POOL_LOOKUPS] = lookups;
+    counts[MOE_POOL_SERVED] = served;
+  }
+}
+
+// Standalone classification from topk_idx: one CTA.
+__global__ void __launch_bounds__(256)
+classify_kernel(const int32_t *__restrict__ topk_idx, int P, int E,
+                const int32_t *__restrict__ slot_of, int n_slots, int32_t *state,
+                int32_t *miss_list, int32_t *counts, int *status) {
+  __shared__ int s_cnt[256];
+  for (int e = threadIdx.x; e < 256; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int e = topk_idx[p];
+    if (e < 0 || e >= E) set_status(status, MOE_ERR_BAD_INDEX, p);
+    else atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32)
+    classify_warp(s_cnt, E, slot_of, n_slots, P, state, miss_list, counts, status);
+}
+
 // Every CTA converts its share of the x rows to f16 in token order
 // (act16[t] = f16(x[t]), clamped to the f16 range).  The first cluster also
 // routes: token t is selected by warp (t / DR_CLUSTER) % DR_WARPS of CTA
 // t % DR_CLUSTER, the cluster meets on its barrier, and CTA 0 derives the
-// dispatch arrays from the selections.
+// dispatch arrays from the selections (and, given a slot table, classifies
+// the selected experts against the resident pool).
+struct PoolOut {
+  const int32_t *slot_of;   // nullptr: no classification
+  int n_slots;
+  int32_t *state, *miss_list, *counts;
+};
+
 __global__ void __cluster_dims__(DR_CLUSTER, 1, 1) __launch_bounds__(DR_THREADS)
 decode_route_kernel(const float *__restrict__ logits, int n, int E, int k, int gate_mode,
                     const __nv_bfloat16 *__restrict__ x, int d, int32_t *__restrict__ topk_idx,
                     float *__restrict__ topk_gate, int32_t *__restrict__ counts,
                     int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
-                    int32_t *__restrict__ inv_perm, uint16_t *__restrict__ act16, int *status) {
+                    int32_t *__restrict__ inv_perm, uint16_t *__restrict__ act16, PoolOut pool,
+                    int *status) {
   __shared__ int32_t s_idx[kDecodeMaxPairs];
   __shared__ int s_cnt[256];
   __shared__ int s_off[256];
@@ -94,6 +162,9 @@ decode_route_kernel(const float *__restrict__ logits, int n, int E, int k, int g
     atomicAdd(&s_cnt[e], 1);
   }
   __syncthreads();
+  if (warp == 1 && pool.slot_of)
+    classify_warp(s_cnt, E, pool.slot_of, pool.n_slots, P, pool.state, pool.miss_list,
+                  pool.counts, status);
   if (warp == 0) {
     // exclusive prefix sum of the counts (lane l owns experts 8l .. 8l+7)
     int c[8], run = 0;
@@ -147,7 +218,8 @@ bool decode_route_supported(const moe_config &c) {
 cudaError_t launch_decode_route(const moe_config &c, const float *logits, const void *x,
                                 int32_t *topk_idx, float *topk_gate, int32_t *counts,
                                 int32_t *offsets, int32_t *perm, int32_t *inv_perm, void *act16,
-                                int *status, cudaStream_t s) {
+                                int *status, cudaStream_t s, const moe_expert_pool *pool,
+                                int32_t *state, int32_t *miss_list, int32_t *pool_counts) {
   // enough clusters that every thread converts at most DR_UNROLL x vectors
   const long vec = (long)c.n * (c.d / 8);
   const long per_cluster = (long)DR_CLUSTER * DR_THREADS * DR_UNROLL;
@@ -155,10 +227,26 @@ cudaError_t launch_decode_route(const moe_config &c, const float *logits, const 
   const long max_clusters = num_sms() / DR_CLUSTER;
   if (clusters > max_clusters) clusters = max_clusters;
   if (clusters < 1) clusters = 1;
+  PoolOut po{};
+  if (pool) {
+    po.slot_of = pool->slot_of;
+    po.n_slots = pool->n_slots;
+    po.state = state;
+    po.miss_list = miss_list;
+    po.counts = pool_counts;
+  }
   return launch_pdl(decode_route_kernel, dim3((unsigned)(clusters * DR_CLUSTER)), dim3(DR_THREADS),
                     0, s, logits, c.n, c.n_experts, c.top_k, (int)c.gate,
                     static_cast<const __nv_bfloat16 *>(x), c.d, topk_idx, topk_gate, counts,
-                    offsets, perm, inv_perm, static_cast<uint16_t *>(act16), status);
+                    offsets, perm, inv_perm, static_cast<uint16_t *>(act16), po, status);
+}
+
+cudaError_t launch_classify(const moe_config &c, const int32_t *topk_idx, const int32_t *slot_of,
+                            int n_slots, int32_t *state, int32_t *miss_list, int32_t *counts,
+                            int *status, cudaStream_t s) {
+  classify_kernel<<<1, 256, 0, s>>>(topk_idx, c.n * c.top_k, c.n_experts, slot_of, n_slots, state,
+                                    miss_list, counts, status);
+  return cudaGetLastError();
 }
 
 }  // namespace moe

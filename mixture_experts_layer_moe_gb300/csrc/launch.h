@@ -120,18 +120,32 @@ size_t mx_act16_bytes(const moe_config &c);
 cudaError_t launch_rows_to_f16(const void *src, const int32_t *perm, int top_k, int P, int K,
                                void *dst, int *status, cudaStream_t s);
 // part 0 with act == nullptr: act16 already holds the f16 x rows in token order
-// (as launch_decode_route writes them), read through perm.
+// (as launch_decode_route writes them), read through perm.  With a pool, an
+// expert e with pool->slot_of[e] >= 0 is read from that slot of the pool.
 cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
                               const int32_t *perm, const int32_t *offsets, const moe_weights &w,
-                              void *h, void *y_perm, void *act16, int *status, cudaStream_t s);
+                              void *h, void *y_perm, void *act16, int *status, cudaStream_t s,
+                              const moe_expert_pool *pool = nullptr);
+cudaError_t launch_decode_ffn_pooled(const moe_config &c, int part, const void *act,
+                                     const int32_t *perm, const int32_t *offsets,
+                                     const moe_weights &w, void *h, void *y_perm, void *act16,
+                                     int *status, cudaStream_t s, const moe_expert_pool &pool);
 // Small-batch routing in one launch (decode_supported configurations with a
 // bf16 x): selection and gates from the logits, counts / offsets / perm /
 // inv_perm of the stable dispatch, and the f16 x rows in token order (act16,
 // as launch_decode_ffn part 0 reads them with act == nullptr).
 bool decode_route_supported(const moe_config &c);
+// With a pool, CTA 0 also classifies the selected experts against it (state,
+// miss_list, pool_counts as moe_classify_experts writes them; each nullable).
 cudaError_t launch_decode_route(const moe_config &c, const float *logits, const void *x,
                                 int32_t *topk_idx, float *topk_gate, int32_t *counts,
                                 int32_t *offsets, int32_t *perm, int32_t *inv_perm, void *act16,
-                                int *status, cudaStream_t s);
+                                int *status, cudaStream_t s,
+                                const moe_expert_pool *pool = nullptr, int32_t *state = nullptr,
+                                int32_t *miss_list = nullptr, int32_t *pool_counts = nullptr);
+// Hit/miss classification of topk_idx against slot_of (one CTA; E <= 256).
+cudaError_t launch_classify(const moe_config &c, const int32_t *topk_idx, const int32_t *slot_of,
+                            int n_slots, int32_t *state, int32_t *miss_list, int32_t *counts,
+                            int *status, cudaStream_t s);
 
 }  // namespace moe

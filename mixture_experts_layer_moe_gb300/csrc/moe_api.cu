@@ -53,8 +53,9 @@ moe_status check_expert_weights(const moe_config &c, const moe_weights *w) {
   if (swiglu != (w->W3 != nullptr)) return MOE_ERR_INVALID_ARG;
   if (swiglu && !ok_ptr(w->W3)) return MOE_ERR_INVALID_ARG;
   if (c.weight_dtype == MOE_MXFP4) {
-    if (w->S1 == nullptr || w->S2 == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!ok_ptr(w->S1) || !ok_ptr(w->S2)) return MOE_ERR_INVALID_ARG;
     if (swiglu != (w->S3 != nullptr)) return MOE_ERR_INVALID_ARG;
+    if (swiglu && !ok_ptr(w->S3)) return MOE_ERR_INVALID_ARG;
   } else if (w->S1 || w->S2 || w->S3) {
     return MOE_ERR_INVALID_ARG;
   }
@@ -231,6 +232,55 @@ moe_status run_expert_ffn(const moe_config &c, const void *x_perm, const int32_t
   dn.out = y_perm;
   stage(MOE_STAGE_FFN_DOWN, 1);
   return cuda_status(launch_gemm(dn, status, s));
+}
+
+// The small-batch forward: the router's linear layer, selection + dispatch +
+// f16 x rows in one launch (plus the hit/miss classification against the
+// pool, if any), the two FFN kernels streaming the selected experts (from
+// their pool slots where resident), combine.
+template <typename StageFn>
+moe_status run_small_batch(const moe_config &c, const void *x, const moe_weights *w,
+                           const moe_expert_pool *pool, void *y, int32_t *state,
+                           int32_t *miss_list, int32_t *pool_counts, void *ws, cudaStream_t s,
+                           StageFn &&stage) {
+  const Layout L = layout_of(c);
+  int *status = at<int>(ws, L.status);
+  int32_t *offsets = at<int32_t>(ws, L.offsets);
+  int32_t *perm = at<int32_t>(ws, L.perm);
+  int32_t *inv_perm = at<int32_t>(ws, L.inv_perm);
+  float *gates = at<float>(ws, L.topk_gate);
+  stage(MOE_STAGE_ROUTE, 1);
+  MOE_TRY(cuda_status(launch_route_logits(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits),
+                                          status, s)));
+  stage(MOE_STAGE_DISPATCH, 1);
+  MOE_TRY(cuda_status(launch_decode_route(c, at<float>(ws, L.logits), x,
+                                          at<int32_t>(ws, L.topk_idx), gates,
+                                          at<int32_t>(ws, L.counts), offsets, perm, inv_perm,
+                                          at<void>(ws, L.act16), status, s, pool, state, miss_list,
+                                          pool_counts)));
+  stage(MOE_STAGE_FFN_UP, 1);
+  MOE_TRY(cuda_status(launch_decode_ffn(c, 0, nullptr, perm, offsets, *w, at<void>(ws, L.h),
+                                        at<void>(ws, L.y_perm), at<void>(ws, L.act16), status, s,
+                                        pool)));
+  stage(MOE_STAGE_FFN_DOWN, 1);
+  MOE_TRY(cuda_status(launch_decode_ffn(c, 1, nullptr, perm, offsets, *w, at<void>(ws, L.h),
+                                        at<void>(ws, L.y_perm), at<void>(ws, L.act16), status, s,
+                                        pool)));
+  stage(MOE_STAGE_COMBINE, 1);
+  MOE_TRY(cuda_status(launch_combine(c.act_dtype, at<void>(ws, L.y_perm), inv_perm, gates, nullptr,
+                                     y, c.n, c.top_k, c.d, status, s)));
+  stage(MOE_STAGE_END, 0);
+  return MOE_OK;
+}
+
+moe_status check_pool(const moe_config &c, const moe_expert_pool *p) {
+  if (p == nullptr || !ok_ptr(p->slot_of) || p->n_slots < 1) return MOE_ERR_INVALID_ARG;
+  const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  if (!ok_ptr(p->W1) || !ok_ptr(p->W2) || !ok_ptr(p->S1) || !ok_ptr(p->S2))
+    return MOE_ERR_INVALID_ARG;
+  if (swiglu != (p->W3 != nullptr) || swiglu != (p->S3 != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (swiglu && (!ok_ptr(p->W3) || !ok_ptr(p->S3))) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
 }
 
 moe_status run_shared_expert(const moe_config &c, const void *x, const moe_weights *w, void *ws,
@@ -412,30 +462,8 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
   int32_t *inv_perm = at<int32_t>(ws, L.inv_perm);
   const bool decode = decode_supported(c);
   const bool mx_tc = mx_tc_path(c);
-  if (decode && decode_route_supported(c)) {
-    // small batch: the router's linear layer, then selection, dispatch and the
-    // f16 activation rows in one launch; the FFN streams the chosen experts
-    stage(MOE_STAGE_ROUTE, 1);
-    MOE_TRY(cuda_status(launch_route_logits(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits),
-                                            status, s)));
-    stage(MOE_STAGE_DISPATCH, 1);
-    MOE_TRY(cuda_status(launch_decode_route(c, at<float>(ws, L.logits), x, topk_idx, gates,
-                                            at<int32_t>(ws, L.counts), offsets, perm, inv_perm,
-                                            at<void>(ws, L.act16), status, s)));
-    stage(MOE_STAGE_FFN_UP, 1);
-    MOE_TRY(cuda_status(launch_decode_ffn(c, 0, nullptr, perm, offsets, *w, at<void>(ws, L.h),
-                                          at<void>(ws, L.y_perm), at<void>(ws, L.act16), status,
-                                          s)));
-    stage(MOE_STAGE_FFN_DOWN, 1);
-    MOE_TRY(cuda_status(launch_decode_ffn(c, 1, nullptr, perm, offsets, *w, at<void>(ws, L.h),
-                                          at<void>(ws, L.y_perm), at<void>(ws, L.act16), status,
-                                          s)));
-    stage(MOE_STAGE_COMBINE, 1);
-    MOE_TRY(cuda_status(launch_combine(c.act_dtype, at<void>(ws, L.y_perm), inv_perm, gates,
-                                       nullptr, y, c.n, c.top_k, c.d, status, s)));
-    stage(MOE_STAGE_END, 0);
-    return MOE_OK;
-  }
+  if (decode && decode_route_supported(c))
+    return run_small_batch(c, x, w, nullptr, y, nullptr, nullptr, nullptr, ws, s, stage);
   stage(MOE_STAGE_ROUTE, 2);
   MOE_TRY(cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits), topk_idx,
                                    gates, nullptr, status, s)));
@@ -477,6 +505,55 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
 moe_status moe_forward(const moe_config *cfg, const void *x, const moe_weights *w, void *y,
                        void *ws, size_t ws_bytes, void *stream) {
   return moe_forward_staged(cfg, x, w, y, ws, ws_bytes, stream, nullptr, nullptr);
+}
+
+moe_status moe_classify_experts(const moe_config *cfg, const int32_t *topk_idx,
+                                const int32_t *slot_of, int32_t n_slots, int32_t *state,
+                                int32_t *miss_list, int32_t *counts, void *ws, size_t ws_bytes,
+                                void *stream) {
+  MOE_TRY(check_config(cfg));
+  const moe_config &c = *cfg;
+  if (!ok_ptr(topk_idx) || !ok_ptr(slot_of) || n_slots < 1 || !ok_ptr(state) ||
+      !ok_ptr(miss_list) || !ok_ptr(counts))
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  const Layout L = layout_of(c);
+  return cuda_status(launch_classify(c, topk_idx, slot_of, n_slots, state, miss_list, counts,
+                                     at<int>(ws, L.status), as_stream(stream)));
+}
+
+moe_status moe_forward_pooled(const moe_config *cfg, const void *x, const moe_weights *w,
+                              const moe_expert_pool *pool, void *y, int32_t *state,
+                              int32_t *miss_list, int32_t *counts, void *ws, size_t ws_bytes,
+                              void *stream) {
+  return moe_forward_pooled_staged(cfg, x, w, pool, y, state, miss_list, counts, ws, ws_bytes,
+                                   stream, nullptr, nullptr);
+}
+
+moe_status moe_forward_pooled_staged(const moe_config *cfg, const void *x, const moe_weights *w,
+                                     const moe_expert_pool *pool, void *y, int32_t *state,
+                                     int32_t *miss_list, int32_t *counts, void *ws,
+                                     size_t ws_bytes, void *stream, moe_stage_hook hook,
+                                     void *user) {
+  MOE_TRY(check_config(cfg));
+  const moe_config &c = *cfg;
+  if (!decode_route_supported(c)) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(check_router_weights(c, w));
+  MOE_TRY(check_expert_weights(c, w));
+  MOE_TRY(check_pool(c, pool));
+  if (!ok_ptr(x) || !ok_ptr(y)) return MOE_ERR_INVALID_ARG;
+  if ((state && !ok_ptr(state)) || (miss_list && !ok_ptr(miss_list)) || (counts && !ok_ptr(counts)))
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_ws(c, ws, ws_bytes));
+  const Layout L = layout_of(c);
+  cudaStream_t s = as_stream(stream);
+  MOE_TRY(cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, 2 * sizeof(int), s)));
+  int launched = 0;
+  auto stage = [&](int id, int kernels) {
+    if (hook) hook(id, launched, user);
+    launched += kernels;
+  };
+  return run_small_batch(c, x, w, pool, y, state, miss_list, counts, ws, s, stage);
 }
 
 moe_status moe_status_check(const void *ws, void *stream, int32_t *detail) {

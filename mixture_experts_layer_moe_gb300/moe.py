@@ -41,6 +41,16 @@ class moe_weights(ctypes.Structure):
                 ("Wg", "router_bias", "W1", "W3", "W2", "S1", "S3", "S2", "Ws1", "Ws3", "Ws2")]
 
 
+class moe_expert_pool(ctypes.Structure):
+    _fields_ = [("slot_of", ctypes.c_void_p), ("n_slots", ctypes.c_int32),
+                ("W1", ctypes.c_void_p), ("W3", ctypes.c_void_p), ("W2", ctypes.c_void_p),
+                ("S1", ctypes.c_void_p), ("S3", ctypes.c_void_p), ("S2", ctypes.c_void_p)]
+
+
+# indices of the classification counts (MOE_POOL_*)
+POOL_SELECTED, POOL_RESIDENT, POOL_LOOKUPS, POOL_SERVED = 0, 1, 2, 3
+
+
 class moe_workspace_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("status", "logits", "topk_idx", "topk_gate", "counts", "offsets", "perm",
@@ -55,6 +65,7 @@ def _load() -> ctypes.CDLL:
     P, I32, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     cfgp = ctypes.POINTER(moe_config)
     wp = ctypes.POINTER(moe_weights)
+    pp = ctypes.POINTER(moe_expert_pool)
     sig = {
         "moe_workspace_size": [cfgp, ctypes.POINTER(SZ)],
         "moe_workspace_layout_of": [cfgp, ctypes.POINTER(moe_workspace_layout)],
@@ -66,6 +77,9 @@ def _load() -> ctypes.CDLL:
         "moe_combine": [cfgp, P, P, P, P, P, P, SZ, P],
         "moe_forward": [cfgp, P, wp, P, P, SZ, P],
         "moe_forward_staged": [cfgp, P, wp, P, P, SZ, P, STAGE_HOOK, P],
+        "moe_classify_experts": [cfgp, P, P, ctypes.c_int32, P, P, P, P, SZ, P],
+        "moe_forward_pooled": [cfgp, P, wp, pp, P, P, P, P, P, SZ, P],
+        "moe_forward_pooled_staged": [cfgp, P, wp, pp, P, P, P, P, P, SZ, P, STAGE_HOOK, P],
         "moe_status_check": [P, P, ctypes.POINTER(ctypes.c_int32)],
         "moe_status_clear": [P, P],
     }
@@ -117,6 +131,14 @@ def make_weights(inputs: dict) -> moe_weights:
         _ptr(g("W2q") if mx else g("W2")),
         _ptr(g("S1")), _ptr(g("S3")), _ptr(g("S2")),
         _ptr(g("Ws1")), _ptr(g("Ws3")), _ptr(g("Ws2")))
+
+
+def make_pool(slot_of: torch.Tensor, pool: dict) -> moe_expert_pool:
+    """moe_expert_pool from the device slot table and a dict of device pool
+    tensors (keys as in moe_synth.make_pool: W1q, W3q, W2q, S1, S3, S2)."""
+    g = pool.get
+    return moe_expert_pool(_ptr(slot_of), int(g("W1q").shape[0]), _ptr(g("W1q")), _ptr(g("W3q")),
+                           _ptr(g("W2q")), _ptr(g("S1")), _ptr(g("S3")), _ptr(g("S2")))
 
 
 def _stream(stream) -> Optional[int]:
@@ -203,6 +225,33 @@ def moe_forward_staged(cfg, x, w: moe_weights, y, ws, hook, stream=None):
     cb = STAGE_HOOK(lambda st, k, _u: hook(st, k))
     _check(_lib.moe_forward_staged(ctypes.byref(c), _ptr(x), ctypes.byref(w), _ptr(y), _ptr(ws),
                                    ws.numel(), _stream(stream), cb, None), "moe_forward_staged")
+
+
+def moe_classify_experts(cfg, topk_idx, slot_of, n_slots, state, miss_list, counts, ws,
+                         stream=None):
+    c = make_config(cfg)
+    _check(_lib.moe_classify_experts(ctypes.byref(c), _ptr(topk_idx), _ptr(slot_of), int(n_slots),
+                                     _ptr(state), _ptr(miss_list), _ptr(counts), _ptr(ws),
+                                     ws.numel(), _stream(stream)), "moe_classify_experts")
+
+
+def moe_forward_pooled(cfg, x, w: moe_weights, pool: moe_expert_pool, y, state, miss_list, counts,
+                       ws, stream=None):
+    c = make_config(cfg)
+    _check(_lib.moe_forward_pooled(ctypes.byref(c), _ptr(x), ctypes.byref(w), ctypes.byref(pool),
+                                   _ptr(y), _ptr(state), _ptr(miss_list), _ptr(counts), _ptr(ws),
+                                   ws.numel(), _stream(stream)), "moe_forward_pooled")
+
+
+def moe_forward_pooled_staged(cfg, x, w: moe_weights, pool: moe_expert_pool, y, state, miss_list,
+                              counts, ws, hook, stream=None):
+    """hook(stage: int, kernels_so_far: int) runs on this thread before each stage is enqueued."""
+    c = make_config(cfg)
+    cb = STAGE_HOOK(lambda st, k, _u: hook(st, k))
+    _check(_lib.moe_forward_pooled_staged(ctypes.byref(c), _ptr(x), ctypes.byref(w),
+                                          ctypes.byref(pool), _ptr(y), _ptr(state),
+                                          _ptr(miss_list), _ptr(counts), _ptr(ws), ws.numel(),
+                                          _stream(stream), cb, None), "moe_forward_pooled_staged")
 
 
 def moe_status_check(ws, stream=None) -> tuple[int, int]:

@@ -137,3 +137,33 @@ def test_status_strings(lib):
         s = lib.status_string(code)
         assert s.startswith("MOE_")
     assert "unknown" in lib.status_string(42)
+
+
+def test_pool_entry_point_argument_checks(lib):
+    """moe_forward_pooled / moe_classify_experts reject bad arguments before any launch."""
+    c = _c(lib, n=4, weight_dtype="mxfp4")
+    _, n = _size(lib, c)
+    w = lib.moe_weights(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None)
+    pool = lib.moe_expert_pool(FAKE, 3, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
+    fwd = lambda cfg, p, ws=FAKE, nb=n: lib.raw_call(
+        "moe_forward_pooled", ctypes.byref(cfg), FAKE, ctypes.byref(w),
+        None if p is None else ctypes.byref(p), FAKE, None, None, None, ws, nb, None)
+    assert fwd(c, None) == 1                                       # no pool
+    assert fwd(c, lib.moe_expert_pool(FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)) == 1
+    assert fwd(c, lib.moe_expert_pool(None, 3, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)) == 1
+    assert fwd(c, lib.moe_expert_pool(FAKE, 3, FAKE, None, FAKE, FAKE, FAKE, FAKE)) == 1  # no W3
+    assert fwd(c, lib.moe_expert_pool(FAKE, 3, FAKE, FAKE, FAKE, FAKE + 4, FAKE, FAKE)) == 1
+    assert fwd(c, pool, nb=n - 1) == 3                             # workspace too small
+    bf16 = _c(lib, n=4)
+    wb = lib.moe_weights(FAKE, None, FAKE, FAKE, FAKE, None, None, None, None, None, None)
+    assert lib.raw_call("moe_forward_pooled", ctypes.byref(bf16), FAKE, ctypes.byref(wb),
+                        ctypes.byref(pool), FAKE, None, None, None, FAKE, n, None) == 2
+    big = _c(lib, n=200, weight_dtype="mxfp4")                     # n*K above the small-batch limit
+    _, nbig = _size(lib, big)
+    assert lib.raw_call("moe_forward_pooled", ctypes.byref(big), FAKE, ctypes.byref(w),
+                        ctypes.byref(pool), FAKE, None, None, None, FAKE, nbig, None) == 2
+    cls = lambda slot, ns, st=FAKE: lib.raw_call("moe_classify_experts", ctypes.byref(c), FAKE,
+                                                 slot, ns, st, FAKE, FAKE, FAKE, n, None)
+    assert cls(None, 3) == 1
+    assert cls(FAKE, 0) == 1
+    assert cls(FAKE, 3, st=None) == 1
