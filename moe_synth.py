@@ -13,6 +13,7 @@ expert is a copy of the FFN d -> d_ff -> d):
 * ``mixtral_bf16``           top-2 renormalised, SwiGLU, bf16, n=4096 d=4096 F=14336 E=8
 * ``gptoss_decode_mxfp4``    top-4, SwiGLU, MXFP4 experts, n in {1,4,16,64}, d=F=2880, E=128
 * ``gptoss_prefill_zipf_mxfp4``  as above, n=8192, router bias giving Zipf(1.2) loads
+* ``gptoss_decode_nvfp4``    the decode workload with NVFP4 experts (blocks of 16)
 * ``finegrained_shared_bf16``    top-8 of 256, SwiGLU F=2048, d=7168, one shared expert, n=16384
 
 Storage conventions (all row-major, weights stored out x in so the reduction
@@ -25,6 +26,9 @@ dimension is contiguous):
 * MXFP4 experts: ``W1q``/``W3q`` [E, F, d/2] uint8, element i of a row in byte i//2,
   low nibble when i is even; ``S1``/``S3`` [E, F, d/32] uint8 E8M0 block scales
   (one per 32 consecutive elements along d); ``W2q`` [E, d, F/2], ``S2`` [E, d, F/32].
+* NVFP4 experts: codes as MXFP4; ``S1``/``S3`` [E, F, d/16], ``S2`` [E, d, F/16] uint8
+  FP8 E4M3 block scales (one per 16 consecutive elements); ``G1``/``G3``/``G2`` [E] fp32,
+  one scale per expert matrix.
 * shared expert (bf16): ``Ws1``, ``Ws3`` [Fs, d]; ``Ws2`` [d, Fs].
 
 Draw order for a seed: x, Wg, [expert ordering for the bias], then per expert
@@ -51,7 +55,7 @@ class MoEConfig:
     E: int
     k: int
     act_dtype: str          # "f32" | "bf16"
-    weight_dtype: str       # "f32" | "bf16" | "mxfp4"
+    weight_dtype: str       # "f32" | "bf16" | "mxfp4" | "nvfp4"
     gate: str               # "top_prob" (Switch: g = p of the chosen expert) | "renorm"
     act: str                # "relu" | "swiglu"
     router_bias: str = "none"   # "none" | "zipf"
@@ -83,6 +87,9 @@ CONFIGS = {
         "gptoss_prefill_zipf_mxfp4", n=8192, d=2880, d_ff=2880, E=128, k=4,
         act_dtype="bf16", weight_dtype="mxfp4", gate="renorm", act="swiglu",
         router_bias="zipf"),
+    "gptoss_decode_nvfp4": MoEConfig(
+        "gptoss_decode_nvfp4", n=1, d=2880, d_ff=2880, E=128, k=4,
+        act_dtype="bf16", weight_dtype="nvfp4", gate="renorm", act="swiglu"),
     "finegrained_shared_bf16": MoEConfig(
         "finegrained_shared_bf16", n=16384, d=7168, d_ff=2048, E=256, k=8,
         act_dtype="bf16", weight_dtype="bf16", gate="renorm", act="swiglu",
@@ -114,6 +121,17 @@ def _mxfp4_matrix(rows, cols, g, device):
     scales = torch.randint(119, 124, (rows, cols // 32), generator=g, device=device,
                            dtype=torch.uint8)
     return _pack_nibbles(codes), scales
+
+
+def _nvfp4_matrix(rows, cols, g, device):
+    """Uniform E2M1 codes (all 16); E4M3 block scales with exponent field
+    uniform over 4..10 (2^-3 .. 2^3) and uniform mantissa; one fp32 matrix
+    scale uniform over [2^-8, 2^-7)."""
+    codes = torch.randint(0, 16, (rows, cols), generator=g, device=device, dtype=torch.uint8)
+    ex = torch.randint(4, 11, (rows, cols // 16), generator=g, device=device, dtype=torch.uint8)
+    man = torch.randint(0, 8, (rows, cols // 16), generator=g, device=device, dtype=torch.uint8)
+    gs = (1.0 + torch.rand((), generator=g, device=device, dtype=torch.float32)) / 256.0
+    return _pack_nibbles(codes), (ex << 3) | man, gs
 
 
 def zipf_router_bias(cfg: MoEConfig, order: torch.Tensor) -> torch.Tensor:
@@ -163,6 +181,24 @@ def make_inputs(cfg: MoEConfig, seed: int = 0, device="cpu") -> dict:
             W2q[e], S2[e] = _mxfp4_matrix(d, F, g, device)
         out.update(W1q=W1q, S1=S1, W3q=W3q, S3=S3, W2q=W2q, S2=S2,
                    W1=None, W3=None, W2=None)
+    elif cfg.weight_dtype == "nvfp4":
+        assert d % 32 == 0 and F % 32 == 0
+        W1q = torch.empty((E, F, d // 2), dtype=torch.uint8, device=device)
+        S1 = torch.empty((E, F, d // 16), dtype=torch.uint8, device=device)
+        W3q = torch.empty_like(W1q) if swiglu else None
+        S3 = torch.empty_like(S1) if swiglu else None
+        W2q = torch.empty((E, d, F // 2), dtype=torch.uint8, device=device)
+        S2 = torch.empty((E, d, F // 16), dtype=torch.uint8, device=device)
+        G1 = torch.empty(E, dtype=torch.float32, device=device)
+        G3 = torch.empty(E, dtype=torch.float32, device=device) if swiglu else None
+        G2 = torch.empty(E, dtype=torch.float32, device=device)
+        for e in range(E):
+            W1q[e], S1[e], G1[e] = _nvfp4_matrix(F, d, g, device)
+            if swiglu:
+                W3q[e], S3[e], G3[e] = _nvfp4_matrix(F, d, g, device)
+            W2q[e], S2[e], G2[e] = _nvfp4_matrix(d, F, g, device)
+        out.update(W1q=W1q, S1=S1, W3q=W3q, S3=S3, W2q=W2q, S2=S2, G1=G1, G3=G3, G2=G2,
+                   W1=None, W3=None, W2=None)
     else:
         wdt = _TORCH_DTYPE[cfg.weight_dtype]
         W1 = torch.empty((E, F, d), dtype=wdt, device=device)
@@ -196,6 +232,8 @@ def weight_bytes_per_expert(cfg: MoEConfig) -> int:
     elems = cfg.d * cfg.d_ff
     if cfg.weight_dtype == "mxfp4":
         return mats * (elems // 2 + elems // 32)
+    if cfg.weight_dtype == "nvfp4":
+        return mats * (elems // 2 + elems // 16 + 4)
     return mats * elems * (4 if cfg.weight_dtype == "f32" else 2)
 
 

@@ -30,6 +30,9 @@ states.  Sources (page titles and sections):
 * [Feed] minseoc03.com feed, post "What is MXFP4?": 4-bit floats in blocks of
   32 values sharing one scale.  The bit-level element (E2M1) and scale (E8M0)
   definitions are those of the OCP Microscaling Formats specification v1.0.
+  The same post names NVFP4 (blocks of 16); its scale byte is FP8 E4M3 as the
+  OCP 8-bit floating point specification defines it, with one fp32 scale per
+  matrix (the reading taken where the post gives only the block size).
 
 Readings where the pages leave a step open (listed again in the design doc):
 selection ties go to the lower expert index; the Switch (top-1) gate is the
@@ -109,6 +112,43 @@ def mxfp4_decode(packed: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
     scale = e8m0_value(scales)
     assert scale.shape[-1] * 32 == K
     return (vals.reshape(*vals.shape[:-1], K // 32, 32) * scale.unsqueeze(-1)).reshape(vals.shape)
+
+
+def e4m3_value(s: torch.Tensor) -> torch.Tensor:
+    """FP8 E4M3 (OCP 8-bit Floating Point Specification, the "FN" variant):
+    1 sign, 4 exponent (bias 7), 3 mantissa bits.  Exponent field 0 is
+    subnormal: (-1)^s * 2^-6 * (m/8); otherwise (-1)^s * 2^(e-7) * (1 + m/8).
+    Exponent 15 with mantissa 7 (0x7F, 0xFF) is NaN; there are no infinities.
+    """
+    c = s.to(torch.int64)
+    sign = (c >> 7) & 1
+    e = (c >> 3) & 15
+    m = (c & 7).to(F64)
+    sub = torch.pow(2.0, torch.full_like(m, -6.0)) * (m / 8.0)
+    nrm = torch.pow(2.0, (e - 7).to(F64)) * (1.0 + m / 8.0)
+    mag = torch.where(e == 0, sub, nrm)
+    v = torch.where(sign == 1, -mag, mag)
+    return torch.where((e == 15) & ((c & 7) == 7), torch.full_like(v, math.nan), v)
+
+
+def nvfp4_decode(packed: torch.Tensor, scales: torch.Tensor, gscale: float) -> torch.Tensor:
+    """Rows of NVFP4 data -> float64 [..., K].
+
+    Feed post "What is MXFP4?": the NVFP4 variant gives each block of 16
+    values its own scale.  Elements are E2M1 packed as in ``mxfp4_decode``;
+    scales [..., K/16] uint8 hold one FP8 E4M3 scale per block of 16
+    consecutive elements, and the whole matrix carries one fp32 scale gscale:
+    value = e2m1(code) * e4m3(block scale) * gscale.
+    """
+    lo = packed & 0x0F
+    hi = packed >> 4
+    codes = torch.stack((lo, hi), dim=-1).reshape(*packed.shape[:-1], packed.shape[-1] * 2)
+    vals = e2m1_value(torch.arange(16, dtype=torch.uint8))[codes.to(torch.int64)]
+    K = vals.shape[-1]
+    scale = e4m3_value(scales)
+    assert scale.shape[-1] * 16 == K
+    out = vals.reshape(*vals.shape[:-1], K // 16, 16) * scale.unsqueeze(-1)
+    return out.reshape(vals.shape) * float(gscale)
 
 
 # ---------------------------------------------------------------------------
@@ -243,6 +283,12 @@ def expert_weights(inputs: dict, cfg, e: int):
         W1 = mxfp4_decode(inputs["W1q"][e], inputs["S1"][e])
         W3 = mxfp4_decode(inputs["W3q"][e], inputs["S3"][e]) if cfg.act == "swiglu" else None
         W2 = mxfp4_decode(inputs["W2q"][e], inputs["S2"][e])
+    elif cfg.weight_dtype == "nvfp4":
+        g = lambda key: float(inputs[key][e])
+        W1 = nvfp4_decode(inputs["W1q"][e], inputs["S1"][e], g("G1"))
+        W3 = (nvfp4_decode(inputs["W3q"][e], inputs["S3"][e], g("G3"))
+              if cfg.act == "swiglu" else None)
+        W2 = nvfp4_decode(inputs["W2q"][e], inputs["S2"][e], g("G2"))
     else:
         W1 = to_f64(inputs["W1"][e])
         W3 = to_f64(inputs["W3"][e]) if cfg.act == "swiglu" else None

@@ -429,6 +429,75 @@ def test_mxfp4_expert_bruteforce():
         assert np.allclose(res["y"][t].numpy(), W2 @ h, rtol=1e-12, atol=1e-12)
 
 
+# ---------------------------------------------------------------- NVFP4 pins
+
+def check_e4m3(golden_dir):
+    g = _load(golden_dir, "e4m3_values.json")
+    for code, want in g["examples"].items():
+        v = O.e4m3_value(torch.tensor([int(code)], dtype=torch.uint8)).item()
+        if want == "NaN":
+            assert math.isnan(v), code
+        else:
+            assert v == want and math.copysign(1, v) == math.copysign(1, want), code
+
+
+def test_e4m3_examples(golden_dir):
+    check_e4m3(golden_dir)
+
+
+def test_e4m3_matches_library_type():
+    """All 256 bytes against torch's float8_e4m3fn (the same OCP encoding)."""
+    codes = torch.arange(256, dtype=torch.uint8)
+    ours = O.e4m3_value(codes)
+    lib = codes.view(torch.float8_e4m3fn).to(torch.float64)
+    assert torch.equal(torch.isnan(ours), torch.isnan(lib))
+    ok = ~torch.isnan(ours)
+    assert torch.equal(ours[ok], lib[ok])
+
+
+def check_nvfp4_bruteforce():
+    """NVFP4 expert weights decoded element by element (block = element // 16), tiny layer."""
+    cfg = _cfg(n=3, d=64, d_ff=32, E=2, k=1, act_dtype="bf16", weight_dtype="nvfp4")
+    inp = moe_synth.make_inputs(cfg, seed=6)
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    e4m3 = lambda b: float(torch.tensor([b], dtype=torch.uint8).view(torch.float8_e4m3fn)
+                           .to(torch.float64))
+
+    def dec(packed, scales, gs, rows, cols):
+        out = np.zeros((rows, cols))
+        for r in range(rows):
+            for c in range(cols):
+                byte = int(packed[r, c // 2])
+                code = (byte & 15) if c % 2 == 0 else (byte >> 4)
+                v = table[code & 7] * (-1 if code & 8 else 1)
+                out[r, c] = v * e4m3(int(scales[r, c // 16])) * float(gs)
+        return out
+
+    res = O.forward(cfg, inp)
+    X = _np_bf16(inp["x"])
+    for t in range(cfg.n):
+        e = int(res["routing"]["topk_idx"][t, 0])
+        W1 = dec(inp["W1q"][e], inp["S1"][e], inp["G1"][e], cfg.d_ff, cfg.d)
+        W3 = dec(inp["W3q"][e], inp["S3"][e], inp["G3"][e], cfg.d_ff, cfg.d)
+        W2 = dec(inp["W2q"][e], inp["S2"][e], inp["G2"][e], cfg.d, cfg.d_ff)
+        A = W1 @ X[t]
+        h = A / (1 + np.exp(-A)) * (W3 @ X[t])
+        assert np.allclose(res["y"][t].numpy(), W2 @ h, rtol=1e-12, atol=1e-12)
+
+
+def test_nvfp4_expert_bruteforce():
+    check_nvfp4_bruteforce()
+
+
+def test_nvfp4_unit_scales_equal_mxfp4():
+    """Block scales of 1.0 (E4M3 0x38, E8M0 127) and a matrix scale of 1: both
+    formats decode the same codes to the same values."""
+    packed = torch.randint(0, 256, (5, 32), dtype=torch.uint8, generator=torch.Generator().manual_seed(1))
+    nv = O.nvfp4_decode(packed, torch.full((5, 4), 0x38, dtype=torch.uint8), 1.0)
+    mx = O.mxfp4_decode(packed, torch.full((5, 2), 127, dtype=torch.uint8))
+    assert torch.equal(nv, mx)
+
+
 # ------------------------------------------------- expert-slot classification
 
 def check_expert_cache_example(golden_dir):
@@ -558,6 +627,16 @@ def _bad_stats(probs, top1, alpha):             # P_i averaged over experts, not
     return dict(P=P, f=f, aux=alpha * E * float((f * P).sum()))
 
 
+def _bad_nvfp4(packed, scales, gscale):          # one scale per 32 elements, not 16
+    lo = packed & 0x0F
+    hi = packed >> 4
+    codes = torch.stack((lo, hi), dim=-1).reshape(*packed.shape[:-1], packed.shape[-1] * 2)
+    vals = O.e2m1_value(codes)
+    K = vals.shape[-1]
+    sc = O.e4m3_value(scales[..., 0::2])
+    return (vals.reshape(*vals.shape[:-1], K // 32, 32) * sc.unsqueeze(-1)).reshape(vals.shape) * gscale
+
+
 def _bad_classify(idx, E, slot_of):              # counts distinct experts as lookups served
     r = _orig_classify(idx, E, slot_of)
     return dict(r, served=r["resident"])
@@ -584,6 +663,7 @@ MUTANTS = [
     ("dispatch_arrays", _bad_dispatch, check_dispatch_example),
     ("softmax_rows", _bad_softmax, check_softmax_example),
     ("routing_statistics", _bad_stats, check_aux_loss_example),
+    ("nvfp4_decode", _bad_nvfp4, lambda gd: check_nvfp4_bruteforce()),
     ("classify_experts", _bad_classify, check_expert_cache_example),
     ("classify_experts", _bad_classify_slot0, lambda gd: check_classify_bruteforce()),
 ]
