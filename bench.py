@@ -171,7 +171,7 @@ DECODE_BATCHES = 8       # token batches rotated through in decode timing
 
 
 def is_decode(cfg) -> bool:
-    return cfg.weight_dtype == "mxfp4" and cfg.n * cfg.k <= DECODE_MAX_PAIRS
+    return cfg.weight_dtype in ("mxfp4", "nvfp4") and cfg.n * cfg.k <= DECODE_MAX_PAIRS
 
 
 def dominant_kernel(cfg, active_experts=None):
@@ -179,15 +179,18 @@ def dominant_kernel(cfg, active_experts=None):
 
     Tensor-bound workloads: the up-projection grouped GEMM (W1 and W3, 2/3 of the
     expert FLOPs with SwiGLU), FLOPs = 2 * (n*k) * d * d_ff * (2 for SwiGLU, else 1).
-    Small-batch MXFP4 (decode): the up-projection kernel streams the selected
+    Small-batch FP4 (decode): the up-projection kernel streams the selected
     experts' W1/W3 codes and scales once, reads the tokens' x rows and writes h:
-    bytes = u * mats * d_ff * (d/2 + d/32) + n*k*d*2 + n*k*d_ff*2.
+    bytes = u * mats * d_ff * (d/2 + d/32) + n*k*d*2 + n*k*d_ff*2 (MXFP4; NVFP4
+    has d/16 scale bytes per row and one fp32 scale per matrix).
     """
     mats = 2 if cfg.act == "swiglu" else 1
     if is_decode(cfg):
         u = active_experts if active_experts is not None else min(cfg.E, cfg.n * cfg.k)
         P = cfg.n * cfg.k
-        nbytes = (u * mats * cfg.d_ff * (cfg.d // 2 + cfg.d // 32)
+        scale_bytes = cfg.d // 16 if cfg.weight_dtype == "nvfp4" else cfg.d // 32
+        extra = 4 if cfg.weight_dtype == "nvfp4" else 0
+        nbytes = (u * mats * (cfg.d_ff * (cfg.d // 2 + scale_bytes) + extra)
                   + P * cfg.d * 2 + P * cfg.d_ff * 2)
         return "ffn_up", "hbm", nbytes, "GB/s"
     flops = 2 * cfg.n * cfg.k * cfg.d * cfg.d_ff * mats
@@ -228,6 +231,7 @@ def time_oracle_step(scfg, sub):
 
 def default_cpu_sample(cfg):
     return {"tiny_switch_fp32": 256, "mixtral_bf16": 4096, "gptoss_decode_mxfp4": cfg.n,
+            "gptoss_decode_nvfp4": cfg.n,
             "gptoss_prefill_zipf_mxfp4": 256, "finegrained_shared_bf16": 64}.get(cfg.name, 64)
 
 

@@ -64,7 +64,12 @@ typedef enum {
                                tensor-core path applies exactly (E8M0 byte 113..142) */
 } moe_status;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_MXFP4 = 2 } moe_dtype;
+/* NVFP4: the feed post "What is MXFP4?" names it as the block-of-16 variant
+ * (blocks of 16 with their own scale); the scale byte is FP8 E4M3 (OCP 8-bit
+ * floating point specification) and each expert matrix carries one fp32
+ * scale.  Expert weights only, small batches only (n * top_k <= 256, bf16
+ * activations): other NVFP4 configurations return MOE_ERR_UNSUPPORTED. */
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_MXFP4 = 2, MOE_NVFP4 = 3 } moe_dtype;
 
 /* Gate rule. TOP_PROB: g = p of the chosen expert, unrenormalised (Switch
  * top-1; "Routing", output x 0.45).  RENORM: g_j = p_j / sum of the chosen p
@@ -84,7 +89,8 @@ typedef struct {
   int32_t n_experts;    /* E, 1..256 */
   int32_t top_k;        /* K, 1..E */
   int32_t act_dtype;    /* MOE_F32 or MOE_BF16: x, Wg, y, shared-expert weights */
-  int32_t weight_dtype; /* routed expert weights: MOE_F32 (needs act F32), MOE_BF16, MOE_MXFP4 */
+  int32_t weight_dtype; /* routed expert weights: MOE_F32 (needs act F32), MOE_BF16, MOE_MXFP4,
+                           MOE_NVFP4 */
   int32_t gate;         /* moe_gate */
   int32_t act;          /* moe_act */
   int32_t d_ff_shared;  /* 0: none; else one always-on SwiGLU expert added unweighted */
@@ -94,19 +100,25 @@ typedef struct {
 typedef struct {
   const void *Wg;            /* [E][d], act_dtype */
   const float *router_bias;  /* [E] fp32 added to the router logits, or NULL */
-  const void *W1;            /* [E][d_ff][d] (f32/bf16) or MXFP4 codes [E][d_ff][d/2] */
+  const void *W1;            /* [E][d_ff][d] (f32/bf16) or FP4 codes [E][d_ff][d/2] */
   const void *W3;            /* as W1; SwiGLU only, else NULL */
-  const void *W2;            /* [E][d][d_ff] (f32/bf16) or MXFP4 codes [E][d][d_ff/2] */
-  const uint8_t *S1;         /* MXFP4 E8M0 scales [E][d_ff][d/32], else NULL */
-  const uint8_t *S3;         /* MXFP4 scales of W3 [E][d_ff][d/32], else NULL */
-  const uint8_t *S2;         /* MXFP4 scales of W2 [E][d][d_ff/32], else NULL */
+  const void *W2;            /* [E][d][d_ff] (f32/bf16) or FP4 codes [E][d][d_ff/2] */
+  const uint8_t *S1;         /* block scales of W1: MXFP4 E8M0 [E][d_ff][d/32], NVFP4 E4M3
+                                [E][d_ff][d/16]; else NULL */
+  const uint8_t *S3;         /* block scales of W3, as S1; else NULL */
+  const uint8_t *S2;         /* block scales of W2: [E][d][d_ff/32] or [E][d][d_ff/16] */
   const void *Ws1;           /* shared expert [d_ff_shared][d], act_dtype, or NULL */
   const void *Ws3;           /* shared expert [d_ff_shared][d] */
   const void *Ws2;           /* shared expert [d][d_ff_shared] */
+  const float *G1;           /* NVFP4: fp32 scale of each expert's W1 [E], else NULL */
+  const float *G3;           /* NVFP4: of W3 [E] (SwiGLU), else NULL */
+  const float *G2;           /* NVFP4: of W2 [E], else NULL */
 } moe_weights;
 /* MXFP4 codes: element i of a row sits in byte i/2, low nibble when i is even.
  * Scale byte s gives the 32 consecutive elements of its block 2^(s-127);
- * s = 255 (NaN) is not accepted and decodes to NaN. */
+ * s = 255 (NaN) is not accepted and decodes to NaN.  NVFP4 codes are packed the
+ * same way; element i of row r of expert e is e2m1(code) * e4m3(S[e][r][i/16])
+ * * G[e]. */
 
 /* Offsets (bytes from the workspace start) of the intermediates that
  * moe_forward leaves in the workspace, for inspection after a call. */

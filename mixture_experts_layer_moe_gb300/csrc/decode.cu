@@ -36,12 +36,14 @@ __global__ void rows_to_f16_kernel(const __nv_bfloat16 *__restrict__ src,
 }  // namespace
 
 bool decode_supported(const moe_config &c) {
-  return c.weight_dtype == MOE_MXFP4 && c.act_dtype == MOE_BF16 && c.d % 32 == 0 &&
+  return (c.weight_dtype == MOE_MXFP4 || c.weight_dtype == MOE_NVFP4) &&
+         c.act_dtype == MOE_BF16 && c.d % 32 == 0 &&
          c.d_ff % 32 == 0 && (int64_t)c.n * c.top_k <= kDecodeMaxPairs;
 }
 
 size_t mx_act16_bytes(const moe_config &c) {
-  if (c.weight_dtype != MOE_MXFP4 || c.act_dtype != MOE_BF16) return 0;
+  if ((c.weight_dtype != MOE_MXFP4 && c.weight_dtype != MOE_NVFP4) || c.act_dtype != MOE_BF16)
+    return 0;
   const size_t P = (size_t)c.n * c.top_k;
   return P * (size_t)c.d * 2 + P * (size_t)c.d_ff * 2;
 }
@@ -61,10 +63,14 @@ cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
                               const int32_t *perm, const int32_t *offsets, const moe_weights &w,
                               void *h, void *y_perm, void *act16, int *status, cudaStream_t s,
                               const moe_expert_pool *pool) {
+  if (c.weight_dtype == MOE_NVFP4)
+    return pool ? cudaErrorNotSupported
+                : launch_decode_ffn_nvfp4(c, part, act, perm, offsets, w, h, y_perm, act16, status,
+                                          s);
   if (pool) return launch_decode_ffn_pooled(c, part, act, perm, offsets, w, h, y_perm, act16,
                                             status, s, *pool);
-  return run_decode_ffn<false>(c, part, act, perm, offsets, w, h, y_perm, act16, status, s,
-                               nullptr);
+  return run_decode_ffn<false, 0>(c, part, act, perm, offsets, w, h, y_perm, act16, status, s,
+                                  nullptr);
 }
 
 }  // namespace moe

@@ -49,6 +49,7 @@ struct DecodeArgs {
   const int32_t *slot_of;         // [E] pool slot of each expert or -1; nullptr: no pool
   int n_slots;
   const uint8_t *PS, *PS3;        // pool scales [n_slots][R][K/32]
+  const float *G, *G3;            // NVFP4: per-expert fp32 scales of the two matrices
   int R, K;
   __nv_bfloat16 *out;             // [P][R]
   uint16_t *out16;                // f16 copy of out (the next projection's input), or nullptr
@@ -105,6 +106,39 @@ __device__ __forceinline__ void mx_block(float (&acc)[4], uint32_t wg, uint32_t 
   acc[3] = fmaf(sh, p[3], acc[3]);
 }
 
+// NVFP4 (blocks of 16): the two 16-bit halves of w, each two E4M3 bytes, ->
+// two f16x2 (low byte to the low half).  E4M3 values are exact in f16.
+__device__ __forceinline__ uint2 e4m3x4_to_f16x2x2(uint32_t w) {
+  uint2 d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(d.x), "=r"(d.y)
+      : "r"(w));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// One 16-byte chunk (two NVFP4 blocks) of rows g and g+8 against 8 tokens.
+// Lane (g, t) holds word t of each row, which lies in block t / 2, so one
+// scale per row covers all of the lane's elements: sgh = {s_g, s_g+8} as
+// f16x2.  E2M1 x E4M3 has at most 5 significant bits and lies within
+// 2^-10 .. 2688, so the scaled codes are exact in f16 and both MMAs
+// accumulate straight into the fp32 accumulator.
+__device__ __forceinline__ void nv_block(float (&acc)[4], uint32_t wg, uint32_t wh, uint32_t sgh,
+                                         const uint4 &b) {
+  const F16x2x4 ag = e2m1x8_to_f16x2x4(wg), ah = e2m1x8_to_f16x2x4(wh);
+  const uint32_t sg = __byte_perm(sgh, sgh, 0x1010), sh = __byte_perm(sgh, sgh, 0x3232);
+  mma_16816(acc, hmul2_bits(ag.v[0], sg), hmul2_bits(ah.v[0], sh), hmul2_bits(ag.v[1], sg),
+            hmul2_bits(ah.v[1], sh), b.x, b.y);
+  mma_16816(acc, hmul2_bits(ag.v[2], sg), hmul2_bits(ah.v[2], sh), hmul2_bits(ag.v[3], sg),
+            hmul2_bits(ah.v[3], sh), b.z, b.w);
+}
+
 __device__ __forceinline__ uint16_t to_f16_bits(float v) {
   v = fminf(fmaxf(v, -65504.f), 65504.f);
   const __half h = __float2half_rn(v);
@@ -138,12 +172,13 @@ struct DecodePlan {
   int KB;          // MX blocks per row
   int bps;         // blocks per reduction split
   int PP;          // decoded-scale row pitch (u32) of one warp
+  int spc;         // scale bytes per 16-byte code chunk: 1 (MXFP4) or 2 (NVFP4)
   int sc_pitch;    // raw scale bytes of one unit and matrix, padded to 16
   int nraw;        // raw scale buffers (two for short units: copies run two units ahead)
   size_t raw_off, pairs_off, red_off, bytes;
 };
 
-__host__ __device__ inline DecodePlan decode_plan(int nmat, int K, int rg) {
+__host__ __device__ inline DecodePlan decode_plan(int nmat, int K, int rg, int fmt) {
   DecodePlan p;
   const int ks = DV_WARPS / rg;
   p.KB = K / 32;
@@ -151,7 +186,8 @@ __host__ __device__ inline DecodePlan decode_plan(int nmat, int K, int rg) {
   p.bps = (((p.KB + ks - 1) / ks) + 1) & ~1;
   p.PP = (p.bps + 7) & ~7;
   if (p.PP % 32 == 0) p.PP += 8;   // rows g and g + 1 of a quarter-warp on other banks
-  p.sc_pitch = (16 * rg * p.KB + 15) & ~15;
+  p.spc = fmt == 1 ? 2 : 1;
+  p.sc_pitch = (16 * rg * p.KB * p.spc + 15) & ~15;
   p.nraw = rg == 1 ? 2 : 1;
   p.raw_off = (size_t)DV_WARPS * DV_STAGES * 2 * DV_BOX;
   p.pairs_off = p.raw_off + (size_t)p.nraw * nmat * p.sc_pitch;
@@ -185,7 +221,7 @@ struct ProducerState {
 // it next.  B fragments (the tokens' f16 activation rows, a few KB in L2) are
 // loaded at the top of each slot, and the next slot's lines are prefetched
 // into L1.
-template <int EPI, int RG, bool POOL>
+template <int EPI, int RG, bool POOL, int FMT>
 __global__ void __launch_bounds__(32 * DV_WARPS, 2)
 decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm3,
                     const __grid_constant__ CUtensorMap tp1, const __grid_constant__ CUtensorMap tp3,
@@ -194,6 +230,7 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   constexpr int KS = DV_WARPS / RG;
   constexpr int CTA_ROWS = 16 * RG;
   constexpr int RV = KS == 2 ? 4 : 8;   // partial sums a warp hands over per lane
+  constexpr int SPC = FMT == 1 ? 2 : 1; // scale bytes per 16-byte code chunk
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ uint64_t full[DV_WARPS][DV_STAGES];
   __shared__ uint64_t sbar[2];
@@ -278,7 +315,7 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   }
   __syncthreads();
   uint8_t *smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
-  const DecodePlan plan = decode_plan(NMAT, a.K, RG);
+  const DecodePlan plan = decode_plan(NMAT, a.K, RG, FMT);
   const int K = a.K, R = a.R, KB = plan.KB, PP = plan.PP, sc_pitch = plan.sc_pitch;
   const int grp = warp / KS, split = warp - grp * KS;
   const int b_beg = min(KB, split * plan.bps), b_end = min(KB, b_beg + plan.bps);
@@ -308,7 +345,7 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     if (u >= total) return;
     const int sl = u / row_blocks;
     const int e = s_active[sl], r0 = (u - sl * row_blocks) * CTA_ROWS;
-    const uint32_t bytes = (uint32_t)min(CTA_ROWS, R - r0) * KB;   // rows % 16 == 0
+    const uint32_t bytes = (uint32_t)min(CTA_ROWS, R - r0) * KB * SPC;   // rows % 16 == 0
     const int b = i % NRAW;
     tc::mbar_arrive_expect_tx(&sbar[b], NMAT * bytes);
     uint8_t *dst = smem + plan.raw_off + (size_t)b * NMAT * sc_pitch;
@@ -316,8 +353,8 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     const int ps = POOL ? s_slot[sl] : -1;
     const uint8_t *S1 = ps >= 0 ? a.PS : a.S, *S3 = ps >= 0 ? a.PS3 : a.S3;
     const size_t row = (size_t)(ps >= 0 ? ps : e) * R + r0;
-    bulk_load(dst, S1 + row * KB, bytes, &sbar[b]);
-    if (NMAT == 2) bulk_load(dst + sc_pitch, S3 + row * KB, bytes, &sbar[b]);
+    bulk_load(dst, S1 + row * KB * SPC, bytes, &sbar[b]);
+    if (NMAT == 2) bulk_load(dst + sc_pitch, S3 + row * KB * SPC, bytes, &sbar[b]);
     if (b) raw_mine1 = i;
     else raw_mine0 = i;
   };
@@ -392,7 +429,26 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
                     tc::mbar_wait(&sbar[i % NRAW], (uint32_t)((i / NRAW) & 1), abort));
     // the warps of a group leave together, so none waits on a barrier alone
     if (group_sync_or(grp, 32 * KS, !ok)) { ok = false; break; }
-    {
+    if constexpr (FMT == 1) {
+      // NVFP4: lane (gg = lane / 4, q = lane % 4) takes chunks q, q + 4, ...
+      // of row pair gg; a chunk's two scale bytes of row gg and of row gg + 8
+      // become two byte pairs {s_gg, s_gg+8}, one per block parity, stored
+      // [matrix][row pair][parity][chunk] as 16-bit values
+      const int gg = lane >> 2, q = lane & 3;
+      uint16_t *pw16 = reinterpret_cast<uint16_t *>(pw);
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m) {
+        const uint8_t *src = smem + plan.raw_off + (size_t)((i % NRAW) * NMAT + m) * sc_pitch +
+                             ((grp * 16 + gg) * KB + b_beg) * 2;
+        uint16_t *dst = pw16 + (size_t)(m * 8 + gg) * 2 * PP;
+        for (int b = q; b < nbl; b += 4) {
+          const uint32_t x = *reinterpret_cast<const uint16_t *>(src + 2 * b);
+          const uint32_t y = *reinterpret_cast<const uint16_t *>(src + 2 * b + 16 * KB);
+          dst[b] = (uint16_t)__byte_perm(x, y, 0x0040);
+          dst[PP + b] = (uint16_t)__byte_perm(x, y, 0x0051);
+        }
+      }
+    } else {
       // lane (gg = lane / 4, q = lane % 4) takes blocks 2q, 2q + 1, 2q + 8, ...
       // of row pair gg: two raw bytes of row gg and two of row gg + 8 per step
       // (16-bit loads where the row pitch is even: the split point always is)
@@ -432,6 +488,14 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     }
     const uint32_t *pr1 = pw + g * PP;
     const uint32_t *pr3 = pr1 + 8 * PP;
+    // NVFP4: this lane's block parity (t / 2) row of byte pairs
+    const uint16_t *pn1 = reinterpret_cast<const uint16_t *>(pw) + (size_t)(g * 2 + (t >> 1)) * PP;
+    const uint16_t *pn3 = pn1 + (size_t)8 * 2 * PP;
+    float gs1 = 1.f, gs3 = 1.f;   // NVFP4 matrix scales of this unit's expert
+    if constexpr (FMT == 1) {
+      gs1 = a.G[s_active[sl]];
+      if (NMAT == 2) gs3 = a.G3[s_active[sl]];
+    }
 
     for (int tg = 0; tg < cnt; tg += DV_TOK, ++npass) {
       // token g of this pass, or the pass's last token where g is past it (its
@@ -453,6 +517,42 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       // the 8-block group at local block cb: matrix 1 in box sw (matrix 3,
       // SwiGLU, in the box after it)
       auto compute8 = [&](const uint8_t *sw, int cb, int nb) {
+        if constexpr (FMT == 1) {
+          const uint4 n1 = *reinterpret_cast<const uint4 *>(pn1 + cb);
+          uint4 n3 = n1;
+          if constexpr (NMAT == 2) n3 = *reinterpret_cast<const uint4 *>(pn3 + cb);
+          // the eight chunks' scale pairs {s_g, s_g+8} as f16x2
+          const uint2 f1a = e4m3x4_to_f16x2x2(n1.x), f1b = e4m3x4_to_f16x2x2(n1.y),
+                      f1c = e4m3x4_to_f16x2x2(n1.z), f1d = e4m3x4_to_f16x2x2(n1.w);
+          const uint32_t f1[8] = {f1a.x, f1a.y, f1b.x, f1b.y, f1c.x, f1c.y, f1d.x, f1d.y};
+          uint32_t f3[8] = {f1[0], f1[1], f1[2], f1[3], f1[4], f1[5], f1[6], f1[7]};
+          if constexpr (NMAT == 2) {
+            const uint2 a = e4m3x4_to_f16x2x2(n3.x), b = e4m3x4_to_f16x2x2(n3.y),
+                        c = e4m3x4_to_f16x2x2(n3.z), d = e4m3x4_to_f16x2x2(n3.w);
+            f3[0] = a.x; f3[1] = a.y; f3[2] = b.x; f3[3] = b.y;
+            f3[4] = c.x; f3[5] = c.y; f3[6] = d.x; f3[7] = d.y;
+          }
+          auto block = [&](int bl) {
+            const uint8_t *w = sw + (lane_off ^ (uint32_t)(bl << 4));
+            const uint32_t wg = *reinterpret_cast<const uint32_t *>(w);
+            const uint32_t wh = *reinterpret_cast<const uint32_t *>(w + 8 * DV_BOXB);
+            nv_block(acc1, wg, wh, f1[bl], bx[bl]);
+            if constexpr (NMAT == 2) {
+              const uint32_t vg = *reinterpret_cast<const uint32_t *>(w + DV_BOX);
+              const uint32_t vh = *reinterpret_cast<const uint32_t *>(w + DV_BOX + 8 * DV_BOXB);
+              nv_block(acc3, vg, vh, f3[bl], bx[bl]);
+            }
+          };
+          if (nb == 8) {
+#pragma unroll
+            for (int bl = 0; bl < 8; ++bl) block(bl);
+          } else {
+#pragma unroll
+            for (int bl = 0; bl < 8; ++bl)
+              if (bl < nb) block(bl);
+          }
+          return;
+        }
         const uint4 s1a = *reinterpret_cast<const uint4 *>(pr1 + cb);
         const uint4 s1b = *reinterpret_cast<const uint4 *>(pr1 + cb + 4);
         uint4 s3a = s1a, s3b = s1b;
@@ -578,9 +678,10 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           float v;
-          if constexpr (EPI == 2) v = f1[q] / (1.f + __expf(-f1[q])) * f3[q];
-          else if constexpr (EPI == 1) v = fmaxf(f1[q], 0.f);
-          else v = f1[q];
+          const float a1 = f1[q] * gs1, a3 = f3[q] * gs3;   // NVFP4 matrix scales (else 1)
+          if constexpr (EPI == 2) v = a1 / (1.f + __expf(-a1)) * a3;
+          else if constexpr (EPI == 1) v = fmaxf(a1, 0.f);
+          else v = a1;
           const int tk = tg + 2 * t + q;
           if (tk < cnt && row < R) {
             const __nv_bfloat16 hb = __float2bfloat16_rn(v);
@@ -607,22 +708,22 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   }
 }
 
-template <int EPI, int RG, bool POOL>
+template <int EPI, int RG, bool POOL, int FMT>
 cudaError_t launch_one(DecodeArgs a, const uint8_t *W, const uint8_t *W3, const uint8_t *PW,
                        const uint8_t *PW3, int num_experts, int slots, cudaStream_t s) {
   constexpr int NMAT = (EPI == 2) ? 2 : 1;
-  const size_t smem = 1024 + decode_plan(NMAT, a.K, RG).bytes;
+  const size_t smem = 1024 + decode_plan(NMAT, a.K, RG, FMT).bytes;
   static size_t smem_set = 0;
   static int per_sm = 0;
   if (smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mxfp4_kernel<EPI, RG, POOL>,
+    cudaError_t e = cudaFuncSetAttribute(decode_mxfp4_kernel<EPI, RG, POOL, FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     smem_set = smem;
     per_sm = 0;
   }
   if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mxfp4_kernel<EPI, RG, POOL>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mxfp4_kernel<EPI, RG, POOL, FMT>,
                                                       32 * DV_WARPS, smem) != cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
@@ -656,27 +757,33 @@ cudaError_t launch_one(DecodeArgs a, const uint8_t *W, const uint8_t *W3, const 
   long grid = (long)per_sm * num_sms();
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
-  return launch_pdl(decode_mxfp4_kernel<EPI, RG, POOL>, dim3((unsigned)grid), dim3(32 * DV_WARPS),
+  return launch_pdl(decode_mxfp4_kernel<EPI, RG, POOL, FMT>, dim3((unsigned)grid), dim3(32 * DV_WARPS),
                     smem, s, m1, m3, p1, p3, a);
 }
 
 // Rows per work unit: 64 (four 16-row groups, two reduction splits each)
-// where that still gives every resident CTA a unit, else 32, else 16.  Longer
+// where that still gives every resident CTA a unit, else 32, else 16.
+// Every configuration's shared memory stays within two CTAs per SM.  Longer
 // units spread the per-unit costs (scale decoding, the partial-sum exchange,
 // the epilogue) over more weight bytes.
-template <int EPI, bool POOL>
+template <int EPI, bool POOL, int FMT>
 cudaError_t launch_rg(DecodeArgs a, const uint8_t *W, const uint8_t *W3, const uint8_t *PW,
                       const uint8_t *PW3, int num_experts, int slots, cudaStream_t s) {
   const long ctas = 2L * num_sms();
   auto units = [&](int rg) { return (long)slots * ((a.R + 16 * rg - 1) / (16 * rg)); };
-  if (units(4) >= ctas) return launch_one<EPI, 4, POOL>(a, W, W3, PW, PW3, num_experts, slots, s);
-  if (units(2) >= ctas) return launch_one<EPI, 2, POOL>(a, W, W3, PW, PW3, num_experts, slots, s);
-  return launch_one<EPI, 1, POOL>(a, W, W3, PW, PW3, num_experts, slots, s);
+  // (NVFP4 units stop at 32 rows: their scale bytes double, and 64-row units
+  // would not fit two CTAs per SM)
+  if constexpr (FMT == 0)
+    if (units(4) >= ctas)
+      return launch_one<EPI, 4, POOL, FMT>(a, W, W3, PW, PW3, num_experts, slots, s);
+  if (units(2) >= ctas)
+    return launch_one<EPI, 2, POOL, FMT>(a, W, W3, PW, PW3, num_experts, slots, s);
+  return launch_one<EPI, 1, POOL, FMT>(a, W, W3, PW, PW3, num_experts, slots, s);
 }
 
 // Both projections of the small-batch FFN (see launch_decode_ffn); POOL: the
 // kernels read resident experts from pool's slots.
-template <bool POOL>
+template <bool POOL, int FMT>
 cudaError_t run_decode_ffn(const moe_config &c, int part, const void *act, const int32_t *perm,
                            const int32_t *offsets, const moe_weights &w, void *h, void *y_perm,
                            void *act16, int *status, cudaStream_t s, const moe_expert_pool *pool) {
@@ -706,6 +813,8 @@ cudaError_t run_decode_ffn(const moe_config &c, int part, const void *act, const
     a.S3 = w.S3;
     a.PS = pool ? pool->S1 : nullptr;
     a.PS3 = pool ? pool->S3 : nullptr;
+    a.G = w.G1;
+    a.G3 = w.G3;
     a.R = c.d_ff;
     a.K = c.d;
     a.out = static_cast<__nv_bfloat16 *>(h);
@@ -713,19 +822,21 @@ cudaError_t run_decode_ffn(const moe_config &c, int part, const void *act, const
     const uint8_t *W1 = static_cast<const uint8_t *>(w.W1), *W3 = static_cast<const uint8_t *>(w.W3);
     const uint8_t *P1 = pool ? static_cast<const uint8_t *>(pool->W1) : nullptr;
     const uint8_t *P3 = pool ? static_cast<const uint8_t *>(pool->W3) : nullptr;
-    return c.act == MOE_ACT_SWIGLU ? launch_rg<2, POOL>(a, W1, W3, P1, P3, c.n_experts, slots, s)
-                                   : launch_rg<1, POOL>(a, W1, nullptr, P1, nullptr, c.n_experts, slots, s);
+    return c.act == MOE_ACT_SWIGLU ? launch_rg<2, POOL, FMT>(a, W1, W3, P1, P3, c.n_experts, slots, s)
+                                   : launch_rg<1, POOL, FMT>(a, W1, nullptr, P1, nullptr, c.n_experts, slots, s);
   }
   a.act16 = h16;
   a.S = w.S2;
   a.S3 = nullptr;
   a.PS = pool ? pool->S2 : nullptr;
   a.PS3 = nullptr;
+  a.G = w.G2;
+  a.G3 = nullptr;
   a.R = c.d;
   a.K = c.d_ff;
   a.out = static_cast<__nv_bfloat16 *>(y_perm);
   a.out16 = nullptr;
-  return launch_rg<0, POOL>(a, static_cast<const uint8_t *>(w.W2), nullptr,
+  return launch_rg<0, POOL, FMT>(a, static_cast<const uint8_t *>(w.W2), nullptr,
                       pool ? static_cast<const uint8_t *>(pool->W2) : nullptr, nullptr, c.n_experts,
                       slots, s);
 }

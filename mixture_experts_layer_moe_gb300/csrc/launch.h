@@ -126,6 +126,10 @@ cudaError_t launch_decode_ffn(const moe_config &c, int part, const void *act,
                               const int32_t *perm, const int32_t *offsets, const moe_weights &w,
                               void *h, void *y_perm, void *act16, int *status, cudaStream_t s,
                               const moe_expert_pool *pool = nullptr);
+cudaError_t launch_decode_ffn_nvfp4(const moe_config &c, int part, const void *act,
+                                    const int32_t *perm, const int32_t *offsets,
+                                    const moe_weights &w, void *h, void *y_perm, void *act16,
+                                    int *status, cudaStream_t s);
 cudaError_t launch_decode_ffn_pooled(const moe_config &c, int part, const void *act,
                                      const int32_t *perm, const int32_t *offsets,
                                      const moe_weights &w, void *h, void *y_perm, void *act16,

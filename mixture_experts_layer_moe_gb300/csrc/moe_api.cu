@@ -24,7 +24,8 @@ moe_status check_config(const moe_config *c) {
   if (c->n_experts < 1 || c->n_experts > 256) return MOE_ERR_INVALID_ARG;
   if (c->top_k < 1 || c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
   if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
-  if (c->weight_dtype != MOE_F32 && c->weight_dtype != MOE_BF16 && c->weight_dtype != MOE_MXFP4)
+  if (c->weight_dtype != MOE_F32 && c->weight_dtype != MOE_BF16 && c->weight_dtype != MOE_MXFP4 &&
+      c->weight_dtype != MOE_NVFP4)
     return MOE_ERR_INVALID_ARG;
   if (c->gate != MOE_GATE_TOP_PROB && c->gate != MOE_GATE_RENORM) return MOE_ERR_INVALID_ARG;
   if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
@@ -36,7 +37,12 @@ moe_status check_config(const moe_config *c) {
   // rows must be whole 16-byte vectors
   const int vec = c->act_dtype == MOE_F32 ? 4 : 8;
   if (c->d % vec || c->d_ff % vec || c->d_ff_shared % vec) return MOE_ERR_UNSUPPORTED;
-  if (c->weight_dtype == MOE_MXFP4 && (c->d % 32 || c->d_ff % 32)) return MOE_ERR_UNSUPPORTED;
+  const bool fp4 = c->weight_dtype == MOE_MXFP4 || c->weight_dtype == MOE_NVFP4;
+  if (fp4 && (c->d % 32 || c->d_ff % 32)) return MOE_ERR_UNSUPPORTED;
+  // NVFP4 runs on the small-batch path only
+  if (c->weight_dtype == MOE_NVFP4 &&
+      (c->act_dtype != MOE_BF16 || (int64_t)c->n * c->top_k > kDecodeMaxPairs))
+    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -52,7 +58,14 @@ moe_status check_expert_weights(const moe_config &c, const moe_weights *w) {
   const bool swiglu = c.act == MOE_ACT_SWIGLU;
   if (swiglu != (w->W3 != nullptr)) return MOE_ERR_INVALID_ARG;
   if (swiglu && !ok_ptr(w->W3)) return MOE_ERR_INVALID_ARG;
-  if (c.weight_dtype == MOE_MXFP4) {
+  const bool nv = c.weight_dtype == MOE_NVFP4;
+  if (nv) {
+    if (!w->G1 || !w->G2 || !aligned(w->G1, 4) || !aligned(w->G2, 4)) return MOE_ERR_INVALID_ARG;
+    if (swiglu != (w->G3 != nullptr) || (swiglu && !aligned(w->G3, 4))) return MOE_ERR_INVALID_ARG;
+  } else if (w->G1 || w->G2 || w->G3) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (c.weight_dtype == MOE_MXFP4 || nv) {
     if (!ok_ptr(w->S1) || !ok_ptr(w->S2)) return MOE_ERR_INVALID_ARG;
     if (swiglu != (w->S3 != nullptr)) return MOE_ERR_INVALID_ARG;
     if (swiglu && !ok_ptr(w->S3)) return MOE_ERR_INVALID_ARG;

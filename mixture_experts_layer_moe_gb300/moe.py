@@ -15,7 +15,7 @@ import torch
 
 from . import build as _build
 
-_DTYPE = {"f32": 0, "bf16": 1, "mxfp4": 2}
+_DTYPE = {"f32": 0, "bf16": 1, "mxfp4": 2, "nvfp4": 3}
 _GATE = {"top_prob": 0, "renorm": 1}
 _ACT = {"relu": 0, "swiglu": 1}
 
@@ -38,7 +38,8 @@ class moe_config(ctypes.Structure):
 
 class moe_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("Wg", "router_bias", "W1", "W3", "W2", "S1", "S3", "S2", "Ws1", "Ws3", "Ws2")]
+                ("Wg", "router_bias", "W1", "W3", "W2", "S1", "S3", "S2", "Ws1", "Ws3", "Ws2",
+                 "G1", "G3", "G2")]
 
 
 class moe_expert_pool(ctypes.Structure):
@@ -130,7 +131,8 @@ def make_weights(inputs: dict) -> moe_weights:
         _ptr(g("W1q") if mx else g("W1")), _ptr(g("W3q") if mx else g("W3")),
         _ptr(g("W2q") if mx else g("W2")),
         _ptr(g("S1")), _ptr(g("S3")), _ptr(g("S2")),
-        _ptr(g("Ws1")), _ptr(g("Ws3")), _ptr(g("Ws2")))
+        _ptr(g("Ws1")), _ptr(g("Ws3")), _ptr(g("Ws2")),
+        _ptr(g("G1")), _ptr(g("G3")), _ptr(g("G2")))
 
 
 def make_pool(slot_of: torch.Tensor, pool: dict) -> moe_expert_pool:

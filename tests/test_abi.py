@@ -69,6 +69,8 @@ def _size(lib, c):
     (dict(weight_dtype="mxfp4", d=80), 2), (dict(weight_dtype="f32"), 2),
     (dict(act_dtype="f32", weight_dtype="bf16"), 2), (dict(act_dtype="f32", weight_dtype="f32", d=4), 0),
     (dict(weight_dtype="mxfp4", d=64, d_ff=96), 0), (dict(E=256, k=256), 0), (dict(n=1, E=1, k=1), 0),
+    (dict(weight_dtype="nvfp4", n=64, k=4), 0), (dict(weight_dtype="nvfp4", n=65, k=4), 2),
+    (dict(weight_dtype="nvfp4", d=80), 2), (dict(act_dtype="f32", weight_dtype="nvfp4"), 2),
 ])
 def test_config_checks(lib, kw, want):
     st, _ = _size(lib, _c(lib, **kw))
@@ -167,3 +169,20 @@ def test_pool_entry_point_argument_checks(lib):
     assert cls(None, 3) == 1
     assert cls(FAKE, 0) == 1
     assert cls(FAKE, 3, st=None) == 1
+
+
+def test_nvfp4_weight_checks(lib):
+    """NVFP4 weights need their per-matrix fp32 scales; other formats must not pass them."""
+    c = _c(lib, n=4, weight_dtype="nvfp4")
+    _, n = _size(lib, c)
+    call = lambda cfg, w: lib.raw_call("moe_forward", ctypes.byref(cfg), FAKE, ctypes.byref(w),
+                                       FAKE, FAKE, n, None)
+    no_g = lib.moe_weights(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None)
+    assert call(c, no_g) == 1
+    no_g3 = lib.moe_weights(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+                            FAKE, None, FAKE)
+    assert call(c, no_g3) == 1
+    mx = _c(lib, n=4, weight_dtype="mxfp4")
+    with_g = lib.moe_weights(FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+                             FAKE, FAKE, FAKE)
+    assert call(mx, with_g) == 1

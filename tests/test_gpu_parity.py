@@ -41,6 +41,12 @@ SMALL = {
                                                          act="relu"),
     # an odd number of MX blocks per row (3 and 5) on both projections
     "decode_odd_blocks": C["gptoss_decode_mxfp4"].scaled(n=4, d=96, d_ff=160, E=8, k=2),
+    "nvfp4_decode_small": C["gptoss_decode_nvfp4"].scaled(n=8, d=256, d_ff=320, E=16),
+    "nvfp4_decode_relu": C["gptoss_decode_nvfp4"].scaled(n=16, d=128, d_ff=192, E=8, k=2,
+                                                         act="relu"),
+    "nvfp4_decode_odd_chunks": C["gptoss_decode_nvfp4"].scaled(n=4, d=96, d_ff=160, E=8, k=2),
+    "nvfp4_decode_many_tokens_per_expert": C["gptoss_decode_nvfp4"].scaled(n=64, d=256, d_ff=320,
+                                                                          E=4),
     "prefill_zipf_small": C["gptoss_prefill_zipf_mxfp4"].scaled(n=600, d=256, d_ff=320, E=16),
     "finegrained_small": C["finegrained_shared_bf16"].scaled(n=500, d=256, d_ff=128, E=32,
                                                              d_ff_shared=192),
@@ -61,6 +67,8 @@ FULL = {
     "mixtral_bf16": (C["mixtral_bf16"], 24),
     "gptoss_decode_mxfp4_n16": (C["gptoss_decode_mxfp4"].scaled(n=16), 8),
     "gptoss_decode_mxfp4_n64": (C["gptoss_decode_mxfp4"].scaled(n=64), 8),
+    "gptoss_decode_nvfp4_n1": (C["gptoss_decode_nvfp4"].scaled(n=1), 1),
+    "gptoss_decode_nvfp4_n64": (C["gptoss_decode_nvfp4"].scaled(n=64), 8),
     "gptoss_prefill_zipf_mxfp4": (C["gptoss_prefill_zipf_mxfp4"], 24),
     "finegrained_shared_bf16": (C["finegrained_shared_bf16"], 12),
 }
