@@ -1,0 +1,498 @@
+// MXFP4 grouped GEMM on the 5th-generation tensor cores, weights as the A
+// operand in tensor memory.
+//
+// "How Mixture of Experts Scales Model Parameters": each expert's FFN runs on
+// the rows routed to it (sections "Sparse models" and "The forward pass:
+// dispatch, then combine"); weights are MXFP4 (feed post "What is MXFP4?": 4-bit
+// elements in blocks of 32 sharing one scale; E2M1 / E8M0 bits per the OCP MX
+// v1.0 format).
+//
+// A tile computes D[w][t] = sum_k W[w][k] * X[t][k] for 128 weight rows w (MMA
+// M, the TMEM lanes) and 128 tokens t of one expert's segment (MMA N), i.e. the
+// transposed output tile.  The token rows (f16 copies of the activations) come
+// by TMA into a 128-byte-swizzled shared-memory tile, the B operand.  The
+// weights never touch shared memory in f16: four transform warps read the
+// packed codes (TMA, 32-byte swizzle), convert each row's 64 codes of a k-block
+// with cvt.rn.f16x2.e2m1x2, multiply by the block's E8M0 scale as an f16 pair
+// (exact for scale bytes 113..142; others are reported as MOE_ERR_RANGE) and
+// write them with tcgen05.st into the A stage in tensor memory (lane = weight
+// row, 32-bit column c = k-elements 2c and 2c + 1).  Shared memory carries only
+// the TMA traffic and the code reads, not a dequantised tile written and read
+// back.  Used for the single-matrix projections (the down projection, and a
+// ReLU up projection); the SwiGLU up projection, whose tiles would cover only
+// 64 output columns here, stays on the shared-memory-transform kernel of
+// gemm_tc.cu, which measured faster for it.
+//
+// Warp roles (persistent, one CTA per SM): 0 TMA producer, 1 MMA issuer and
+// TMEM owner, 2-5 epilogue (TMEM -> registers -> global), 6-9 transform.  TMEM:
+// two 128-column accumulators, then GS stages of 32 columns of A.
+#include "common.cuh"
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int GM = 128;                         // weight rows per tile (MMA M)
+constexpr int GN = 128;                         // tokens per tile (MMA N)
+constexpr int GK = 64;                          // k-block
+constexpr int GS = 8;                           // pipeline stages
+constexpr int G_B_BYTES = GN * GK * 2;          // token tile: 16 KB
+constexpr int G_C_BYTES = GM * GK / 2;          // codes of the k-block: 4 KB
+constexpr int G_STAGE = G_B_BYTES + G_C_BYTES;  // 20 KB
+constexpr int G_THREADS = 320;
+constexpr uint32_t G_TMEM_COLS = 512;
+constexpr uint32_t G_A_COL0 = 2 * GN;           // A stages after the two accumulators
+constexpr int G_MAX_E = 256;
+constexpr int G_XFORM = 4;                      // transform warps
+constexpr int G_EPI = 4;                        // epilogue warps
+
+struct GShared {
+  uint64_t full[GS], empty[GS], aready[GS];
+  uint64_t tfull[2], tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort, failed_on_entry, num_tiles;
+  int offs[G_MAX_E + 1];
+  int tile_start[G_MAX_E];
+};
+
+struct GArgs {
+  const int32_t *offsets;
+  int num_experts, rows, K, N;
+  const uint8_t *S;          // E8M0 scales [E][N][K/32]
+  __nv_bfloat16 *out;        // [rows][N]
+  uint16_t *out16;           // f16 copy of out, or nullptr
+  int *status;
+};
+
+struct GTile {
+  int e, row0, seg_end, n_idx;
+};
+
+__device__ __forceinline__ GTile g_decode(const GShared &sh, int E, int t) {
+  int lo = 0, hi = E;   // largest e with tile_start[e] <= t (skips empty experts)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (sh.tile_start[mid] <= t) lo = mid; else hi = mid;
+  }
+  GTile tl;
+  tl.e = lo;
+  const int beg = sh.offs[lo], end = sh.offs[lo + 1];
+  const int m_tiles = (end - beg + GN - 1) / GN;
+  const int local = t - sh.tile_start[lo];
+  tl.n_idx = local / m_tiles;                  // token blocks fastest: neighbours share weights
+  tl.row0 = beg + (local - tl.n_idx * m_tiles) * GN;
+  tl.seg_end = end;
+  return tl;
+}
+
+__device__ __forceinline__ uint4 e2m1x8_to_f16x2x4(uint32_t w) {
+  uint4 r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "r"(w));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// E8M0 byte -> 2^(s-127) as an f16 pair; 0 (and *bad set) outside f16's normal range.
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t s, bool &bad) {
+  if (s < 113u || s > 142u) {
+    bad = true;
+    return 0u;
+  }
+  const uint32_t h = (s - 112u) << 10;
+  return h | (h << 16);
+}
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (f16 inputs, fp32 accumulate).
+__device__ __forceinline__ void mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns from registers (thread l of the
+// warp -> lane 32*(warp%4) + l).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Named barrier `id` over n threads, OR of pred over them (the same answer for all).
+__device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ uint16_t f16_bits_of_bf16(__nv_bfloat16 b) {
+  float v = fminf(fmaxf(__bfloat162float(b), -65504.f), 65504.f);
+  const __half h = __float2half_rn(v);
+  return *reinterpret_cast<const uint16_t *>(&h);
+}
+
+__host__ __device__ inline size_t g_scale_pitch(int K) {
+  return ((size_t)GM * (K / 32) + 15) & ~(size_t)15;
+}
+__host__ __device__ inline size_t g_scale_off() { return (size_t)GS * G_STAGE; }
+size_t g_dyn_smem(int K) { return 1024 + g_scale_off() + 2 * g_scale_pitch(K); }
+
+// EPI 0: y = X W^T; EPI 1: h = relu(X W^T).  128 output columns per tile.
+template <int EPI>
+__global__ void __launch_bounds__(G_THREADS, 1)
+gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+               GArgs args) {
+  constexpr int N_OUT = GM;                         // output columns per tile
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ GShared sh;
+  uint8_t *smem = dyn_smem + ((1024 - (tc::smem_u32(dyn_smem) & 1023)) & 1023);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = args.num_experts;
+  const int n_tiles = (args.N + N_OUT - 1) / N_OUT;
+  const int KB = args.K / GK;
+  const int KBLK = args.K / 32;
+
+  pdl_launch_dependents();
+  pdl_wait();
+  if (threadIdx.x == 0) {
+    sh.failed_on_entry = status_failed(args.status) ? 1 : 0;
+    sh.abort = sh.failed_on_entry;
+  }
+  for (int i = threadIdx.x; i <= E; i += G_THREADS) sh.offs[i] = args.offsets[i];
+  if (warp == 1) tc::tmem_alloc(&sh.tmem_base, G_TMEM_COLS);
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < GS; ++s) {
+      tc::mbar_init(&sh.full[s], 1);
+      tc::mbar_init(&sh.empty[s], 1 + G_XFORM);   // the MMAs (token tile), the transform (codes)
+      tc::mbar_init(&sh.aready[s], G_XFORM);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&sh.tfull[a], 1);
+      tc::mbar_init(&sh.tempty[a], G_EPI);
+    }
+    tc::mbar_init(&sh.drain, 1);
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // tile prefix over experts: lane l owns experts 8l .. 8l+7
+    int cnt[8];
+    int sum = 0, bad = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      cnt[i] = 0;
+      if (e < E) {
+        const int b = sh.offs[e], en = sh.offs[e + 1];
+        if (b < 0 || en < b || en > args.rows) bad = 1;
+        else cnt[i] = ((en - b + GN - 1) / GN) * n_tiles;
+      }
+      sum += cnt[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      if (e < E) sh.tile_start[e] = run;
+      run += cnt[i];
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      sh.num_tiles = bad ? 0 : total;
+      if (bad) set_status(args.status, MOE_ERR_BAD_INDEX, -1);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = sh.tmem_base;
+  const int num_tiles = sh.num_tiles;
+  volatile int *abort = &sh.abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer: token tile + the k-block's codes
+      tc::prefetch_tmap(&tmX);
+      tc::prefetch_tmap(&tmW);
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_phase[GS];
+#pragma unroll
+      for (int s = 0; s < GS; ++s) last_phase[s] = -1;
+      for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
+        const GTile tl = g_decode(sh, E, t);
+        const int wrow = tl.n_idx * N_OUT;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc::mbar_wait(&sh.empty[stage], phase ^ 1u, abort)) break;
+          uint8_t *sb = smem + stage * G_STAGE;
+          uint8_t *sc = sb + G_B_BYTES;
+          tc::mbar_arrive_expect_tx(&sh.full[stage], G_STAGE);
+          tc::tma_load_2d(&tmX, &sh.full[stage], sb, kb * GK, tl.row0);
+          tc::tma_load_3d(&tmW, &sh.full[stage], sc, kb * (GK / 2), wrow, tl.e);
+          last_phase[stage] = (int)phase;
+          if (++stage == GS) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (*abort) {
+        for (int s = 0; s < GS; ++s)
+          if (last_phase[s] >= 0)
+            tc::mbar_wait_drain(&sh.full[s], (uint32_t)last_phase[s], 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: D(acc) = A(TMEM, weights) x B(smem, tokens)^T
+      constexpr uint32_t idesc = tc::idesc_f16_f32(GM, GN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok && !*abort; t += gridDim.x, ++local) {
+        const int acc = local & 1;
+        if (!tc::mbar_wait(&sh.tempty[acc], ((local >> 1) & 1) ^ 1u, abort)) { ok = false; break; }
+        tc::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * GN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc::mbar_wait(&sh.full[stage], phase, abort)) { ok = false; break; }
+          if (!tc::mbar_wait(&sh.aready[stage], phase, abort)) { ok = false; break; }
+          tc::tc_fence_after();
+          const uint32_t sb = tc::smem_u32(smem + stage * G_STAGE);
+          const uint32_t a_tmem = tmem_base + G_A_COL0 + (uint32_t)(stage * (GK / 2));
+#pragma unroll
+          for (int k = 0; k < GK / 16; ++k)
+            mma_ta(d_tmem, a_tmem + k * 8, tc::smem_desc_sw128(sb + k * 32), idesc,
+                   (kb != 0 || k != 0) ? 1u : 0u);
+          tc::mma_commit(&sh.empty[stage]);
+          if (++stage == GS) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc::mma_commit(&sh.tfull[acc]);
+      }
+      if (*abort) {
+        tc::mma_commit(&sh.drain);
+        tc::mbar_wait_drain(&sh.drain, 0, 100000000ull);
+      }
+    }
+  } else if (warp < 2 + G_EPI) {
+    // ---------------- epilogue: warp w drains TMEM lanes 32*(w%4) .. +31; the
+    // thread of weight row j writes column j of 32 tokens per chunk (a warp's
+    // stores of one token are 64 contiguous bytes)
+    const int quarter = warp & 3;
+    const int j = quarter * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    int local = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+      const GTile tl = g_decode(sh, E, t);
+      const int acc = local & 1;
+      const bool ok = tc::mbar_wait(&sh.tfull[acc], (local >> 1) & 1, abort);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc::tc_fence_after();
+      const int col = tl.n_idx * N_OUT + j;
+      const bool col_ok = col < args.N;
+#pragma unroll 1
+      for (int c = 0; c < GN / 32; ++c) {
+        uint32_t a[32];
+        tc::tmem_ld32(lane_base + (uint32_t)(acc * GN) + c * 32, a);
+        tc::tmem_ld_wait();
+        const int tok0 = tl.row0 + c * 32;
+        if (col_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int tok = tok0 + i;
+            if (tok < tl.seg_end) {
+              float v = __uint_as_float(a[i]);
+              if constexpr (EPI == 1) v = fmaxf(v, 0.f);
+              const __nv_bfloat16 hb = __float2bfloat16_rn(v);
+              args.out[(size_t)tok * args.N + col] = hb;
+              if (args.out16) args.out16[(size_t)tok * args.N + col] = f16_bits_of_bf16(hb);
+            }
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sh.tempty[acc]);
+    }
+  } else {
+    // ---------------- transform: warp w writes TMEM lanes 32*(w%4) .. +31, one
+    // weight row per thread.  A tile's scales are copied (cp.async) into one
+    // of two buffers while the previous tile runs.  The codes arrive with a
+    // 32-byte swizzle: 16-byte half c of row r sits at c ^ ((r >> 2) & 1).
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int tt = threadIdx.x - 32 * (2 + G_EPI);     // 0 .. 127
+    constexpr int XT = 32 * G_XFORM;
+    const size_t spitch = g_scale_pitch(args.K);
+    uint8_t *scale_buf[2] = {smem + g_scale_off(), smem + g_scale_off() + spitch};
+    auto fetch_scales = [&](int t, int b) {
+      const GTile tl = g_decode(sh, E, t);
+      const int wrow = tl.n_idx * N_OUT;
+      const int rows = min(GM, args.N - wrow);
+      const size_t bytes = (size_t)rows * KBLK;       // a multiple of 16
+      const uint8_t *src = args.S + ((size_t)tl.e * args.N + wrow) * KBLK;
+      for (size_t o = (size_t)tt * 16; o < bytes; o += XT * 16)
+        cp_async16(scale_buf[b] + o, src + o);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    int stage = 0;
+    uint32_t phase = 0;
+    int buf = 0;
+    bool bad_scale = false;
+    const int sw = ((r >> 2) & 1) << 4;
+    const uint32_t a_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + G_A_COL0;
+    if (blockIdx.x < num_tiles) fetch_scales(blockIdx.x, 0);
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, buf ^= 1) {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      // this tile's scales are in; the transform warps also agree here on
+      // stopping (a warp whose wait ran out has raised *abort)
+      if (bar_or(3, XT, *abort != 0)) break;
+      if (t + (int)gridDim.x < num_tiles) fetch_scales(t + gridDim.x, buf ^ 1);
+      const uint8_t *srow = scale_buf[buf] + (size_t)r * KBLK;
+      const int wrow = g_decode(sh, E, t).n_idx * N_OUT;
+      const bool row_ok = wrow + r < args.N;          // else: zero row
+      for (int kb = 0; kb < KB; ++kb) {
+        const bool ok = tc::mbar_wait(&sh.full[stage], phase, abort);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const uint8_t *codes = smem + stage * G_STAGE + G_B_BYTES + r * 32;
+        uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
+        if (row_ok) {
+          c0 = *reinterpret_cast<const uint4 *>(codes + sw);
+          c1 = *reinterpret_cast<const uint4 *>(codes + (sw ^ 16));
+        }
+        // the codes are in registers: this warp is done with the stage's codes
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sh.empty[stage]);
+        uint32_t v[32];
+        if (row_ok) {
+          const uint32_t f0 = scale_f16x2(srow[2 * kb], bad_scale);
+          const uint32_t f1 = scale_f16x2(srow[2 * kb + 1], bad_scale);
+          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            const uint32_t f = w < 4 ? f0 : f1;
+            const uint4 q = e2m1x8_to_f16x2x4(words[w]);
+            v[4 * w] = hmul2(q.x, f);
+            v[4 * w + 1] = hmul2(q.y, f);
+            v[4 * w + 2] = hmul2(q.z, f);
+            v[4 * w + 3] = hmul2(q.w, f);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        // the stage's A columns are free: the MMAs that read them completed
+        // before the producer refilled this stage
+        tmem_st32(a_lane + (uint32_t)(stage * (GK / 2)), v);
+        tmem_st_wait();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sh.aready[stage]);
+        if (++stage == GS) { stage = 0; phase ^= 1u; }
+      }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (bad_scale) set_status(args.status, MOE_ERR_RANGE, 0);
+  }
+
+  __syncwarp();
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, G_TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && sh.abort && !sh.failed_on_entry)
+    set_status(args.status, MOE_ERR_TIMEOUT, blockIdx.x);
+}
+
+template <int EPI>
+cudaError_t launch_mx(const GemmStage &g, int *status, cudaStream_t s) {
+  const size_t smem = g_dyn_smem(g.K);
+  static size_t smem_set = 0;
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_mx_kernel<EPI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set = smem;
+  }
+  CUtensorMap mX, mW;
+  const uint64_t dX[2] = {(uint64_t)g.K, (uint64_t)g.rows};
+  const uint32_t bX[2] = {GK, GN};
+  if (!make_tensor_map(&mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.A, 2, dX, bX,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  // packed codes: [E][N][K/2] bytes, boxes of 32 bytes (one k-block) x 128 rows
+  const uint64_t dC[3] = {(uint64_t)g.K / 2, (uint64_t)g.N, (uint64_t)g.num_experts};
+  const uint32_t bC[3] = {GK / 2, (uint32_t)GM, 1};
+  if (!make_tensor_map(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.B, 3, dC, bC,
+                       CU_TENSOR_MAP_SWIZZLE_32B))
+    return cudaErrorInvalidValue;
+  GArgs a{};
+  a.offsets = g.offsets;
+  a.num_experts = g.num_experts;
+  a.rows = g.rows;
+  a.K = g.K;
+  a.N = g.N;
+  a.S = g.SB;
+  a.out = static_cast<__nv_bfloat16 *>(g.out);
+  a.out16 = static_cast<uint16_t *>(g.out16);
+  a.status = status;
+  return launch_pdl(gemm_mx_kernel<EPI>, dim3(num_sms()), dim3(G_THREADS), smem, s, mX, mW, a);
+}
+
+}  // namespace
+
+bool gemm_mx_supported(const GemmStage &g) {
+  return g.rows > 0 && tensor_maps_available() && g.b_dtype == MOE_MXFP4 && g.a_dtype == kF16 &&
+         g.out_dtype == MOE_BF16 && (g.epi == 0 || g.epi == 1) && g.offsets != nullptr &&
+         g.num_experts <= G_MAX_E && g.K % GK == 0 && g.N % 32 == 0 &&
+         g_dyn_smem(g.K) + sizeof(GShared) <= 227 * 1024;
+}
+
+cudaError_t launch_gemm_mx(const GemmStage &g, int *status, cudaStream_t s) {
+  return g.epi == 1 ? launch_mx<1>(g, status, s) : launch_mx<0>(g, status, s);
+}
+
+}  // namespace moe

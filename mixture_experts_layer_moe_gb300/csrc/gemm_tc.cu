@@ -42,18 +42,27 @@ constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int DYN_SMEM = STAGES * STAGE_BYTES + 1024;
-// MX variant: 3 stages of [A 16 KB][B 32 KB][codes 8 KB], two scale buffers
-constexpr int MX_STAGES = 3;
+// MX variant: a TMA ring of [A 16 KB][codes 8 KB] stages and a separate ring of
+// dequantised f16 B tiles (32 KB) written by the transform warps, so the TMA
+// runs MX_STAGES k-blocks ahead of the MMAs while only MX_BSTAGES B tiles
+// exist; plus two tile-sized buffers of E8M0 scales.
+constexpr int MX_STAGES = 4;
+constexpr int MX_BSTAGES = 2;
 constexpr int MX_XWARPS = 8;                       // transform warps (one B row per thread)
 constexpr int MX_THREADS = 192 + 32 * MX_XWARPS;
 constexpr int CODE_BYTES = BN * BK / 2;
-constexpr int MX_STAGE_BYTES = A_BYTES + B_BYTES + CODE_BYTES;
+constexpr int MX_STAGE_BYTES = A_BYTES + CODE_BYTES;
+constexpr int MAX_STAGES = STAGES > MX_STAGES ? STAGES : MX_STAGES;
 constexpr int MAX_E = 256;
 constexpr uint32_t TMEM_COLS = 512;
 
 __host__ __device__ inline size_t mx_scale_buf_bytes(int K) { return (size_t)BN * (K / 32); }
+__host__ __device__ inline size_t mx_bring_off() { return (size_t)MX_STAGES * MX_STAGE_BYTES; }
+__host__ __device__ inline size_t mx_scale_off() {
+  return mx_bring_off() + (size_t)MX_BSTAGES * B_BYTES;
+}
 size_t mx_dyn_smem(int K) {
-  return 1024 + (size_t)MX_STAGES * MX_STAGE_BYTES + 2 * ((mx_scale_buf_bytes(K) + 15) & ~15);
+  return 1024 + mx_scale_off() + 2 * ((mx_scale_buf_bytes(K) + 15) & ~15);
 }
 
 struct TcArgs {
@@ -71,9 +80,10 @@ struct TcArgs {
 };
 
 struct TcShared {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t bready[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
+  uint64_t bready[MX_BSTAGES];    // MX: a dequantised B tile is written
+  uint64_t bempty[MX_BSTAGES];    // MX: the MMAs have read it
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -191,8 +201,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (threadIdx.x == 32) {
     for (int s = 0; s < NSTAGE; ++s) {
       tc::mbar_init(&sh.full[s], 1);
-      tc::mbar_init(&sh.empty[s], 1);
-      tc::mbar_init(&sh.bready[s], 32 * MX_XWARPS);
+      // MX: the codes are read by the transform warps (one arrival each), A by
+      // the MMAs
+      tc::mbar_init(&sh.empty[s], MX ? 1 + MX_XWARPS : 1);
+    }
+    for (int b = 0; b < MX_BSTAGES; ++b) {
+      tc::mbar_init(&sh.bready[b], 32 * MX_XWARPS);
+      tc::mbar_init(&sh.bempty[b], 1);
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&sh.tfull[a], 1);
@@ -252,9 +267,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (EPI == 2) tc::prefetch_tmap(&tmB3);
       int stage = 0;
       uint32_t phase = 0;
-      int last_phase[STAGES];
+      int last_phase[MAX_STAGES];
 #pragma unroll
-      for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
+      for (int s = 0; s < MAX_STAGES; ++s) last_phase[s] = -1;
       for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
         const Tile tl = decode_tile(sh, E, t);
         const int wrow = tl.n_idx * N_OUT;
@@ -265,7 +280,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           tc::mbar_arrive_expect_tx(&sh.full[stage], TX_BYTES);
           tc::tma_load_2d(&tmA, &sh.full[stage], sa, kb * BK, tl.row0);
           if constexpr (MX) {
-            uint8_t *sc = sb + B_BYTES;
+            uint8_t *sc = sb;                         // the codes follow A
             if (EPI == 2) {
               tc::tma_load_3d(&tmB, &sh.full[stage], sc, kb * (BK / 2), wrow, tl.e);
               tc::tma_load_3d(&tmB3, &sh.full[stage], sc + CODE_BYTES / 2, kb * (BK / 2), wrow,
@@ -296,6 +311,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       constexpr uint32_t idesc = MX ? tc::idesc_f16_f32(BM, BNT) : tc::idesc_bf16_f32(BM, BNT);
       int stage = 0;
       uint32_t phase = 0;
+      int bstage = 0;              // MX: dequantised B ring
+      uint32_t bphase = 0;
       int local = 0;   // accumulator uses so far (tiles, or k-blocks with KPART)
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok && !*abort; t += gridDim.x) {
@@ -309,16 +326,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
           if (!tc::mbar_wait(&sh.full[stage], phase, abort)) { ok = false; break; }
-          if (MX && !tc::mbar_wait(&sh.bready[stage], phase, abort)) { ok = false; break; }
+          if (MX && !tc::mbar_wait(&sh.bready[bstage], bphase, abort)) { ok = false; break; }
           tc::tc_fence_after();
           const uint32_t sa = tc::smem_u32(smem + stage * SBYTES);
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sb = MX ? tc::smem_u32(smem + mx_bring_off() + (size_t)bstage * B_BYTES)
+                                 : sa + A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             tc::mma_bf16(d_tmem, tc::smem_desc_sw128(sa + k * 32), tc::smem_desc_sw128(sb + k * 32),
                          idesc, (k != 0 || (!KPART && kb != 0)) ? 1u : 0u);
           tc::mma_commit(&sh.empty[stage]);
           if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
+          if constexpr (MX) {
+            tc::mma_commit(&sh.bempty[bstage]);
+            if (++bstage == MX_BSTAGES) { bstage = 0; bphase ^= 1u; }
+          }
           if (KPART || kb == KB - 1) {
             tc::mma_commit(&sh.tfull[acc]);
             ++local;
@@ -438,8 +460,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int KBLK = args.K / 32;
     const size_t sbuf = mx_scale_buf_bytes(args.K);
     const size_t spitch = (sbuf + 15) & ~(size_t)15;
-    uint8_t *scale_buf[2] = {smem + (size_t)MX_STAGES * MX_STAGE_BYTES,
-                             smem + (size_t)MX_STAGES * MX_STAGE_BYTES + spitch};
+    uint8_t *scale_buf[2] = {smem + mx_scale_off(), smem + mx_scale_off() + spitch};
     // scales of tile t's rows -> buffer b (rows past N are left unset: their
     // codes are zero-filled by TMA and their columns are never stored)
     auto fetch_scales = [&](int t, int b) {
@@ -457,8 +478,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, bstage = 0;
+    uint32_t phase = 0, bphase = 0;
     int buf = 0;
     bool bad_scale = false;
     const int r = tt;                                         // B row in the tile
@@ -482,13 +503,23 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int wrow = decode_tile(sh, E, t).n_idx * N_OUT;
       const bool row_ok = wrow + (r % rows_per) < args.N;    // else: zero row
       for (int kb = 0; kb < KB; ++kb) {
-        const bool ok = tc::mbar_wait(&sh.full[stage], phase, abort);
+        bool ok = tc::mbar_wait(&sh.full[stage], phase, abort);
         if (!__all_sync(0xffffffffu, ok)) break;
-        const uint8_t *codes = smem + stage * SBYTES + A_BYTES + B_BYTES + r * 32;
-        uint8_t *brow = smem + stage * SBYTES + A_BYTES + (r >> 3) * 1024 + (r & 7) * 128;
+        const uint8_t *codes = smem + stage * SBYTES + A_BYTES + r * 32;
+        uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
         if (row_ok) {
-          const uint4 c0 = *reinterpret_cast<const uint4 *>(codes + sw);
-          const uint4 c1 = *reinterpret_cast<const uint4 *>(codes + (sw ^ 16));
+          c0 = *reinterpret_cast<const uint4 *>(codes + sw);
+          c1 = *reinterpret_cast<const uint4 *>(codes + (sw ^ 16));
+        }
+        // the codes are in registers: this warp is done with the TMA stage
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sh.empty[stage]);
+        if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
+        ok = tc::mbar_wait(&sh.bempty[bstage], bphase ^ 1u, abort);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        uint8_t *brow = smem + mx_bring_off() + (size_t)bstage * B_BYTES + (r >> 3) * 1024 +
+                        (r & 7) * 128;
+        if (row_ok) {
           const uint32_t s0 = 2 * kb < KBLK ? srow[2 * kb] : 127u;
           const uint32_t s1 = 2 * kb + 1 < KBLK ? srow[2 * kb + 1] : 127u;
           const uint32_t f0 = scale_f16x2(s0, bad_scale), f1 = scale_f16x2(s1, bad_scale);
@@ -507,8 +538,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         // generic-proxy writes of the B tile -> visible to the tensor core
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc::mbar_arrive(&sh.bready[stage]);
-        if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
+        tc::mbar_arrive(&sh.bready[bstage]);
+        if (++bstage == MX_BSTAGES) { bstage = 0; bphase ^= 1u; }
       }
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -595,9 +626,10 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
 bool gemm_tc_supported(const GemmStage &g) {
   if (g.rows <= 0 || !tensor_maps_available()) return false;
   if (g.b_dtype == MOE_MXFP4) {
+    if (g.epi != 2) return gemm_mx_supported(g);
     // f16 activations, MXFP4 weights; all scale buffers must fit in shared memory
-    return g.a_dtype == kF16 && g.out_dtype == MOE_BF16 && (g.epi == 0 || g.epi == 2) &&
-           g.K % 64 == 0 && g.N % 32 == 0 && mx_dyn_smem(g.K) + sizeof(TcShared) <= 227 * 1024;
+    return g.a_dtype == kF16 && g.out_dtype == MOE_BF16 && g.K % 64 == 0 && g.N % 32 == 0 &&
+           mx_dyn_smem(g.K) + sizeof(TcShared) <= 227 * 1024;
   }
   const bool out_ok = g.epi == 3 ? g.out_dtype == MOE_F32 : g.out_dtype == MOE_BF16;
   const bool n_ok = g.epi == 3 ? true : g.N % 8 == 0;
@@ -605,8 +637,11 @@ bool gemm_tc_supported(const GemmStage &g) {
 }
 
 cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s) {
-  if (g.b_dtype == MOE_MXFP4) return g.epi == 2 ? launch_epi<2, true>(g, status, s)
-                                                : launch_epi<0, true>(g, status, s);
+  // MXFP4: the SwiGLU up projection on this file's kernel (dequantised tile in
+  // shared memory), the single-matrix projections with the weights in tensor
+  // memory (gemm_mx.cu)
+  if (g.b_dtype == MOE_MXFP4)
+    return g.epi == 2 ? launch_epi<2, true>(g, status, s) : launch_gemm_mx(g, status, s);
   switch (g.epi) {
     case 0: return launch_epi<0, false>(g, status, s);
     case 1: return launch_epi<1, false>(g, status, s);

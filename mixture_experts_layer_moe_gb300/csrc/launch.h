@@ -98,6 +98,10 @@ cudaError_t launch_gemm_simt(const GemmStage &g, int *status, cudaStream_t s);
 // TMEM, TMA-fed); gemm_tc_supported() says whether the shape/dtypes qualify.
 bool gemm_tc_supported(const GemmStage &g);
 cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s);
+// MXFP4 grouped GEMM with the dequantised weights as the tcgen05 A operand in
+// tensor memory (f16 activation copies in, bf16 out; epi 0 or 1).
+bool gemm_mx_supported(const GemmStage &g);
+cudaError_t launch_gemm_mx(const GemmStage &g, int *status, cudaStream_t s);
 
 // Picks the tensor-core kernel when it applies, else the CUDA-core one.
 inline cudaError_t launch_gemm(const GemmStage &g, int *status, cudaStream_t s) {

@@ -48,6 +48,8 @@ SMALL = {
     "nvfp4_decode_many_tokens_per_expert": C["gptoss_decode_nvfp4"].scaled(n=64, d=256, d_ff=320,
                                                                           E=4),
     "prefill_zipf_small": C["gptoss_prefill_zipf_mxfp4"].scaled(n=600, d=256, d_ff=320, E=16),
+    "prefill_relu_mxfp4_small": C["gptoss_prefill_zipf_mxfp4"].scaled(n=600, d=256, d_ff=320,
+                                                                      E=16, act="relu"),
     "finegrained_small": C["finegrained_shared_bf16"].scaled(n=500, d=256, d_ff=128, E=32,
                                                              d_ff_shared=192),
 }
