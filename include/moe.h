@@ -196,7 +196,10 @@ moe_status moe_route_noalloc(const moe_config *cfg, const void *x, const moe_wei
  *   and are skipped); counts int32 [E]; offsets int32 [E+1] (exclusive prefix
  *   sum, offsets[E] = n*K); perm int32 [n*K] (position -> pair t*K+j, pairs of
  *   one expert in increasing pair order); inv_perm int32 [n*K] (its inverse);
- *   x_perm act_dtype [n*K][d] = x[perm[q] / K], or NULL to skip the gather. */
+ *   x_perm act_dtype [n*K][d] = x[perm[q] / K], or NULL to skip the gather.
+ * From 16,384 pairs on the sort runs over one CTA per SM in two launches,
+ * with its per-CTA counts in the workspace's h region (free at this point of
+ * the forward); the arrays are the same either way. */
 moe_status moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x,
                         int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv_perm,
                         void *x_perm, void *ws, size_t ws_bytes, void *stream);

@@ -139,6 +139,190 @@ dispatch_kernel(const int32_t *__restrict__ topk_idx, int P, int E, int32_t *__r
   }
 }
 
+// ------------------------------------------------------------------ many CTAs
+// For large batches the same sort runs over one CTA per SM, each owning a
+// contiguous range of pairs:
+//   1. dispatch_hist_kernel: counts per expert in each range -> hist[g][e]
+//   2. dispatch_scatter_kernel: every CTA sums hist over all ranges (totals,
+//      hence counts and offsets) and over the ranges before its own (base),
+//      then ranks its pairs as the single-CTA kernel does (earlier warps,
+//      earlier groups, lower lanes) from offsets[e] + base[e]
+// so every pair lands where the single-CTA kernel puts it.  The scatter
+// kernel starts early (programmatic dependent launch) and builds its own
+// per-warp counts while the first kernel finishes.
+
+constexpr int DM_THREADS = 1024;
+constexpr int DM_WARPS = DM_THREADS / 32;
+
+// Per-warp counts of this CTA's range (hist: [DM_WARPS][E] in shared memory,
+// zeroed by the caller); warp w takes the w-th of DM_WARPS equal sub-ranges,
+// whole groups of 32 pairs in pair order.
+__device__ __forceinline__ void range_hist(const int32_t *__restrict__ topk_idx, int beg, int end,
+                                           int E, int *hist, int *status, bool report) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = end - beg;
+  const int chunk = ((n + DM_WARPS - 1) / DM_WARPS + 31) & ~31;
+  const int wb = min(end, beg + w * chunk), we = min(end, wb + chunk);
+  int *my = hist + w * E;
+  for (int base0 = wb; base0 < we; base0 += 32 * DP_PREFETCH) {
+    int ev[DP_PREFETCH];
+#pragma unroll
+    for (int u = 0; u < DP_PREFETCH; ++u) {
+      const int p = base0 + 32 * u + lane;
+      ev[u] = (p < we) ? topk_idx[p] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < DP_PREFETCH; ++u) {
+      const int p = base0 + 32 * u + lane;
+      int e = ev[u];
+      if (p < we && (e < 0 || e >= E)) {
+        if (report) set_status(status, MOE_ERR_BAD_INDEX, p);
+        e = -1;
+      }
+      if (p >= we) e = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+}
+
+__global__ void __launch_bounds__(DM_THREADS)
+dispatch_hist_kernel(const int32_t *__restrict__ topk_idx, int P, int E, int range,
+                     int32_t *__restrict__ hist_out, int *status) {
+  extern __shared__ int smem[];
+  pdl_launch_dependents();
+  int *hist = smem;                                   // [DM_WARPS][E]
+  for (int i = threadIdx.x; i < DM_WARPS * E; i += DM_THREADS) hist[i] = 0;
+  __syncthreads();
+  const int beg = min(P, (int)blockIdx.x * range), end = min(P, beg + range);
+  range_hist(topk_idx, beg, end, E, hist, status, true);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += DM_THREADS) {
+    int t = 0;
+    for (int w = 0; w < DM_WARPS; ++w) t += hist[w * E + e];
+    hist_out[(size_t)blockIdx.x * E + e] = t;
+  }
+}
+
+__global__ void __launch_bounds__(DM_THREADS)
+dispatch_scatter_kernel(const int32_t *__restrict__ topk_idx, int P, int E, int range, int G,
+                        const int32_t *__restrict__ hist_g, int32_t *__restrict__ counts,
+                        int32_t *__restrict__ offsets, int32_t *__restrict__ perm,
+                        int32_t *__restrict__ inv_perm) {
+  extern __shared__ int smem[];
+  int *hist = smem;                                   // [DM_WARPS][E] -> running positions
+  int *part_tot = hist + DM_WARPS * E;                // [DM_THREADS]: partial sums over ranges
+  int *part_bef = part_tot + DM_THREADS;              // [DM_THREADS]: the same, earlier ranges
+  int *start = part_bef + DM_THREADS;                 // [E]: offsets[e] + base of this range
+  __shared__ int warp_sums[DM_WARPS];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < DM_WARPS * E; i += DM_THREADS) hist[i] = 0;
+  __syncthreads();
+  const int beg = min(P, (int)blockIdx.x * range), end = min(P, beg + range);
+  range_hist(topk_idx, beg, end, E, hist, nullptr, false);
+
+  // totals over all ranges and over the ranges before this one: thread t sums
+  // expert t % E over its share of the ranges
+  pdl_wait();
+  {
+    const int parts = DM_THREADS / E;
+    const int t = threadIdx.x, e = t % E, part = t / E;
+    int tot = 0, bef = 0;
+    if (part < parts) {
+      const int per = (G + parts - 1) / parts;
+      const int g0 = part * per, g1 = min(G, g0 + per);
+      for (int g = g0; g < g1; ++g) {
+        const int c = hist_g[(size_t)g * E + e];
+        tot += c;
+        bef += (g < (int)blockIdx.x) ? c : 0;
+      }
+    }
+    part_tot[t] = tot;
+    part_bef[t] = bef;
+  }
+  __syncthreads();
+  {
+    // exclusive scan of the totals over experts (E <= 256 <= DM_THREADS)
+    const int e = threadIdx.x, parts = DM_THREADS / E;
+    int v = 0, bef = 0;
+    if (e < E)
+      for (int q = 0; q < parts; ++q) {
+        v += part_tot[q * E + e];
+        bef += part_bef[q * E + e];
+      }
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) warp_sums[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+      const int sv = warp_sums[lane];
+      int si = sv;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, si, o);
+        if (lane >= o) si += u;
+      }
+      warp_sums[lane] = si - sv;
+    }
+    __syncthreads();
+    const int excl = incl - v + warp_sums[w];
+    if (e < E) {
+      start[e] = excl + bef;
+      if (blockIdx.x == 0) {
+        counts[e] = v;
+        offsets[e] = excl;
+        if (e == E - 1) offsets[E] = excl + v;
+      }
+    }
+  }
+  __syncthreads();
+  // per-warp start positions: the range's start plus earlier warps' pairs
+  for (int e = threadIdx.x; e < E; e += DM_THREADS) {
+    int run = start[e];
+    for (int ww = 0; ww < DM_WARPS; ++ww) {
+      const int c = hist[ww * E + e];
+      hist[ww * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  const int n = end - beg;
+  const int chunk = ((n + DM_WARPS - 1) / DM_WARPS + 31) & ~31;
+  const int wb = min(end, beg + w * chunk), we = min(end, wb + chunk);
+  int *my = hist + w * E;
+  for (int base0 = wb; base0 < we; base0 += 32 * DP_PREFETCH) {
+    int ev[DP_PREFETCH];
+#pragma unroll
+    for (int u = 0; u < DP_PREFETCH; ++u) {
+      const int p = base0 + 32 * u + lane;
+      ev[u] = (p < we) ? topk_idx[p] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < DP_PREFETCH; ++u) {
+      const int p = base0 + 32 * u + lane;
+      int e = ev[u];
+      if (e >= E || e < 0 || p >= we) e = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      int pos = 0;
+      if (e >= 0) pos = my[e] + __popc(peers & lanemask_lt());
+      __syncwarp();
+      if (e >= 0) {
+        perm[pos] = p;
+        inv_perm[p] = pos;
+        if (lane == __ffs(peers) - 1) my[e] += __popc(peers);
+      } else if (p < we) {
+        inv_perm[p] = -1;
+      }
+      __syncwarp();
+    }
+  }
+}
+
 // x_perm[q] = x[perm[q] / k], 16-byte vectors; one row per CTA iteration so
 // the source row is resolved once per row.  perm entries outside [0, P) are
 // reported and their row is zero-filled.
@@ -160,7 +344,22 @@ gather_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ perm, int
 
 cudaError_t launch_dispatch(int P, int E, const int32_t *topk_idx, int32_t *counts,
                             int32_t *offsets, int32_t *perm, int32_t *inv_perm, int *status,
-                            cudaStream_t s) {
+                            cudaStream_t s, void *scratch, size_t scratch_bytes) {
+  // many CTAs once there is enough to share out and the scratch holds hist + base
+  const int G = num_sms();
+  const size_t need = (size_t)G * E * sizeof(int32_t);
+  if (P >= kDispatchManyMinPairs && scratch != nullptr && scratch_bytes >= need) {
+    int32_t *hist = static_cast<int32_t *>(scratch);
+    const int range = (P + G - 1) / G;
+    const size_t smem1 = (size_t)DM_WARPS * E * sizeof(int);
+    dispatch_hist_kernel<<<G, DM_THREADS, smem1, s>>>(topk_idx, P, E, range, hist, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t smem2 = smem1 + (2 * (size_t)DM_THREADS + E) * sizeof(int);
+    return launch_pdl(dispatch_scatter_kernel, dim3((unsigned)G), dim3(DM_THREADS), smem2, s,
+                      topk_idx, P, E, range, G, (const int32_t *)hist, counts, offsets, perm,
+                      inv_perm);
+  }
   const size_t smem = (size_t)(DP_WARPS + 1) * E * sizeof(int);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(dispatch_kernel,

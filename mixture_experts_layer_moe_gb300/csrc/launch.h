@@ -53,9 +53,13 @@ cudaError_t launch_route_stats(const moe_config &c, const float *probs, const in
                                cudaStream_t s);
 
 // Stable counting sort of P pairs by expert (one CTA).
+// From kDispatchManyMinPairs pairs on, the sort runs over one CTA per SM (two
+// launches) when scratch holds SMs * E int32 (per-range counts); otherwise one
+// CTA.  Both give the same arrays.
+constexpr int kDispatchManyMinPairs = 16384;
 cudaError_t launch_dispatch(int P, int E, const int32_t *topk_idx, int32_t *counts,
                             int32_t *offsets, int32_t *perm, int32_t *inv_perm, int *status,
-                            cudaStream_t s);
+                            cudaStream_t s, void *scratch = nullptr, size_t scratch_bytes = 0);
 
 // x_perm[q] = x[perm[q] / k]; rows of row_bytes (multiple of 16).
 cudaError_t launch_gather(const void *x, const int32_t *perm, int P, int k, int n,

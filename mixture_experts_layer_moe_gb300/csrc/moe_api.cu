@@ -408,7 +408,8 @@ moe_status moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const vo
   const int P = c.n * c.top_k;
   cudaStream_t s = as_stream(stream);
   MOE_TRY(cuda_status(
-      launch_dispatch(P, c.n_experts, topk_idx, counts, offsets, perm, inv_perm, status, s)));
+      launch_dispatch(P, c.n_experts, topk_idx, counts, offsets, perm, inv_perm, status, s,
+                      at<void>(ws, L.h), (size_t)P * c.d_ff * h_size(c))));
   if (x_perm != nullptr)
     MOE_TRY(cuda_status(launch_gather(x, perm, P, c.top_k, c.n, (int64_t)c.d * act_size(c),
                                       x_perm, status, s)));
@@ -481,8 +482,10 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
   MOE_TRY(cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits), topk_idx,
                                    gates, nullptr, status, s)));
   stage(MOE_STAGE_DISPATCH, (decode || mx_tc) ? 1 : 2);
+  // (the h buffer is free until the FFN: scratch for a many-CTA sort)
   MOE_TRY(cuda_status(launch_dispatch(P, c.n_experts, topk_idx, at<int32_t>(ws, L.counts), offsets,
-                                      perm, inv_perm, status, s)));
+                                      perm, inv_perm, status, s, at<void>(ws, L.h),
+                                      (size_t)P * c.d_ff * h_size(c))));
   if (decode) {
     // small batch: the FFN reads x rows through perm, no x_perm copy
     stage(MOE_STAGE_FFN_UP, 2);

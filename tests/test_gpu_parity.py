@@ -203,6 +203,43 @@ def test_dispatch_all_to_one_expert(lib):
     assert perm.tolist() == list(range(n))
 
 
+@pytest.mark.parametrize("n,E,k,skew", [(40001, 64, 1, "one"), (20011, 256, 8, "zipf"),
+                                        (16385, 3, 1, "zipf"), (65536, 32, 4, "empty_half")])
+def test_dispatch_many_ctas(lib, n, E, k, skew):
+    """From 16,384 pairs on the sort runs over many CTAs: same arrays as the
+    oracle's stable sort, with ragged ranges, heavy skew and empty experts."""
+    g = torch.Generator().manual_seed(n + E)
+    if skew == "one":
+        idx = torch.full((n, k), E // 3)
+    elif skew == "zipf":
+        w = 1.0 / torch.arange(1, E + 1, dtype=torch.float64) ** 1.2
+        idx = torch.multinomial(w.expand(n, E), k, replacement=False, generator=g)
+    else:
+        logits = torch.randn(n, E, generator=g, dtype=torch.float64)
+        logits[:, E // 2:] = -1e9
+        idx = O.topk_select(logits, k)
+    st, counts, offsets, perm, inv, _ = _dispatch(lib, _cfg(n, E, k), idx)
+    assert st[0] == 0
+    d = O.dispatch_arrays(idx, E)
+    assert torch.equal(counts.long(), d["counts"])
+    assert torch.equal(offsets.long(), d["offsets"])
+    assert torch.equal(perm.long(), d["perm"])
+    assert torch.equal(inv.long(), d["inv_perm"])
+
+
+def test_dispatch_many_ctas_bad_index(lib):
+    n, E = 30000, 16
+    idx = (torch.arange(n) % E).view(n, 1).clone()
+    idx[12345, 0] = E + 4
+    st, counts, offsets, perm, inv, _ = _dispatch(lib, _cfg(n, E, 1), idx)
+    assert st == (5, 12345)
+    assert counts.sum().item() == n - 1
+    assert inv[12345].item() == -1
+    good = torch.ones(n, dtype=torch.bool)
+    good[12345] = False
+    assert sorted(perm[: n - 1].tolist()) == torch.arange(n)[good].tolist()
+
+
 def test_dispatch_bad_index_reported(lib):
     """An out-of-range expert id is reported in the status word and skipped."""
     idx = torch.tensor([[0], [1], [9], [2]])
