@@ -8,24 +8,36 @@
 // v1.0 format).
 //
 // A tile computes D[w][t] = sum_k W[w][k] * X[t][k] for 128 weight rows w (MMA
-// M, the TMEM lanes) and 128 tokens t of one expert's segment (MMA N), i.e. the
-// transposed output tile.  The token rows (f16 copies of the activations) come
-// by TMA into a 128-byte-swizzled shared-memory tile, the B operand.  The
-// weights never touch shared memory in f16: four transform warps read the
-// packed codes (TMA, 32-byte swizzle), convert each row's 64 codes of a k-block
-// with cvt.rn.f16x2.e2m1x2, multiply by the block's E8M0 scale as an f16 pair
+// M, the TMEM lanes) and up to 256 tokens t of one expert's segment (MMA N),
+// i.e. the transposed output tile.  N is the segment's remaining token count
+// rounded up to 16, so a small expert costs a small MMA instead of a padded
+// one.  The token rows (f16 copies of the activations) come by TMA, in boxes of
+// 64 rows and only as many boxes as the tile has tokens, into a
+// 128-byte-swizzled shared-memory tile, the B operand.  The weights never
+// touch shared memory in f16: four transform warps read the packed codes (TMA,
+// 32-byte swizzle), convert each row's 64 codes of a k-block with
+// cvt.rn.f16x2.e2m1x2, multiply by the block's E8M0 scale as an f16 pair
 // (exact for scale bytes 113..142; others are reported as MOE_ERR_RANGE) and
-// write them with tcgen05.st into the A stage in tensor memory (lane = weight
-// row, 32-bit column c = k-elements 2c and 2c + 1).  Shared memory carries only
-// the TMA traffic and the code reads, not a dequantised tile written and read
-// back.  Used for the single-matrix projections (the down projection, and a
-// ReLU up projection); the SwiGLU up projection, whose tiles would cover only
-// 64 output columns here, stays on the shared-memory-transform kernel of
-// gemm_tc.cu, which measured faster for it.
+// write them with tcgen05.st into an A stage in tensor memory (lane = weight
+// row, 32-bit column c = k-elements 2c and 2c + 1).
+//
+// 256-token MMAs keep the tensor pipe busy between the per-k-block barrier
+// waits of the issuing thread (measured: 128-token MMAs with the same waits
+// ran at about 60% of the pipe's rate, 256-token ones at its full rate).  The
+// 256-column accumulator leaves no room for a second one, so the epilogue
+// drains it into registers (bf16 pairs), releases it to the next tile's MMAs
+// and only then writes to global memory.
+//
+// Epilogues: 0 y = X W^T; 1 h = relu(X W^T); 2 SwiGLU over 64 output columns,
+// h = silu(X W1^T) * (X W3^T): in each 32-lane quarter of the tile, lanes
+// 0..15 hold 16 rows of W1 and lanes 16..31 the same 16 rows of W3, so one
+// shuffle between the half-warps brings each gate value next to its up value
+// (each half then finishes half of the tokens).
 //
 // Warp roles (persistent, one CTA per SM): 0 TMA producer, 1 MMA issuer and
-// TMEM owner, 2-5 epilogue (TMEM -> registers -> global), 6-9 transform.  TMEM:
-// two 128-column accumulators, then GS stages of 32 columns of A.
+// TMEM owner, 2-9 epilogue (two per TMEM lane quarter, one per 128-token
+// half), 10-13 transform.  TMEM: the 256-column accumulator, then GS stages of
+// 32 columns of A.
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -34,22 +46,27 @@ namespace moe {
 namespace {
 
 constexpr int GM = 128;                         // weight rows per tile (MMA M)
-constexpr int GN = 128;                         // tokens per tile (MMA N)
+constexpr int GN = 256;                         // tokens per tile at most (MMA N)
 constexpr int GK = 64;                          // k-block
-constexpr int GS = 8;                           // pipeline stages
-constexpr int G_B_BYTES = GN * GK * 2;          // token tile: 16 KB
+constexpr int GS = 5;                           // pipeline stages
+constexpr int G_BOX = 64;                       // token rows per TMA box
+constexpr int G_BOX_BYTES = G_BOX * GK * 2;     // 8 KB
+constexpr int G_B_BYTES = GN * GK * 2;          // token tile: 32 KB
 constexpr int G_C_BYTES = GM * GK / 2;          // codes of the k-block: 4 KB
-constexpr int G_STAGE = G_B_BYTES + G_C_BYTES;  // 20 KB
-constexpr int G_THREADS = 320;
-constexpr uint32_t G_TMEM_COLS = 512;
-constexpr uint32_t G_A_COL0 = 2 * GN;           // A stages after the two accumulators
-constexpr int G_MAX_E = 256;
+constexpr int G_STAGE = G_B_BYTES + G_C_BYTES;  // 36 KB
 constexpr int G_XFORM = 4;                      // transform warps
-constexpr int G_EPI = 4;                        // epilogue warps
+constexpr int G_EPI = 8;                        // epilogue warps
+constexpr int G_THREADS = 32 * (2 + G_EPI + G_XFORM);
+constexpr uint32_t G_TMEM_COLS = 512;
+constexpr uint32_t G_A_COL0 = GN;               // A stages after the accumulator
+constexpr int G_MAX_E = 256;
+constexpr int G_BAR_XFORM = 3;                  // named barrier: transform agreement
+static_assert(G_A_COL0 + GS * (GK / 2) <= G_TMEM_COLS, "tensor memory columns");
+static_assert(G_STAGE % 1024 == 0, "stage alignment");
 
 struct GShared {
   uint64_t full[GS], empty[GS], aready[GS];
-  uint64_t tfull[2], tempty[2];
+  uint64_t tfull, tempty;
   uint64_t drain;
   uint32_t tmem_base;
   int abort, failed_on_entry, num_tiles;
@@ -60,7 +77,8 @@ struct GShared {
 struct GArgs {
   const int32_t *offsets;
   int num_experts, rows, K, N;
-  const uint8_t *S;          // E8M0 scales [E][N][K/32]
+  const uint8_t *S;          // E8M0 scales [E][N][K/32] (W1's for SwiGLU)
+  const uint8_t *S3;         // SwiGLU: W3's scales (else S)
   __nv_bfloat16 *out;        // [rows][N]
   uint16_t *out16;           // f16 copy of out, or nullptr
   int *status;
@@ -159,9 +177,19 @@ __device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
       : "memory");
   return r != 0;
 }
+// silu(a) * b; the quotient by the fast reciprocal (h is rounded to bf16)
+__device__ __forceinline__ float silu_mul(float a, float b) {
+  return __fdividef(a, 1.f + __expf(-a)) * b;
+}
 
-__device__ __forceinline__ uint16_t f16_bits_of_bf16(__nv_bfloat16 b) {
-  float v = fminf(fmaxf(__bfloat162float(b), -65504.f), 65504.f);
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// bf16 bits -> f16 bits (clamped to the f16 range)
+__device__ __forceinline__ uint16_t f16_bits_of_bf16(uint32_t b) {
+  const float v = fminf(fmaxf(__uint_as_float(b << 16), -65504.f), 65504.f);
   const __half h = __float2half_rn(v);
   return *reinterpret_cast<const uint16_t *>(&h);
 }
@@ -172,12 +200,11 @@ __host__ __device__ inline size_t g_scale_pitch(int K) {
 __host__ __device__ inline size_t g_scale_off() { return (size_t)GS * G_STAGE; }
 size_t g_dyn_smem(int K) { return 1024 + g_scale_off() + 2 * g_scale_pitch(K); }
 
-// EPI 0: y = X W^T; EPI 1: h = relu(X W^T).  128 output columns per tile.
 template <int EPI>
 __global__ void __launch_bounds__(G_THREADS, 1)
 gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-               GArgs args) {
-  constexpr int N_OUT = GM;                         // output columns per tile
+               const __grid_constant__ CUtensorMap tmW3, GArgs args) {
+  constexpr int N_OUT = (EPI == 2) ? GM / 2 : GM;   // output columns per tile
   extern __shared__ uint8_t dyn_smem[];
   __shared__ GShared sh;
   uint8_t *smem = dyn_smem + ((1024 - (tc::smem_u32(dyn_smem) & 1023)) & 1023);
@@ -201,10 +228,8 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       tc::mbar_init(&sh.empty[s], 1 + G_XFORM);   // the MMAs (token tile), the transform (codes)
       tc::mbar_init(&sh.aready[s], G_XFORM);
     }
-    for (int a = 0; a < 2; ++a) {
-      tc::mbar_init(&sh.tfull[a], 1);
-      tc::mbar_init(&sh.tempty[a], G_EPI);
-    }
+    tc::mbar_init(&sh.tfull, 1);
+    tc::mbar_init(&sh.tempty, G_EPI);
     tc::mbar_init(&sh.drain, 1);
     tc::fence_mbar_init();
   }
@@ -253,9 +278,11 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer: token tile + the k-block's codes
+      // ---------------- TMA producer: the tile's token boxes + the k-block's
+      // codes of weight rows 0..63 and 64..127 (W1 and W3 rows for SwiGLU)
       tc::prefetch_tmap(&tmX);
       tc::prefetch_tmap(&tmW);
+      if (EPI == 2) tc::prefetch_tmap(&tmW3);
       int stage = 0;
       uint32_t phase = 0;
       int last_phase[GS];
@@ -263,14 +290,24 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       for (int s = 0; s < GS; ++s) last_phase[s] = -1;
       for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
         const GTile tl = g_decode(sh, E, t);
-        const int wrow = tl.n_idx * N_OUT;
+        const int ntok = min(GN, tl.seg_end - tl.row0);
+        const int nbox = (ntok + G_BOX - 1) / G_BOX;
+        const int r_lo = tl.n_idx * N_OUT;
+        const int r_hi = (EPI == 2) ? r_lo : r_lo + GM / 2;
+        const bool hi_ok = r_hi < args.N;            // else rows 64..127 are all past N
         for (int kb = 0; kb < KB; ++kb) {
           if (!tc::mbar_wait(&sh.empty[stage], phase ^ 1u, abort)) break;
           uint8_t *sb = smem + stage * G_STAGE;
           uint8_t *sc = sb + G_B_BYTES;
-          tc::mbar_arrive_expect_tx(&sh.full[stage], G_STAGE);
-          tc::tma_load_2d(&tmX, &sh.full[stage], sb, kb * GK, tl.row0);
-          tc::tma_load_3d(&tmW, &sh.full[stage], sc, kb * (GK / 2), wrow, tl.e);
+          tc::mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)(nbox * G_BOX_BYTES + G_C_BYTES /
+                                                                (hi_ok ? 1 : 2)));
+          for (int j = 0; j < nbox; ++j)
+            tc::tma_load_2d(&tmX, &sh.full[stage], sb + j * G_BOX_BYTES, kb * GK,
+                            tl.row0 + j * G_BOX);
+          tc::tma_load_3d(&tmW, &sh.full[stage], sc, kb * (GK / 2), r_lo, tl.e);
+          if (hi_ok)
+            tc::tma_load_3d(EPI == 2 ? &tmW3 : &tmW, &sh.full[stage], sc + G_C_BYTES / 2,
+                            kb * (GK / 2), r_hi, tl.e);
           last_phase[stage] = (int)phase;
           if (++stage == GS) { stage = 0; phase ^= 1u; }
         }
@@ -283,17 +320,17 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------- MMA issuer: D(acc) = A(TMEM, weights) x B(smem, tokens)^T
-      constexpr uint32_t idesc = tc::idesc_f16_f32(GM, GN);
+      // ---------------- MMA issuer: D = A(TMEM, weights) x B(smem, tokens)^T
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok && !*abort; t += gridDim.x, ++local) {
-        const int acc = local & 1;
-        if (!tc::mbar_wait(&sh.tempty[acc], ((local >> 1) & 1) ^ 1u, abort)) { ok = false; break; }
+        const GTile tl = g_decode(sh, E, t);
+        const int ntok = min(GN, tl.seg_end - tl.row0);
+        const uint32_t idesc = tc::idesc_f16_f32(GM, (ntok + 15) & ~15);
+        if (!tc::mbar_wait(&sh.tempty, (local & 1) ^ 1u, abort)) { ok = false; break; }
         tc::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * GN);
         for (int kb = 0; kb < KB; ++kb) {
           if (!tc::mbar_wait(&sh.full[stage], phase, abort)) { ok = false; break; }
           if (!tc::mbar_wait(&sh.aready[stage], phase, abort)) { ok = false; break; }
@@ -302,13 +339,13 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
           const uint32_t a_tmem = tmem_base + G_A_COL0 + (uint32_t)(stage * (GK / 2));
 #pragma unroll
           for (int k = 0; k < GK / 16; ++k)
-            mma_ta(d_tmem, a_tmem + k * 8, tc::smem_desc_sw128(sb + k * 32), idesc,
+            mma_ta(tmem_base, a_tmem + k * 8, tc::smem_desc_sw128(sb + k * 32), idesc,
                    (kb != 0 || k != 0) ? 1u : 0u);
           tc::mma_commit(&sh.empty[stage]);
           if (++stage == GS) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc::mma_commit(&sh.tfull[acc]);
+        tc::mma_commit(&sh.tfull);
       }
       if (*abort) {
         tc::mma_commit(&sh.drain);
@@ -316,44 +353,85 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       }
     }
   } else if (warp < 2 + G_EPI) {
-    // ---------------- epilogue: warp w drains TMEM lanes 32*(w%4) .. +31; the
-    // thread of weight row j writes column j of 32 tokens per chunk (a warp's
-    // stores of one token are 64 contiguous bytes)
+    // ---------------- epilogue: warp w drains TMEM lanes 32*(w%4) .. +31 over
+    // one 128-token half of the tile, 32 tokens per chunk, into bf16 pairs held
+    // in registers; the accumulator is then released and each thread writes
+    // its output column for its tokens (a warp's stores of one token are 64
+    // contiguous bytes, 2 x 32 for SwiGLU)
     const int quarter = warp & 3;
-    const int j = quarter * 32 + lane;
+    const int half = (warp - 2) >> 2;
+    const int tok_half = half * (GN / 2);
+    const bool low = lane < 16;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
     int local = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
       const GTile tl = g_decode(sh, E, t);
-      const int acc = local & 1;
-      const bool ok = tc::mbar_wait(&sh.tfull[acc], (local >> 1) & 1, abort);
+      const int ntok = min(GN, tl.seg_end - tl.row0);
+      const bool ok = tc::mbar_wait(&sh.tfull, local & 1, abort);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc::tc_fence_after();
-      const int col = tl.n_idx * N_OUT + j;
-      const bool col_ok = col < args.N;
-#pragma unroll 1
-      for (int c = 0; c < GN / 32; ++c) {
-        uint32_t a[32];
-        tc::tmem_ld32(lane_base + (uint32_t)(acc * GN) + c * 32, a);
-        tc::tmem_ld_wait();
-        const int tok0 = tl.row0 + c * 32;
-        if (col_ok) {
+      const int my_end = min(ntok, tok_half + GN / 2);   // this warp's tokens: [tok_half, my_end)
+      uint32_t packed[4][16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int tok = tok0 + i;
-            if (tok < tl.seg_end) {
-              float v = __uint_as_float(a[i]);
-              if constexpr (EPI == 1) v = fmaxf(v, 0.f);
-              const __nv_bfloat16 hb = __float2bfloat16_rn(v);
-              args.out[(size_t)tok * args.N + col] = hb;
-              if (args.out16) args.out16[(size_t)tok * args.N + col] = f16_bits_of_bf16(hb);
+      for (int c = 0; c < 4; ++c) {
+        const int col0 = tok_half + c * 32;
+        if (col0 < my_end) {
+          uint32_t a[32];
+          tc::tmem_ld32(lane_base + (uint32_t)col0, a);
+          tc::tmem_ld_wait();
+          if constexpr (EPI == 2) {
+            // low lane: gate values g[0..31] of its row; high lane: up values
+            // u[0..31] of the same row.  The low lane takes tokens 0..15, the
+            // high lane tokens 16..31.
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+              const uint32_t s0 = __shfl_xor_sync(0xffffffffu, low ? a[16 + i] : a[i], 16);
+              const uint32_t s1 = __shfl_xor_sync(0xffffffffu, low ? a[17 + i] : a[i + 1], 16);
+              const float g0 = __uint_as_float(low ? a[i] : s0);
+              const float u0 = __uint_as_float(low ? s0 : a[16 + i]);
+              const float g1 = __uint_as_float(low ? a[i + 1] : s1);
+              const float u1 = __uint_as_float(low ? s1 : a[17 + i]);
+              packed[c][i >> 1] = pack_bf16x2(silu_mul(g0, u0), silu_mul(g1, u1));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float v0 = __uint_as_float(a[2 * i]), v1 = __uint_as_float(a[2 * i + 1]);
+              if constexpr (EPI == 1) {
+                v0 = fmaxf(v0, 0.f);
+                v1 = fmaxf(v1, 0.f);
+              }
+              packed[c][i] = pack_bf16x2(v0, v1);
             }
           }
         }
       }
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sh.tempty[acc]);
+      if (lane == 0) tc::mbar_arrive(&sh.tempty);
+      constexpr int PER = (EPI == 2) ? 16 : 32;         // tokens per thread per chunk
+      const int col = (EPI == 2) ? tl.n_idx * N_OUT + quarter * 16 + (lane & 15)
+                                 : tl.n_idx * N_OUT + quarter * 32 + lane;
+      const int tsub = (EPI == 2 && !low) ? 16 : 0;
+      if (col < args.N) {
+        uint16_t *o = reinterpret_cast<uint16_t *>(args.out);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (tok_half + c * 32 < my_end) {
+            const int tok0 = tl.row0 + tok_half + c * 32 + tsub;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+              const int tok = tok0 + i;
+              if (tok < tl.seg_end) {
+                const uint32_t hb = (i & 1) ? (packed[c][i >> 1] >> 16)
+                                            : (packed[c][i >> 1] & 0xffffu);
+                o[(size_t)tok * args.N + col] = (uint16_t)hb;
+                if (args.out16) args.out16[(size_t)tok * args.N + col] = f16_bits_of_bf16(hb);
+              }
+            }
+          }
+        }
+      }
     }
   } else {
     // ---------------- transform: warp w writes TMEM lanes 32*(w%4) .. +31, one
@@ -361,41 +439,52 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     // of two buffers while the previous tile runs.  The codes arrive with a
     // 32-byte swizzle: 16-byte half c of row r sits at c ^ ((r >> 2) & 1).
     const int quarter = warp & 3;
+    // this thread's TMEM lane and the row of the codes / scales tile feeding it
+    // (SwiGLU: lanes 16..31 of a quarter take W3 rows, held in tile rows 64..127)
     const int r = quarter * 32 + lane;
+    const int crow = (EPI == 2) ? (lane < 16 ? quarter * 16 + lane : GM / 2 + quarter * 16 + lane - 16)
+                                : r;
     const int tt = threadIdx.x - 32 * (2 + G_EPI);     // 0 .. 127
     constexpr int XT = 32 * G_XFORM;
     const size_t spitch = g_scale_pitch(args.K);
     uint8_t *scale_buf[2] = {smem + g_scale_off(), smem + g_scale_off() + spitch};
+    // scales of tile rows 0..63 and 64..127 (rows past N are left unset: their
+    // codes are zero-filled by TMA and their columns are never stored)
     auto fetch_scales = [&](int t, int b) {
       const GTile tl = g_decode(sh, E, t);
-      const int wrow = tl.n_idx * N_OUT;
-      const int rows = min(GM, args.N - wrow);
-      const size_t bytes = (size_t)rows * KBLK;       // a multiple of 16
-      const uint8_t *src = args.S + ((size_t)tl.e * args.N + wrow) * KBLK;
-      for (size_t o = (size_t)tt * 16; o < bytes; o += XT * 16)
-        cp_async16(scale_buf[b] + o, src + o);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int wrow = (EPI == 2) ? tl.n_idx * N_OUT : tl.n_idx * N_OUT + h * (GM / 2);
+        const uint8_t *S = (EPI == 2 && h == 1) ? args.S3 : args.S;
+        const int rows = max(0, min(GM / 2, args.N - wrow));
+        const size_t bytes = (size_t)rows * KBLK;       // a multiple of 16
+        const uint8_t *src = S + ((size_t)tl.e * args.N + wrow) * KBLK;
+        uint8_t *dst = scale_buf[b] + (size_t)h * (GM / 2) * KBLK;
+        for (size_t o = (size_t)tt * 16; o < bytes; o += XT * 16) cp_async16(dst + o, src + o);
+      }
       asm volatile("cp.async.commit_group;" ::: "memory");
     };
     int stage = 0;
     uint32_t phase = 0;
     int buf = 0;
     bool bad_scale = false;
-    const int sw = ((r >> 2) & 1) << 4;
+    const int sw = ((crow >> 2) & 1) << 4;
     const uint32_t a_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + G_A_COL0;
     if (blockIdx.x < num_tiles) fetch_scales(blockIdx.x, 0);
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, buf ^= 1) {
       asm volatile("cp.async.wait_group 0;" ::: "memory");
       // this tile's scales are in; the transform warps also agree here on
       // stopping (a warp whose wait ran out has raised *abort)
-      if (bar_or(3, XT, *abort != 0)) break;
+      if (bar_or(G_BAR_XFORM, XT, *abort != 0)) break;
       if (t + (int)gridDim.x < num_tiles) fetch_scales(t + gridDim.x, buf ^ 1);
-      const uint8_t *srow = scale_buf[buf] + (size_t)r * KBLK;
-      const int wrow = g_decode(sh, E, t).n_idx * N_OUT;
-      const bool row_ok = wrow + r < args.N;          // else: zero row
+      const uint8_t *srow = scale_buf[buf] + (size_t)crow * KBLK;
+      const GTile tl = g_decode(sh, E, t);
+      const int wrow = tl.n_idx * N_OUT + (crow & (GM / 2 - 1)) + (EPI == 2 ? 0 : (crow & (GM / 2)));
+      const bool row_ok = wrow < args.N;              // else: zero row
       for (int kb = 0; kb < KB; ++kb) {
         const bool ok = tc::mbar_wait(&sh.full[stage], phase, abort);
         if (!__all_sync(0xffffffffu, ok)) break;
-        const uint8_t *codes = smem + stage * G_STAGE + G_B_BYTES + r * 32;
+        const uint8_t *codes = smem + stage * G_STAGE + G_B_BYTES + crow * 32;
         uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
         if (row_ok) {
           c0 = *reinterpret_cast<const uint4 *>(codes + sw);
@@ -457,18 +546,25 @@ cudaError_t launch_mx(const GemmStage &g, int *status, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     smem_set = smem;
   }
-  CUtensorMap mX, mW;
+  CUtensorMap mX, mW, mW3;
   const uint64_t dX[2] = {(uint64_t)g.K, (uint64_t)g.rows};
-  const uint32_t bX[2] = {GK, GN};
+  const uint32_t bX[2] = {GK, G_BOX};
   if (!make_tensor_map(&mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.A, 2, dX, bX,
                        CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  // packed codes: [E][N][K/2] bytes, boxes of 32 bytes (one k-block) x 128 rows
+  // packed codes: [E][N][K/2] bytes, boxes of 32 bytes (one k-block) x 64 rows
   const uint64_t dC[3] = {(uint64_t)g.K / 2, (uint64_t)g.N, (uint64_t)g.num_experts};
-  const uint32_t bC[3] = {GK / 2, (uint32_t)GM, 1};
+  const uint32_t bC[3] = {GK / 2, (uint32_t)(GM / 2), 1};
   if (!make_tensor_map(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.B, 3, dC, bC,
                        CU_TENSOR_MAP_SWIZZLE_32B))
     return cudaErrorInvalidValue;
+  if (EPI == 2) {
+    if (!make_tensor_map(&mW3, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.B3, 3, dC, bC,
+                         CU_TENSOR_MAP_SWIZZLE_32B))
+      return cudaErrorInvalidValue;
+  } else {
+    mW3 = mW;
+  }
   GArgs a{};
   a.offsets = g.offsets;
   a.num_experts = g.num_experts;
@@ -476,23 +572,30 @@ cudaError_t launch_mx(const GemmStage &g, int *status, cudaStream_t s) {
   a.K = g.K;
   a.N = g.N;
   a.S = g.SB;
+  a.S3 = (EPI == 2) ? g.SB3 : g.SB;
   a.out = static_cast<__nv_bfloat16 *>(g.out);
   a.out16 = static_cast<uint16_t *>(g.out16);
   a.status = status;
-  return launch_pdl(gemm_mx_kernel<EPI>, dim3(num_sms()), dim3(G_THREADS), smem, s, mX, mW, a);
+  return launch_pdl(gemm_mx_kernel<EPI>, dim3(num_sms()), dim3(G_THREADS), smem, s, mX, mW, mW3,
+                    a);
 }
 
 }  // namespace
 
+// Shapes only: the callers pass 16-byte-aligned code and scale arrays.
 bool gemm_mx_supported(const GemmStage &g) {
   return g.rows > 0 && tensor_maps_available() && g.b_dtype == MOE_MXFP4 && g.a_dtype == kF16 &&
-         g.out_dtype == MOE_BF16 && (g.epi == 0 || g.epi == 1) && g.offsets != nullptr &&
-         g.num_experts <= G_MAX_E && g.K % GK == 0 && g.N % 32 == 0 &&
+         g.out_dtype == MOE_BF16 && (g.epi == 0 || g.epi == 1 || g.epi == 2) &&
+         g.offsets != nullptr && g.num_experts <= G_MAX_E && g.K % GK == 0 && g.N % 32 == 0 &&
          g_dyn_smem(g.K) + sizeof(GShared) <= 227 * 1024;
 }
 
 cudaError_t launch_gemm_mx(const GemmStage &g, int *status, cudaStream_t s) {
-  return g.epi == 1 ? launch_mx<1>(g, status, s) : launch_mx<0>(g, status, s);
+  switch (g.epi) {
+    case 1: return launch_mx<1>(g, status, s);
+    case 2: return launch_mx<2>(g, status, s);
+    default: return launch_mx<0>(g, status, s);
+  }
 }
 
 }  // namespace moe

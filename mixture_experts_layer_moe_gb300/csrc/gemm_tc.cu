@@ -626,7 +626,8 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
 bool gemm_tc_supported(const GemmStage &g) {
   if (g.rows <= 0 || !tensor_maps_available()) return false;
   if (g.b_dtype == MOE_MXFP4) {
-    if (g.epi != 2) return gemm_mx_supported(g);
+    if (gemm_mx_supported(g)) return true;
+    if (g.epi != 2) return false;
     // f16 activations, MXFP4 weights; all scale buffers must fit in shared memory
     return g.a_dtype == kF16 && g.out_dtype == MOE_BF16 && g.K % 64 == 0 && g.N % 32 == 0 &&
            mx_dyn_smem(g.K) + sizeof(TcShared) <= 227 * 1024;
@@ -637,11 +638,11 @@ bool gemm_tc_supported(const GemmStage &g) {
 }
 
 cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s) {
-  // MXFP4: the SwiGLU up projection on this file's kernel (dequantised tile in
-  // shared memory), the single-matrix projections with the weights in tensor
-  // memory (gemm_mx.cu)
+  // MXFP4: the weights-in-tensor-memory kernel (gemm_mx.cu) where its shared
+  // memory fits; else, for SwiGLU, this file's kernel with the dequantised
+  // tile in shared memory
   if (g.b_dtype == MOE_MXFP4)
-    return g.epi == 2 ? launch_epi<2, true>(g, status, s) : launch_gemm_mx(g, status, s);
+    return gemm_mx_supported(g) ? launch_gemm_mx(g, status, s) : launch_epi<2, true>(g, status, s);
   switch (g.epi) {
     case 0: return launch_epi<0, false>(g, status, s);
     case 1: return launch_epi<1, false>(g, status, s);

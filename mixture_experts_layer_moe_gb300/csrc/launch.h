@@ -103,7 +103,7 @@ cudaError_t launch_gemm_simt(const GemmStage &g, int *status, cudaStream_t s);
 bool gemm_tc_supported(const GemmStage &g);
 cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s);
 // MXFP4 grouped GEMM with the dequantised weights as the tcgen05 A operand in
-// tensor memory (f16 activation copies in, bf16 out; epi 0 or 1).
+// tensor memory (f16 activation copies in, bf16 out; epi 0, 1 or 2).
 bool gemm_mx_supported(const GemmStage &g);
 cudaError_t launch_gemm_mx(const GemmStage &g, int *status, cudaStream_t s);
 

@@ -50,6 +50,11 @@ SMALL = {
     "prefill_zipf_small": C["gptoss_prefill_zipf_mxfp4"].scaled(n=600, d=256, d_ff=320, E=16),
     "prefill_relu_mxfp4_small": C["gptoss_prefill_zipf_mxfp4"].scaled(n=600, d=256, d_ff=320,
                                                                       E=16, act="relu"),
+    # MXFP4 prefill: a down projection whose last 128-row weight tile has 64
+    # rows (d = 192), and k = E so that every expert holds 900 tokens (three
+    # full 256-token tiles and one of 132)
+    "prefill_mx_half_down_tile": C["gptoss_prefill_zipf_mxfp4"].scaled(n=900, d=192, d_ff=320,
+                                                                       E=4),
     "finegrained_small": C["finegrained_shared_bf16"].scaled(n=500, d=256, d_ff=128, E=32,
                                                              d_ff_shared=192),
 }
