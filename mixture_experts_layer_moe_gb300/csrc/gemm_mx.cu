@@ -8,11 +8,10 @@
 // v1.0 format).
 //
 // A tile computes D[w][t] = sum_k W[w][k] * X[t][k] for 128 weight rows w (MMA
-// M, the TMEM lanes) and up to 256 tokens t of one expert's segment (MMA N),
+// M, the TMEM lanes) and up to 128 tokens t of one expert's segment (MMA N),
 // i.e. the transposed output tile.  N is the segment's remaining token count
 // rounded up to 16, so a small expert costs a small MMA instead of a padded
-// one.  The token rows (f16 copies of the activations) come by TMA, in boxes of
-// 64 rows and only as many boxes as the tile has tokens, into a
+// one.  The token rows (f16 copies of the activations) come by TMA into a
 // 128-byte-swizzled shared-memory tile, the B operand.  The weights never
 // touch shared memory in f16: four transform warps read the packed codes (TMA,
 // 32-byte swizzle), convert each row's 64 codes of a k-block with
@@ -21,12 +20,14 @@
 // write them with tcgen05.st into an A stage in tensor memory (lane = weight
 // row, 32-bit column c = k-elements 2c and 2c + 1).
 //
-// 256-token MMAs keep the tensor pipe busy between the per-k-block barrier
-// waits of the issuing thread (measured: 128-token MMAs with the same waits
-// ran at about 60% of the pipe's rate, 256-token ones at its full rate).  The
-// 256-column accumulator leaves no room for a second one, so the epilogue
-// drains it into registers (bf16 pairs), releases it to the next tile's MMAs
-// and only then writes to global memory.
+// Two CTAs share each SM, each with half of its tensor memory: a 128-column
+// accumulator and GS A stages.  One CTA's ring (TMA -> transform -> MMA ->
+// release) is latency-bound; the other CTA's MMAs fill the tensor pipe while
+// it waits (measured on the Zipf-routed prefill, n = 8192: down projection
+// 0.50 ms, against 0.77 ms for one CTA per SM with a double-buffered
+// accumulator and 0.53 ms for one CTA per SM with 256-token tiles).  The single accumulator is drained into registers
+// (bf16 pairs) and released to the next tile's MMAs before the epilogue
+// writes to global memory.
 //
 // Epilogues: 0 y = X W^T; 1 h = relu(X W^T); 2 SwiGLU over 64 output columns,
 // h = silu(X W1^T) * (X W3^T): in each 32-lane quarter of the tile, lanes
@@ -34,10 +35,9 @@
 // shuffle between the half-warps brings each gate value next to its up value
 // (each half then finishes half of the tokens).
 //
-// Warp roles (persistent, one CTA per SM): 0 TMA producer, 1 MMA issuer and
-// TMEM owner, 2-9 epilogue (two per TMEM lane quarter, one per 128-token
-// half), 10-13 transform.  TMEM: the 256-column accumulator, then GS stages of
-// 32 columns of A.
+// Warp roles (persistent, two CTAs per SM): 0 TMA producer, 1 MMA issuer and
+// TMEM owner, 2-5 epilogue (one per TMEM lane quarter), 6-9 transform.  TMEM
+// (256 columns per CTA): the accumulator, then GS stages of 32 columns of A.
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -46,18 +46,19 @@ namespace moe {
 namespace {
 
 constexpr int GM = 128;                         // weight rows per tile (MMA M)
-constexpr int GN = 256;                         // tokens per tile at most (MMA N)
+constexpr int GN = 128;                         // tokens per tile at most (MMA N)
 constexpr int GK = 64;                          // k-block
-constexpr int GS = 5;                           // pipeline stages
-constexpr int G_BOX = 64;                       // token rows per TMA box
-constexpr int G_BOX_BYTES = G_BOX * GK * 2;     // 8 KB
-constexpr int G_B_BYTES = GN * GK * 2;          // token tile: 32 KB
+constexpr int GS = 4;                           // pipeline stages
+constexpr int G_BOX = GN;                       // token rows per TMA box (one box per k-block)
+constexpr int G_BOX_BYTES = G_BOX * GK * 2;     // 16 KB
+constexpr int G_B_BYTES = GN * GK * 2;          // token tile: 16 KB
 constexpr int G_C_BYTES = GM * GK / 2;          // codes of the k-block: 4 KB
-constexpr int G_STAGE = G_B_BYTES + G_C_BYTES;  // 36 KB
+constexpr int G_STAGE = G_B_BYTES + G_C_BYTES;  // 20 KB
 constexpr int G_XFORM = 4;                      // transform warps
-constexpr int G_EPI = 8;                        // epilogue warps
+constexpr int G_EPI = 4;                        // epilogue warps
+constexpr int G_TOK_PER_EPI = GN * 4 / G_EPI;   // tokens an epilogue warp drains
 constexpr int G_THREADS = 32 * (2 + G_EPI + G_XFORM);
-constexpr uint32_t G_TMEM_COLS = 512;
+constexpr uint32_t G_TMEM_COLS = 256;           // two CTAs per SM
 constexpr uint32_t G_A_COL0 = GN;               // A stages after the accumulator
 constexpr int G_MAX_E = 256;
 constexpr int G_BAR_XFORM = 3;                  // named barrier: transform agreement
@@ -162,6 +163,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       : "memory");
 }
 
+// 32 lanes x 16 consecutive 32-bit columns into registers.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -201,7 +214,7 @@ __host__ __device__ inline size_t g_scale_off() { return (size_t)GS * G_STAGE; }
 size_t g_dyn_smem(int K) { return 1024 + g_scale_off() + 2 * g_scale_pitch(K); }
 
 template <int EPI>
-__global__ void __launch_bounds__(G_THREADS, 1)
+__global__ void __launch_bounds__(G_THREADS, 2)
 gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                const __grid_constant__ CUtensorMap tmW3, GArgs args) {
   constexpr int N_OUT = (EPI == 2) ? GM / 2 : GM;   // output columns per tile
@@ -294,13 +307,12 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int nbox = (ntok + G_BOX - 1) / G_BOX;
         const int r_lo = tl.n_idx * N_OUT;
         const int r_hi = (EPI == 2) ? r_lo : r_lo + GM / 2;
-        const bool hi_ok = r_hi < args.N;            // else rows 64..127 are all past N
+        const bool hi_ok = EPI == 2 && r_hi < args.N;  // SwiGLU: the W3 box
         for (int kb = 0; kb < KB; ++kb) {
           if (!tc::mbar_wait(&sh.empty[stage], phase ^ 1u, abort)) break;
           uint8_t *sb = smem + stage * G_STAGE;
           uint8_t *sc = sb + G_B_BYTES;
-          tc::mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)(nbox * G_BOX_BYTES + G_C_BYTES /
-                                                                (hi_ok ? 1 : 2)));
+          tc::mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)(nbox * G_BOX_BYTES + G_C_BYTES));
           for (int j = 0; j < nbox; ++j)
             tc::tma_load_2d(&tmX, &sh.full[stage], sb + j * G_BOX_BYTES, kb * GK,
                             tl.row0 + j * G_BOX);
@@ -360,7 +372,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     // contiguous bytes, 2 x 32 for SwiGLU)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
-    const int tok_half = half * (GN / 2);
+    const int tok_half = half * G_TOK_PER_EPI;
     const bool low = lane < 16;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
     int local = 0;
@@ -370,16 +382,18 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       const bool ok = tc::mbar_wait(&sh.tfull, local & 1, abort);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc::tc_fence_after();
-      const int my_end = min(ntok, tok_half + GN / 2);   // this warp's tokens: [tok_half, my_end)
-      uint32_t packed[4][16];
+      const int my_end = min(ntok, tok_half + G_TOK_PER_EPI);   // this warp's tokens: [tok_half, my_end)
+      // bf16 pairs: packed[c][q] = tokens 2q, 2q+1 of chunk c (SwiGLU: of the
+      // lane's 16 tokens of the chunk, q < 8)
+      uint32_t packed[4][EPI == 2 ? 8 : 16];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int col0 = tok_half + c * 32;
         if (col0 < my_end) {
-          uint32_t a[32];
-          tc::tmem_ld32(lane_base + (uint32_t)col0, a);
-          tc::tmem_ld_wait();
           if constexpr (EPI == 2) {
+            uint32_t a[32];
+            tc::tmem_ld32(lane_base + (uint32_t)col0, a);
+            tc::tmem_ld_wait();
             // low lane: gate values g[0..31] of its row; high lane: up values
             // u[0..31] of the same row.  The low lane takes tokens 0..15, the
             // high lane tokens 16..31.
@@ -395,13 +409,19 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
             }
           } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float v0 = __uint_as_float(a[2 * i]), v1 = __uint_as_float(a[2 * i + 1]);
-              if constexpr (EPI == 1) {
-                v0 = fmaxf(v0, 0.f);
-                v1 = fmaxf(v1, 0.f);
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t a[16];
+              tmem_ld16(lane_base + (uint32_t)(col0 + 16 * hh), a);
+              tc::tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                float v0 = __uint_as_float(a[2 * i]), v1 = __uint_as_float(a[2 * i + 1]);
+                if constexpr (EPI == 1) {
+                  v0 = fmaxf(v0, 0.f);
+                  v1 = fmaxf(v1, 0.f);
+                }
+                packed[c][8 * hh + i] = pack_bf16x2(v0, v1);
               }
-              packed[c][i] = pack_bf16x2(v0, v1);
             }
           }
         }
@@ -554,7 +574,7 @@ cudaError_t launch_mx(const GemmStage &g, int *status, cudaStream_t s) {
     return cudaErrorInvalidValue;
   // packed codes: [E][N][K/2] bytes, boxes of 32 bytes (one k-block) x 64 rows
   const uint64_t dC[3] = {(uint64_t)g.K / 2, (uint64_t)g.N, (uint64_t)g.num_experts};
-  const uint32_t bC[3] = {GK / 2, (uint32_t)(GM / 2), 1};
+  const uint32_t bC[3] = {GK / 2, (uint32_t)(EPI == 2 ? GM / 2 : GM), 1};
   if (!make_tensor_map(&mW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.B, 3, dC, bC,
                        CU_TENSOR_MAP_SWIZZLE_32B))
     return cudaErrorInvalidValue;
@@ -576,7 +596,7 @@ cudaError_t launch_mx(const GemmStage &g, int *status, cudaStream_t s) {
   a.out = static_cast<__nv_bfloat16 *>(g.out);
   a.out16 = static_cast<uint16_t *>(g.out16);
   a.status = status;
-  return launch_pdl(gemm_mx_kernel<EPI>, dim3(num_sms()), dim3(G_THREADS), smem, s, mX, mW, mW3,
+  return launch_pdl(gemm_mx_kernel<EPI>, dim3(2 * num_sms()), dim3(G_THREADS), smem, s, mX, mW, mW3,
                     a);
 }
 
@@ -587,7 +607,7 @@ bool gemm_mx_supported(const GemmStage &g) {
   return g.rows > 0 && tensor_maps_available() && g.b_dtype == MOE_MXFP4 && g.a_dtype == kF16 &&
          g.out_dtype == MOE_BF16 && (g.epi == 0 || g.epi == 1 || g.epi == 2) &&
          g.offsets != nullptr && g.num_experts <= G_MAX_E && g.K % GK == 0 && g.N % 32 == 0 &&
-         g_dyn_smem(g.K) + sizeof(GShared) <= 227 * 1024;
+         g_dyn_smem(g.K) + sizeof(GShared) <= 113 * 1024;   // two CTAs per SM
 }
 
 cudaError_t launch_gemm_mx(const GemmStage &g, int *status, cudaStream_t s) {
