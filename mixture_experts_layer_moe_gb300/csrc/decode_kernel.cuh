@@ -202,7 +202,10 @@ struct ProducerState {
   bool valid, active, pool;
 };
 
-// EPI: 0 none, 1 relu, 2 swiglu (tm3 / S3 hold the linear branch).  RG: 16-row
+// EPI: 0 none, 1 relu, 2 swiglu (tm3 / S3 hold the linear branch), 3 none with
+// 32-row groups: rows r .. r+15 and r+16 .. r+31 of the one matrix take the
+// places of the two SwiGLU matrices, so each activation fragment a warp loads
+// serves two rows' MMAs (the row count must be a multiple of 32).  RG: row
 // groups per CTA; the KS = DV_WARPS / RG warps of a group split the reduction
 // into contiguous, equal runs of MX blocks.
 //
@@ -226,9 +229,11 @@ __global__ void __launch_bounds__(32 * DV_WARPS, 2)
 decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm3,
                     const __grid_constant__ CUtensorMap tp1, const __grid_constant__ CUtensorMap tp3,
                     DecodeArgs a) {
-  constexpr int NMAT = (EPI == 2) ? 2 : 1;
+  constexpr bool PAIRED = EPI == 3;
+  constexpr int NMAT = (EPI == 2 || PAIRED) ? 2 : 1;
+  constexpr int GROWS = PAIRED ? 32 : 16;   // weight rows per group
   constexpr int KS = DV_WARPS / RG;
-  constexpr int CTA_ROWS = 16 * RG;
+  constexpr int CTA_ROWS = GROWS * RG;
   constexpr int RV = KS == 2 ? 4 : 8;   // partial sums a warp hands over per lane
   constexpr int SPC = FMT == 1 ? 2 : 1; // scale bytes per 16-byte code chunk
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -248,10 +253,10 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
     tc::prefetch_tmap(&tm1);
-    if (NMAT == 2) tc::prefetch_tmap(&tm3);
+    if (EPI == 2) tc::prefetch_tmap(&tm3);
     if constexpr (POOL) {
       tc::prefetch_tmap(&tp1);
-      if (NMAT == 2) tc::prefetch_tmap(&tp3);
+      if (EPI == 2) tc::prefetch_tmap(&tp3);
     }
   }
   pdl_wait();
@@ -347,14 +352,14 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     const int e = s_active[sl], r0 = (u - sl * row_blocks) * CTA_ROWS;
     const uint32_t bytes = (uint32_t)min(CTA_ROWS, R - r0) * KB * SPC;   // rows % 16 == 0
     const int b = i % NRAW;
-    tc::mbar_arrive_expect_tx(&sbar[b], NMAT * bytes);
+    tc::mbar_arrive_expect_tx(&sbar[b], (PAIRED ? 1 : NMAT) * bytes);
     uint8_t *dst = smem + plan.raw_off + (size_t)b * NMAT * sc_pitch;
     // the resident copy (pool slot) or the backing expert
     const int ps = POOL ? s_slot[sl] : -1;
     const uint8_t *S1 = ps >= 0 ? a.PS : a.S, *S3 = ps >= 0 ? a.PS3 : a.S3;
     const size_t row = (size_t)(ps >= 0 ? ps : e) * R + r0;
     bulk_load(dst, S1 + row * KB * SPC, bytes, &sbar[b]);
-    if (NMAT == 2) bulk_load(dst + sc_pitch, S3 + row * KB * SPC, bytes, &sbar[b]);
+    if (EPI == 2) bulk_load(dst + sc_pitch, S3 + row * KB * SPC, bytes, &sbar[b]);
     if (b) raw_mine1 = i;
     else raw_mine0 = i;
   };
@@ -367,7 +372,7 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     P.valid = nslot > 0 && u < total;
     if (!P.valid) return;
     const int sl = u / row_blocks;
-    const int r = (u - sl * row_blocks) * CTA_ROWS + grp * 16;
+    const int r = (u - sl * row_blocks) * CTA_ROWS + grp * GROWS;
     P.active = r < R;
     P.pool = POOL && s_slot[sl] >= 0;
     P.wrow = (P.pool ? s_slot[sl] : s_active[sl]) * R + r;
@@ -385,11 +390,13 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       // a box past the end of the row reads zeros
       if (POOL && P.pool) {
         tc::tma_load_2d(&tp1, &full[warp][sl], dst, x, y);
-        if (NMAT == 2) tc::tma_load_2d(&tp3, &full[warp][sl], dst + DV_BOX, x, y);
+        if (EPI == 2) tc::tma_load_2d(&tp3, &full[warp][sl], dst + DV_BOX, x, y);
+        else if (PAIRED) tc::tma_load_2d(&tp1, &full[warp][sl], dst + DV_BOX, x, y + 16);
         else tc::tma_load_2d(&tp1, &full[warp][sl], dst + DV_BOX, x + DV_BOXB, y);
       } else {
         tc::tma_load_2d(&tm1, &full[warp][sl], dst, x, y);
-        if (NMAT == 2) tc::tma_load_2d(&tm3, &full[warp][sl], dst + DV_BOX, x, y);
+        if (EPI == 2) tc::tma_load_2d(&tm3, &full[warp][sl], dst + DV_BOX, x, y);
+        else if (PAIRED) tc::tma_load_2d(&tm1, &full[warp][sl], dst + DV_BOX, x, y + 16);
         else tc::tma_load_2d(&tm1, &full[warp][sl], dst + DV_BOX, x + DV_BOXB, y);
       }
     } else {
@@ -419,7 +426,7 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     const int u = (int)blockIdx.x + i * (int)gridDim.x;
     if (u >= total) break;
     const int sl = u / row_blocks;
-    const int r0 = (u - sl * row_blocks) * CTA_ROWS + grp * 16;
+    const int r0 = (u - sl * row_blocks) * CTA_ROWS + grp * GROWS;
     const bool active = r0 < R;
     const int beg = s_beg[sl], cnt = s_cnt[sl];
 
@@ -429,6 +436,14 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
                     tc::mbar_wait(&sbar[i % NRAW], (uint32_t)((i / NRAW) & 1), abort));
     // the warps of a group leave together, so none waits on a barrier alone
     if (group_sync_or(grp, 32 * KS, !ok)) { ok = false; break; }
+    // raw scale row gg of "matrix" m of this warp's group: the second matrix's
+    // rows (SwiGLU), or rows 16..31 of the group (paired rows), at the
+    // warp's first block
+    auto raw_row = [&](int m, int gg) -> const uint8_t * {
+      const uint8_t *buf = smem + plan.raw_off + (size_t)(i % NRAW) * NMAT * sc_pitch;
+      if constexpr (PAIRED) return buf + ((size_t)(grp * GROWS + 16 * m + gg) * KB + b_beg) * SPC;
+      return buf + (size_t)m * sc_pitch + ((size_t)(grp * 16 + gg) * KB + b_beg) * SPC;
+    };
     if constexpr (FMT == 1) {
       // NVFP4: lane (gg = lane / 4, q = lane % 4) takes chunks q, q + 4, ...
       // of row pair gg; a chunk's two scale bytes of row gg and of row gg + 8
@@ -438,8 +453,7 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       uint16_t *pw16 = reinterpret_cast<uint16_t *>(pw);
 #pragma unroll
       for (int m = 0; m < NMAT; ++m) {
-        const uint8_t *src = smem + plan.raw_off + (size_t)((i % NRAW) * NMAT + m) * sc_pitch +
-                             ((grp * 16 + gg) * KB + b_beg) * 2;
+        const uint8_t *src = raw_row(m, gg);
         uint16_t *dst = pw16 + (size_t)(m * 8 + gg) * 2 * PP;
         for (int b = q; b < nbl; b += 4) {
           const uint32_t x = *reinterpret_cast<const uint16_t *>(src + 2 * b);
@@ -456,8 +470,7 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       const bool even = (KB & 1) == 0;
 #pragma unroll
       for (int m = 0; m < NMAT; ++m) {
-        const uint8_t *src = smem + plan.raw_off + (size_t)((i % NRAW) * NMAT + m) * sc_pitch +
-                             (grp * 16 + gg) * KB + b_beg;
+        const uint8_t *src = raw_row(m, gg);
         uint32_t *dst = pw + (m * 8 + gg) * PP;
         for (int b = 2 * q; b < nbl; b += 8) {
           const bool two = b + 1 < nbl;
@@ -494,7 +507,8 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     float gs1 = 1.f, gs3 = 1.f;   // NVFP4 matrix scales of this unit's expert
     if constexpr (FMT == 1) {
       gs1 = a.G[s_active[sl]];
-      if (NMAT == 2) gs3 = a.G3[s_active[sl]];
+      if (EPI == 2) gs3 = a.G3[s_active[sl]];
+      else if (PAIRED) gs3 = gs1;
     }
 
     for (int tg = 0; tg < cnt; tg += DV_TOK, ++npass) {
@@ -673,7 +687,17 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
         }
         frow = split == 1 ? g + 8 : g;
       }
-      if (fin) {
+      if (PAIRED && fin) {
+        // rows r0 + frow (f1) and r0 + 16 + frow (f3)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int tk = tg + 2 * t + q;
+          if (tk < cnt) {
+            a.out[(size_t)(beg + tk) * R + r0 + frow] = __float2bfloat16_rn(f1[q] * gs1);
+            a.out[(size_t)(beg + tk) * R + r0 + 16 + frow] = __float2bfloat16_rn(f3[q] * gs3);
+          }
+        }
+      } else if (fin) {
         const int row = r0 + frow;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -711,7 +735,8 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
 template <int EPI, int RG, bool POOL, int FMT>
 cudaError_t launch_one(DecodeArgs a, const uint8_t *W, const uint8_t *W3, const uint8_t *PW,
                        const uint8_t *PW3, int num_experts, int slots, cudaStream_t s) {
-  constexpr int NMAT = (EPI == 2) ? 2 : 1;
+  constexpr int NMAT = (EPI == 2 || EPI == 3) ? 2 : 1;
+  constexpr int GROWS = (EPI == 3) ? 32 : 16;
   const size_t smem = 1024 + decode_plan(NMAT, a.K, RG, FMT).bytes;
   static size_t smem_set = 0;
   static int per_sm = 0;
@@ -734,7 +759,7 @@ cudaError_t launch_one(DecodeArgs a, const uint8_t *W, const uint8_t *W3, const 
   if (!make_tensor_map(&m1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W, 2, dims, box,
                        CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if (NMAT == 2) {
+  if (EPI == 2) {
     if (!make_tensor_map(&m3, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, W3, 2, dims, box,
                          CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
@@ -748,12 +773,12 @@ cudaError_t launch_one(DecodeArgs a, const uint8_t *W, const uint8_t *W3, const 
     if (!make_tensor_map(&p1, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, PW, 2, pdims, box,
                          CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
-    if (NMAT == 2 && !make_tensor_map(&p3, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, PW3, 2, pdims, box,
+    if (EPI == 2 && !make_tensor_map(&p3, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, PW3, 2, pdims, box,
                                       CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   // units: at most `slots` experts x row blocks; no more CTAs than units
-  const long units = (long)slots * ((a.R + 16 * RG - 1) / (16 * RG));
+  const long units = (long)slots * ((a.R + GROWS * RG - 1) / (GROWS * RG));
   long grid = (long)per_sm * num_sms();
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
@@ -770,7 +795,8 @@ template <int EPI, bool POOL, int FMT>
 cudaError_t launch_rg(DecodeArgs a, const uint8_t *W, const uint8_t *W3, const uint8_t *PW,
                       const uint8_t *PW3, int num_experts, int slots, cudaStream_t s) {
   const long ctas = 2L * num_sms();
-  auto units = [&](int rg) { return (long)slots * ((a.R + 16 * rg - 1) / (16 * rg)); };
+  constexpr int GROWS = (EPI == 3) ? 32 : 16;
+  auto units = [&](int rg) { return (long)slots * ((a.R + GROWS * rg - 1) / (GROWS * rg)); };
   // (NVFP4 units stop at 32 rows: their scale bytes double, and 64-row units
   // would not fit two CTAs per SM)
   if constexpr (FMT == 0)
@@ -836,9 +862,17 @@ cudaError_t run_decode_ffn(const moe_config &c, int part, const void *act, const
   a.K = c.d_ff;
   a.out = static_cast<__nv_bfloat16 *>(y_perm);
   a.out16 = nullptr;
-  return launch_rg<0, POOL, FMT>(a, static_cast<const uint8_t *>(w.W2), nullptr,
-                      pool ? static_cast<const uint8_t *>(pool->W2) : nullptr, nullptr, c.n_experts,
-                      slots, s);
+  // The down projection's rows (d) are a multiple of 32.  Paired 32-row
+  // groups load each activation fragment once for two rows' MMAs; they pay
+  // off once there are at least two 128-row units per resident CTA (measured
+  // on the gpt-oss shape: n = 64 128 -> 113 us, n = 16 65 -> 59 us; at n = 4
+  // the coarser units balance worse and single groups stay ahead).
+  const uint8_t *W2 = static_cast<const uint8_t *>(w.W2);
+  const uint8_t *P2 = pool ? static_cast<const uint8_t *>(pool->W2) : nullptr;
+  const long paired_units = (long)slots * ((a.R + 127) / 128);
+  if (paired_units >= 4L * num_sms())
+    return launch_rg<3, POOL, FMT>(a, W2, nullptr, P2, nullptr, c.n_experts, slots, s);
+  return launch_rg<0, POOL, FMT>(a, W2, nullptr, P2, nullptr, c.n_experts, slots, s);
 }
 
 }  // namespace

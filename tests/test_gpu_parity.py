@@ -41,6 +41,11 @@ SMALL = {
                                                          act="relu"),
     # an odd number of MX blocks per row (3 and 5) on both projections
     "decode_odd_blocks": C["gptoss_decode_mxfp4"].scaled(n=4, d=96, d_ff=160, E=8, k=2),
+    # enough experts and rows for the down projection's paired 32-row groups
+    # (256 slots x 3 units of 128 rows), the last unit 96 rows, 5 MX blocks
+    "decode_paired_down": C["gptoss_decode_mxfp4"].scaled(n=32, d=352, d_ff=160, E=256, k=8),
+    "nvfp4_decode_paired_down": C["gptoss_decode_nvfp4"].scaled(n=32, d=352, d_ff=160, E=256,
+                                                                k=8),
     "nvfp4_decode_small": C["gptoss_decode_nvfp4"].scaled(n=8, d=256, d_ff=320, E=16),
     "nvfp4_decode_relu": C["gptoss_decode_nvfp4"].scaled(n=16, d=128, d_ff=192, E=8, k=2,
                                                          act="relu"),
