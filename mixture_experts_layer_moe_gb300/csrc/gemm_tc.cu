@@ -20,15 +20,7 @@
 // whole activation segment in L2.  The tile list is derived on the device
 // from the segment offsets; empty segments produce no tiles.
 //
-// MXFP4 weights (MX variant, feed post "What is MXFP4?"; OCP MX v1.0 E2M1
-// codes with one E8M0 scale per 32 elements): TMA brings the packed codes of
-// the B rows (32 bytes per row per k-block) next to the A tile, and four
-// transform warps (6-13) write the dequantised B tile into the 128-byte-swizzled
-// K-major layout the MMA reads: cvt.rn.f16x2.e2m1x2 on each code pair, times
-// the block scale as an f16 pair.  The MMA then runs kind::f16 on f16 operands
-// (the activations come as exact f16 copies of the bf16 rows).  A block scale
-// whose value is outside f16's normal range (E8M0 byte outside 113..142)
-// cannot be applied exactly and is reported as MOE_ERR_RANGE.
+// MXFP4 weights run on gemm_mx.cu (dequantised into tensor memory).
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -42,28 +34,8 @@ constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int DYN_SMEM = STAGES * STAGE_BYTES + 1024;
-// MX variant: a TMA ring of [A 16 KB][codes 8 KB] stages and a separate ring of
-// dequantised f16 B tiles (32 KB) written by the transform warps, so the TMA
-// runs MX_STAGES k-blocks ahead of the MMAs while only MX_BSTAGES B tiles
-// exist; plus two tile-sized buffers of E8M0 scales.
-constexpr int MX_STAGES = 4;
-constexpr int MX_BSTAGES = 2;
-constexpr int MX_XWARPS = 8;                       // transform warps (one B row per thread)
-constexpr int MX_THREADS = 192 + 32 * MX_XWARPS;
-constexpr int CODE_BYTES = BN * BK / 2;
-constexpr int MX_STAGE_BYTES = A_BYTES + CODE_BYTES;
-constexpr int MAX_STAGES = STAGES > MX_STAGES ? STAGES : MX_STAGES;
 constexpr int MAX_E = 256;
 constexpr uint32_t TMEM_COLS = 512;
-
-__host__ __device__ inline size_t mx_scale_buf_bytes(int K) { return (size_t)BN * (K / 32); }
-__host__ __device__ inline size_t mx_bring_off() { return (size_t)MX_STAGES * MX_STAGE_BYTES; }
-__host__ __device__ inline size_t mx_scale_off() {
-  return mx_bring_off() + (size_t)MX_BSTAGES * B_BYTES;
-}
-size_t mx_dyn_smem(int K) {
-  return 1024 + mx_scale_off() + 2 * ((mx_scale_buf_bytes(K) + 15) & ~15);
-}
 
 struct TcArgs {
   const int32_t *offsets;  // nullptr: one segment [0, rows) of expert 0
@@ -74,16 +46,11 @@ struct TcArgs {
   void *out;       // bf16 [rows][N], fp32 for EPI 3
   const float *bias;
   int *status;
-  // MX variant
-  const uint8_t *S, *S3;   // E8M0 scales [E][N][K/32] of B (and B3)
-  uint16_t *out16;         // f16 copy of out, or nullptr
 };
 
 struct TcShared {
-  uint64_t full[MAX_STAGES];
-  uint64_t empty[MAX_STAGES];
-  uint64_t bready[MX_BSTAGES];    // MX: a dequantised B tile is written
-  uint64_t bempty[MX_BSTAGES];    // MX: the MMAs have read it
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -123,46 +90,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// The four code pairs of a 32-bit word (bytes 0..3) as four f16 pairs, low
-// nibble (even element) in the low half.
-__device__ __forceinline__ uint4 e2m1x8_to_f16x2x4(uint32_t w) {
-  uint4 r;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "r"(w));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// E8M0 byte -> 2^(s-127) as an f16 pair; 0 (and *bad set) outside f16's normal range.
-__device__ __forceinline__ uint32_t scale_f16x2(uint32_t s, bool &bad) {
-  if (s < 113u || s > 142u) {
-    bad = true;
-    return 0u;
-  }
-  const uint32_t h = (s - 112u) << 10;
-  return h | (h << 16);
-}
-
-__device__ __forceinline__ uint32_t f16x2_from_bf16x2(uint32_t b) {
-  const float lo = fminf(fmaxf(__uint_as_float(b << 16), -65504.f), 65504.f);
-  const float hi = fminf(fmaxf(__uint_as_float(b & 0xffff0000u), -65504.f), 65504.f);
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t *>(&h);
-}
-
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src)
-               : "memory");
-}
-
 // EPI: 0 plain, 1 relu, 2 swiglu (B = W1 rows, B3 = W3 rows, 128 each),
 // 3 fp32 output + per-column bias (router logits).
 //
@@ -172,17 +99,17 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
 // registers with round-to-nearest.  Accumulating the whole reduction in TMEM
 // instead drifted by ~2e-5 on d = 4096 rows, too close to the 1e-5 near-tie
 // margin of the routing decision.
-template <int EPI, bool MX>
-__global__ void __launch_bounds__(MX ? MX_THREADS : THREADS, 1)
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmB3, TcArgs args) {
   constexpr bool KPART = (EPI == 3);                 // per-k-block partials
   constexpr int BNT = KPART ? 128 : BN;              // MMA N = B rows per stage
   constexpr int N_OUT = (EPI == 2) ? BN / 2 : BNT;   // output columns per tile
-  constexpr int NSTAGE = MX ? MX_STAGES : STAGES;
-  constexpr int SBYTES = MX ? MX_STAGE_BYTES : STAGE_BYTES;
-  constexpr int NTHREADS = MX ? MX_THREADS : THREADS;
-  constexpr uint32_t TX_BYTES = MX ? (A_BYTES + CODE_BYTES) : (A_BYTES + BNT * BK * 2);
+  constexpr int NSTAGE = STAGES;
+  constexpr int SBYTES = STAGE_BYTES;
+  constexpr int NTHREADS = THREADS;
+  constexpr uint32_t TX_BYTES = A_BYTES + BNT * BK * 2;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ TcShared sh;
   uint8_t *smem = dyn_smem + ((1024 - (tc::smem_u32(dyn_smem) & 1023)) & 1023);
@@ -201,13 +128,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (threadIdx.x == 32) {
     for (int s = 0; s < NSTAGE; ++s) {
       tc::mbar_init(&sh.full[s], 1);
-      // MX: the codes are read by the transform warps (one arrival each), A by
-      // the MMAs
-      tc::mbar_init(&sh.empty[s], MX ? 1 + MX_XWARPS : 1);
-    }
-    for (int b = 0; b < MX_BSTAGES; ++b) {
-      tc::mbar_init(&sh.bready[b], 32 * MX_XWARPS);
-      tc::mbar_init(&sh.bempty[b], 1);
+      tc::mbar_init(&sh.empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&sh.tfull[a], 1);
@@ -267,9 +188,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (EPI == 2) tc::prefetch_tmap(&tmB3);
       int stage = 0;
       uint32_t phase = 0;
-      int last_phase[MAX_STAGES];
+      int last_phase[STAGES];
 #pragma unroll
-      for (int s = 0; s < MAX_STAGES; ++s) last_phase[s] = -1;
+      for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
       for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
         const Tile tl = decode_tile(sh, E, t);
         const int wrow = tl.n_idx * N_OUT;
@@ -279,16 +200,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           uint8_t *sb = sa + A_BYTES;
           tc::mbar_arrive_expect_tx(&sh.full[stage], TX_BYTES);
           tc::tma_load_2d(&tmA, &sh.full[stage], sa, kb * BK, tl.row0);
-          if constexpr (MX) {
-            uint8_t *sc = sb;                         // the codes follow A
-            if (EPI == 2) {
-              tc::tma_load_3d(&tmB, &sh.full[stage], sc, kb * (BK / 2), wrow, tl.e);
-              tc::tma_load_3d(&tmB3, &sh.full[stage], sc + CODE_BYTES / 2, kb * (BK / 2), wrow,
-                              tl.e);
-            } else {
-              tc::tma_load_3d(&tmB, &sh.full[stage], sc, kb * (BK / 2), wrow, tl.e);
-            }
-          } else if (EPI == 2) {
+          if (EPI == 2) {
             tc::tma_load_3d(&tmB, &sh.full[stage], sb, kb * BK, wrow, tl.e);
             tc::tma_load_3d(&tmB3, &sh.full[stage], sb + B_BYTES / 2, kb * BK, wrow, tl.e);
           } else {
@@ -308,11 +220,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      constexpr uint32_t idesc = MX ? tc::idesc_f16_f32(BM, BNT) : tc::idesc_bf16_f32(BM, BNT);
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BNT);
       int stage = 0;
       uint32_t phase = 0;
-      int bstage = 0;              // MX: dequantised B ring
-      uint32_t bphase = 0;
       int local = 0;   // accumulator uses so far (tiles, or k-blocks with KPART)
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok && !*abort; t += gridDim.x) {
@@ -326,21 +236,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
           if (!tc::mbar_wait(&sh.full[stage], phase, abort)) { ok = false; break; }
-          if (MX && !tc::mbar_wait(&sh.bready[bstage], bphase, abort)) { ok = false; break; }
           tc::tc_fence_after();
           const uint32_t sa = tc::smem_u32(smem + stage * SBYTES);
-          const uint32_t sb = MX ? tc::smem_u32(smem + mx_bring_off() + (size_t)bstage * B_BYTES)
-                                 : sa + A_BYTES;
+          const uint32_t sb = sa + A_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             tc::mma_bf16(d_tmem, tc::smem_desc_sw128(sa + k * 32), tc::smem_desc_sw128(sb + k * 32),
                          idesc, (k != 0 || (!KPART && kb != 0)) ? 1u : 0u);
           tc::mma_commit(&sh.empty[stage]);
           if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
-          if constexpr (MX) {
-            tc::mma_commit(&sh.bempty[bstage]);
-            if (++bstage == MX_BSTAGES) { bstage = 0; bphase ^= 1u; }
-          }
           if (KPART || kb == KB - 1) {
             tc::mma_commit(&sh.tfull[acc]);
             ++local;
@@ -405,7 +309,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int row = tl.row0 + r_local;
         const bool row_ok = row < tl.seg_end;
         __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(args.out) + (size_t)row * args.N;
-        uint16_t *orow16 = args.out16 ? args.out16 + (size_t)row * args.N : nullptr;
         constexpr int CHUNKS = N_OUT / 32;
 #pragma unroll 1
         for (int c = 0; c < CHUNKS; ++c) {
@@ -438,10 +341,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               if (col0 + v * 8 < args.N) {
                 *reinterpret_cast<uint4 *>(orow + col0 + v * 8) = make_uint4(
                     packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-                if (orow16)
-                  *reinterpret_cast<uint4 *>(orow16 + col0 + v * 8) = make_uint4(
-                      f16x2_from_bf16x2(packed[4 * v]), f16x2_from_bf16x2(packed[4 * v + 1]),
-                      f16x2_from_bf16x2(packed[4 * v + 2]), f16x2_from_bf16x2(packed[4 * v + 3]));
               }
             }
           }
@@ -449,101 +348,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       }
     }
-  } else if constexpr (MX) {
-    // ---------------- transform: warps 6..13 dequantise the B tile of each
-    // stage, thread tt owning B row tt.  Scales of a tile's 256 rows are copied
-    // (cp.async) into one of two buffers while the previous tile runs.  The
-    // codes arrive with a 32-byte swizzle: 16-byte half c of row r sits at
-    // c ^ ((r >> 2) & 1), which keeps the warp's row reads conflict-free.
-    const int tt = threadIdx.x - 192;
-    constexpr int XT = 32 * MX_XWARPS;
-    const int KBLK = args.K / 32;
-    const size_t sbuf = mx_scale_buf_bytes(args.K);
-    const size_t spitch = (sbuf + 15) & ~(size_t)15;
-    uint8_t *scale_buf[2] = {smem + mx_scale_off(), smem + mx_scale_off() + spitch};
-    // scales of tile t's rows -> buffer b (rows past N are left unset: their
-    // codes are zero-filled by TMA and their columns are never stored)
-    auto fetch_scales = [&](int t, int b) {
-      const Tile tl = decode_tile(sh, E, t);
-      const int wrow = tl.n_idx * N_OUT;
-      const int nmat = (EPI == 2) ? 2 : 1;
-      const int rows_per = BN / nmat;
-      for (int m = 0; m < nmat; ++m) {
-        const uint8_t *S = m == 0 ? args.S : args.S3;
-        const int rows = min(rows_per, args.N - wrow);
-        const size_t bytes = (size_t)rows * KBLK;           // a multiple of 16
-        const uint8_t *src = S + ((size_t)tl.e * args.N + wrow) * KBLK;
-        uint8_t *dst = scale_buf[b] + (size_t)m * rows_per * KBLK;
-        for (size_t o = (size_t)tt * 16; o < bytes; o += XT * 16) cp_async16(dst + o, src + o);
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    int stage = 0, bstage = 0;
-    uint32_t phase = 0, bphase = 0;
-    int buf = 0;
-    bool bad_scale = false;
-    const int r = tt;                                         // B row in the tile
-    const int rows_per = (EPI == 2) ? BN / 2 : BN;
-    const int sw = ((r >> 2) & 1) << 4;
-    if (blockIdx.x < num_tiles) fetch_scales(blockIdx.x, 0);
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, buf ^= 1) {
-      asm volatile("cp.async.wait_group 0;" ::: "memory");
-      // this tile's scales are in; the transform warps also agree here on
-      // stopping (a warp whose wait ran out has raised *abort)
-      uint32_t stop;
-      asm volatile(
-          "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-          "bar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-          : "=r"(stop)
-          : "r"((uint32_t)*abort), "n"(XT)
-          : "memory");
-      if (stop) break;
-      if (t + (int)gridDim.x < num_tiles) fetch_scales(t + gridDim.x, buf ^ 1);
-      const uint8_t *srow = scale_buf[buf] + (size_t)r * KBLK;
-      const int wrow = decode_tile(sh, E, t).n_idx * N_OUT;
-      const bool row_ok = wrow + (r % rows_per) < args.N;    // else: zero row
-      for (int kb = 0; kb < KB; ++kb) {
-        bool ok = tc::mbar_wait(&sh.full[stage], phase, abort);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        const uint8_t *codes = smem + stage * SBYTES + A_BYTES + r * 32;
-        uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
-        if (row_ok) {
-          c0 = *reinterpret_cast<const uint4 *>(codes + sw);
-          c1 = *reinterpret_cast<const uint4 *>(codes + (sw ^ 16));
-        }
-        // the codes are in registers: this warp is done with the TMA stage
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sh.empty[stage]);
-        if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
-        ok = tc::mbar_wait(&sh.bempty[bstage], bphase ^ 1u, abort);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        uint8_t *brow = smem + mx_bring_off() + (size_t)bstage * B_BYTES + (r >> 3) * 1024 +
-                        (r & 7) * 128;
-        if (row_ok) {
-          const uint32_t s0 = 2 * kb < KBLK ? srow[2 * kb] : 127u;
-          const uint32_t s1 = 2 * kb + 1 < KBLK ? srow[2 * kb + 1] : 127u;
-          const uint32_t f0 = scale_f16x2(s0, bad_scale), f1 = scale_f16x2(s1, bad_scale);
-          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t f = j < 4 ? f0 : f1;
-            const uint4 q = e2m1x8_to_f16x2x4(words[j]);
-            const uint4 v = make_uint4(hmul2(q.x, f), hmul2(q.y, f), hmul2(q.z, f), hmul2(q.w, f));
-            *reinterpret_cast<uint4 *>(brow + ((j ^ (r & 7)) << 4)) = v;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4 *>(brow + (j << 4)) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        // generic-proxy writes of the B tile -> visible to the tensor core
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        tc::mbar_arrive(&sh.bready[bstage]);
-        if (++bstage == MX_BSTAGES) { bstage = 0; bphase ^= 1u; }
-      }
-    }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    if (bad_scale) set_status(args.status, MOE_ERR_RANGE, 0);
   }
 
   __syncwarp();
@@ -559,12 +363,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
 // ---------------------------------------------------------------- host side
 
-template <int EPI, bool MX>
+template <int EPI>
 cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
-  const size_t smem = MX ? mx_dyn_smem(g.K) : (size_t)DYN_SMEM;
+  const size_t smem = (size_t)DYN_SMEM;
   static size_t smem_set = 0;
   if (smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, MX>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     smem_set = smem;
@@ -574,36 +378,20 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
   const uint64_t dA[2] = {(uint64_t)g.K, (uint64_t)g.rows};
   const uint32_t bA[2] = {BK, BM};
   const int wrows = (EPI == 2) ? BN / 2 : (EPI == 3 ? 128 : BN);
-  const CUtensorMapDataType adt = MX ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!make_tensor_map(&mA, adt, 2, g.A, 2, dA, bA, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!make_tensor_map(&mA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.A, 2, dA, bA,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if (MX) {
-    // packed codes: [E][N][K/2] bytes, boxes of 32 bytes (one k-block) x wrows rows
-    const uint64_t dC[3] = {(uint64_t)g.K / 2, (uint64_t)g.N, (uint64_t)E};
-    const uint32_t bC[3] = {BK / 2, (uint32_t)wrows, 1};
-    if (!make_tensor_map(&mB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.B, 3, dC, bC,
-                         CU_TENSOR_MAP_SWIZZLE_32B))
-      return cudaErrorInvalidValue;
-    if (EPI == 2) {
-      if (!make_tensor_map(&mB3, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.B3, 3, dC, bC,
-                           CU_TENSOR_MAP_SWIZZLE_32B))
-        return cudaErrorInvalidValue;
-    } else {
-      mB3 = mB;
-    }
-  } else {
-    const uint64_t dB[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)E};
-    const uint32_t bB[3] = {BK, (uint32_t)wrows, 1};
-    if (!make_tensor_map(&mB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.B, 3, dB, bB,
+  const uint64_t dB[3] = {(uint64_t)g.K, (uint64_t)g.N, (uint64_t)E};
+  const uint32_t bB[3] = {BK, (uint32_t)wrows, 1};
+  if (!make_tensor_map(&mB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.B, 3, dB, bB,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (EPI == 2) {
+    if (!make_tensor_map(&mB3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.B3, 3, dB, bB,
                          CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
-    if (EPI == 2) {
-      if (!make_tensor_map(&mB3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.B3, 3, dB, bB,
-                           CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    } else {
-      mB3 = mB;
-    }
+  } else {
+    mB3 = mB;
   }
   TcArgs a{};
   a.offsets = g.offsets;
@@ -614,10 +402,7 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
   a.out = g.out;
   a.bias = g.col_bias;
   a.status = status;
-  a.S = g.SB;
-  a.S3 = g.SB3;
-  a.out16 = static_cast<uint16_t *>(g.out16);
-  gemm_tc_kernel<EPI, MX><<<num_sms(), MX ? MX_THREADS : THREADS, smem, s>>>(mA, mB, mB3, a);
+  gemm_tc_kernel<EPI><<<num_sms(), THREADS, smem, s>>>(mA, mB, mB3, a);
   return cudaGetLastError();
 }
 
@@ -625,29 +410,20 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
 
 bool gemm_tc_supported(const GemmStage &g) {
   if (g.rows <= 0 || !tensor_maps_available()) return false;
-  if (g.b_dtype == MOE_MXFP4) {
-    if (gemm_mx_supported(g)) return true;
-    if (g.epi != 2) return false;
-    // f16 activations, MXFP4 weights; all scale buffers must fit in shared memory
-    return g.a_dtype == kF16 && g.out_dtype == MOE_BF16 && g.K % 64 == 0 && g.N % 32 == 0 &&
-           mx_dyn_smem(g.K) + sizeof(TcShared) <= 227 * 1024;
-  }
+  // MXFP4: the weights-in-tensor-memory kernel of gemm_mx.cu
+  if (g.b_dtype == MOE_MXFP4) return gemm_mx_supported(g);
   const bool out_ok = g.epi == 3 ? g.out_dtype == MOE_F32 : g.out_dtype == MOE_BF16;
   const bool n_ok = g.epi == 3 ? true : g.N % 8 == 0;
   return g.a_dtype == MOE_BF16 && g.b_dtype == MOE_BF16 && out_ok && n_ok && g.K % 8 == 0;
 }
 
 cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s) {
-  // MXFP4: the weights-in-tensor-memory kernel (gemm_mx.cu) where its shared
-  // memory fits; else, for SwiGLU, this file's kernel with the dequantised
-  // tile in shared memory
-  if (g.b_dtype == MOE_MXFP4)
-    return gemm_mx_supported(g) ? launch_gemm_mx(g, status, s) : launch_epi<2, true>(g, status, s);
+  if (g.b_dtype == MOE_MXFP4) return launch_gemm_mx(g, status, s);
   switch (g.epi) {
-    case 0: return launch_epi<0, false>(g, status, s);
-    case 1: return launch_epi<1, false>(g, status, s);
-    case 2: return launch_epi<2, false>(g, status, s);
-    default: return launch_epi<3, false>(g, status, s);
+    case 0: return launch_epi<0>(g, status, s);
+    case 1: return launch_epi<1>(g, status, s);
+    case 2: return launch_epi<2>(g, status, s);
+    default: return launch_epi<3>(g, status, s);
   }
 }
 

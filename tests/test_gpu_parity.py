@@ -60,6 +60,9 @@ SMALL = {
     # full 256-token tiles and one of 132)
     "prefill_mx_half_down_tile": C["gptoss_prefill_zipf_mxfp4"].scaled(n=900, d=192, d_ff=320,
                                                                        E=4),
+    # d_ff = 352 is not a multiple of the 64-wide k-block: the MXFP4 prefill
+    # takes the CUDA-core kernels
+    "prefill_mx_cuda_core": C["gptoss_prefill_zipf_mxfp4"].scaled(n=500, d=256, d_ff=352, E=8),
     "finegrained_small": C["finegrained_shared_bf16"].scaled(n=500, d=256, d_ff=128, E=32,
                                                              d_ff_shared=192),
 }
