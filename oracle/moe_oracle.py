@@ -34,7 +34,7 @@ states.  Sources (page titles and sections):
   OCP 8-bit floating point specification defines it, with one fp32 scale per
   matrix (the reading taken where the post gives only the block size).
 
-Readings where the pages leave a step open (listed again in the design doc):
+Readings where the pages leave a step open:
 selection ties go to the lower expert index; the Switch (top-1) gate is the
 unrenormalised probability; SwiGLU applies silu to the W1 branch and
 multiplies by the linear W3 branch; the router bias (when present) is part of

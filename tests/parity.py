@@ -1,7 +1,8 @@
 """Helpers shared by the GPU parity tests: run the library, run the oracle on the
 same seeded inputs, and compare under the stated tolerances.
 
-Tolerances (written here, derived in the design doc):
+Tolerances (derived from the arithmetic: bf16 rounding of h and y_perm, fp32
+accumulation, exact MXFP4 decode):
   * routing indices, counts, offsets, perm, inv_perm: bit-exact, except tokens
     whose oracle top-k margin is below NEAR_TIE (listed, then checked for
     validity instead of equality);
