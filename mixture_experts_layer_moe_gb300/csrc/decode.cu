@@ -33,7 +33,61 @@ __global__ void rows_to_f16_kernel(const __nv_bfloat16 *__restrict__ src,
   }
 }
 
+// The same staging in token order: dst[inv_perm[t*k + j]] = f16(src[t]), each
+// x row read and converted once (pairs with inv_perm < 0 skipped, >= P
+// reported).
+constexpr int RF16_VEC = 4;                   // 16-byte vectors per thread in flight
+__global__ void __launch_bounds__(256)
+rows_to_f16_scatter_kernel(const __nv_bfloat16 *__restrict__ src,
+                           const int32_t *__restrict__ inv_perm, int top_k, int n, int P, int K,
+                           uint16_t *__restrict__ dst, int *status) {
+  const int vpr = K / 8;
+  for (int t = blockIdx.x; t < n; t += gridDim.x) {
+    for (int v0 = 0; v0 < vpr; v0 += RF16_VEC * 256) {
+      uint4 o[RF16_VEC];
+#pragma unroll
+      for (int u = 0; u < RF16_VEC; ++u) {
+        const int v = v0 + threadIdx.x + u * 256;
+        if (v < vpr) {
+          const uint4 raw = *reinterpret_cast<const uint4 *>(src + (size_t)t * K + v * 8);
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t h[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xffff0000u);
+            h[j] = (uint32_t)to_f16_bits(lo) | ((uint32_t)to_f16_bits(hi) << 16);
+          }
+          o[u] = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+      }
+      for (int j = 0; j < top_k; ++j) {
+        const int q = inv_perm[(size_t)t * top_k + j];
+        if (q < 0) continue;
+        if (q >= P) {
+          if (threadIdx.x == 0 && v0 == 0) set_status(status, MOE_ERR_BAD_INDEX, t * top_k + j);
+          continue;
+        }
+#pragma unroll
+        for (int u = 0; u < RF16_VEC; ++u) {
+          const int v = v0 + threadIdx.x + u * 256;
+          if (v < vpr) *reinterpret_cast<uint4 *>(dst + (size_t)q * K + v * 8) = o[u];
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_rows_to_f16_scatter(const void *src, const int32_t *inv_perm, int top_k, int n,
+                                       int K, void *dst, int *status, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  int blocks = n < 152 * 8 ? n : 152 * 8;
+  rows_to_f16_scatter_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src),
+                                                    inv_perm, top_k, n, n * top_k, K,
+                                                    static_cast<uint16_t *>(dst), status);
+  return cudaGetLastError();
+}
 
 bool decode_supported(const moe_config &c) {
   return (c.weight_dtype == MOE_MXFP4 || c.weight_dtype == MOE_NVFP4) &&

@@ -340,7 +340,54 @@ gather_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ perm, int
   }
 }
 
+// The same copy in token order: a CTA reads each x row once and writes it to
+// the segment positions of the token's k pairs (inv_perm), so x is read from
+// HBM once however large k is.  Pairs without a position (inv_perm < 0, an
+// out-of-range expert id already reported by the sort) are skipped; their
+// rows lie past every segment and are never read.
+constexpr int SC_VEC = 4;                     // 16-byte vectors per thread in flight
+__global__ void __launch_bounds__(256)
+scatter_rows_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ inv_perm, int P,
+                    int k, int n, int vec_per_row, uint4 *__restrict__ x_perm, int *status) {
+  for (int t = blockIdx.x; t < n; t += gridDim.x) {
+    const uint4 *src = x + (int64_t)t * vec_per_row;
+    for (int v0 = 0; v0 < vec_per_row; v0 += SC_VEC * 256) {
+      uint4 r[SC_VEC];
+#pragma unroll
+      for (int u = 0; u < SC_VEC; ++u) {
+        const int v = v0 + threadIdx.x + u * 256;
+        if (v < vec_per_row) r[u] = src[v];
+      }
+      for (int j = 0; j < k; ++j) {
+        const int q = inv_perm[(int64_t)t * k + j];
+        if (q < 0) continue;
+        if (q >= P) {
+          if (threadIdx.x == 0 && v0 == 0) set_status(status, MOE_ERR_BAD_INDEX, t * k + j);
+          continue;
+        }
+        uint4 *dst = x_perm + (int64_t)q * vec_per_row;
+#pragma unroll
+        for (int u = 0; u < SC_VEC; ++u) {
+          const int v = v0 + threadIdx.x + u * 256;
+          if (v < vec_per_row) dst[v] = r[u];
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_scatter_rows(const void *x, const int32_t *inv_perm, int P, int k, int n,
+                                int64_t row_bytes, void *x_perm, int *status, cudaStream_t s) {
+  if (P == 0 || n == 0) return cudaSuccess;
+  const int vpr = (int)(row_bytes / 16);
+  int blocks = n < 152 * 8 ? n : 152 * 8;
+  if (blocks < 1) blocks = 1;
+  scatter_rows_kernel<<<blocks, 256, 0, s>>>((const uint4 *)x, inv_perm, P, k, n, vpr,
+                                             (uint4 *)x_perm, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_dispatch(int P, int E, const int32_t *topk_idx, int32_t *counts,
                             int32_t *offsets, int32_t *perm, int32_t *inv_perm, int *status,

@@ -62,6 +62,10 @@ cudaError_t launch_dispatch(int P, int E, const int32_t *topk_idx, int32_t *coun
                             cudaStream_t s, void *scratch = nullptr, size_t scratch_bytes = 0);
 
 // x_perm[q] = x[perm[q] / k]; rows of row_bytes (multiple of 16).
+// x_perm[inv_perm[t*k + j]] = x[t] in token order: each x row read once
+// (pairs with inv_perm < 0 skipped, >= P reported).
+cudaError_t launch_scatter_rows(const void *x, const int32_t *inv_perm, int P, int k, int n,
+                                int64_t row_bytes, void *x_perm, int *status, cudaStream_t s);
 cudaError_t launch_gather(const void *x, const int32_t *perm, int P, int k, int n,
                           int64_t row_bytes, void *x_perm, int *status, cudaStream_t s);
 
@@ -125,6 +129,9 @@ bool decode_supported(const moe_config &c);
 // by both MXFP4 paths; 0 for other configurations.
 size_t mx_act16_bytes(const moe_config &c);
 // dst[q] = f16(src[perm[q] / top_k]) (perm given) or f16(src[q]); rows of K.
+// dst[inv_perm[t*k + j]] = f16(src[t]) in token order, each row converted once.
+cudaError_t launch_rows_to_f16_scatter(const void *src, const int32_t *inv_perm, int top_k, int n,
+                                       int K, void *dst, int *status, cudaStream_t s);
 cudaError_t launch_rows_to_f16(const void *src, const int32_t *perm, int top_k, int P, int K,
                                void *dst, int *status, cudaStream_t s);
 // part 0 with act == nullptr: act16 already holds the f16 x rows in token order

@@ -179,10 +179,10 @@ bool mx_tc_path(const moe_config &c) {
 }
 
 // MXFP4 prefill on tensor cores: f16 copies of the expert-ordered rows (x
-// through perm, or x_perm), then the up and down grouped GEMMs with on-the-fly
-// dequantisation.
+// scattered in token order through inv_perm, or x_perm converted in place),
+// then the up and down grouped GEMMs with on-the-fly dequantisation.
 template <typename StageFn>
-moe_status run_mx_ffn(const moe_config &c, const void *act, const int32_t *perm,
+moe_status run_mx_ffn(const moe_config &c, const void *act, const int32_t *inv_perm,
                       const int32_t *offsets, const moe_weights *w, void *y_perm, void *ws,
                       cudaStream_t s, StageFn &&stage) {
   const Layout L = layout_of(c);
@@ -190,8 +190,12 @@ moe_status run_mx_ffn(const moe_config &c, const void *act, const int32_t *perm,
   GemmStage up, dn;
   mx_stages(c, offsets, w, ws, y_perm, up, dn);
   stage(MOE_STAGE_FFN_UP, 2);
-  MOE_TRY(cuda_status(launch_rows_to_f16(act, perm, c.top_k, c.n * c.top_k, c.d,
-                                         at<void>(ws, L.act16), status, s)));
+  if (inv_perm)
+    MOE_TRY(cuda_status(launch_rows_to_f16_scatter(act, inv_perm, c.top_k, c.n, c.d,
+                                                   at<void>(ws, L.act16), status, s)));
+  else
+    MOE_TRY(cuda_status(launch_rows_to_f16(act, nullptr, c.top_k, c.n * c.top_k, c.d,
+                                           at<void>(ws, L.act16), status, s)));
   MOE_TRY(cuda_status(launch_gemm_tc(up, status, s)));
   stage(MOE_STAGE_FFN_DOWN, 1);
   return cuda_status(launch_gemm_tc(dn, status, s));
@@ -498,10 +502,11 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
                                           s)));
   } else if (mx_tc) {
     // prefill over MXFP4 weights: the f16 staging gathers the rows itself
-    MOE_TRY(run_mx_ffn(c, x, perm, offsets, w, at<void>(ws, L.y_perm), ws, s, stage));
+    MOE_TRY(run_mx_ffn(c, x, inv_perm, offsets, w, at<void>(ws, L.y_perm), ws, s, stage));
   } else {
-    MOE_TRY(cuda_status(launch_gather(x, perm, P, c.top_k, c.n, (int64_t)c.d * act_size(c),
-                                      at<void>(ws, L.x_perm), status, s)));
+    MOE_TRY(cuda_status(launch_scatter_rows(x, inv_perm, P, c.top_k, c.n,
+                                            (int64_t)c.d * act_size(c), at<void>(ws, L.x_perm),
+                                            status, s)));
     MOE_TRY(run_expert_ffn(c, at<void>(ws, L.x_perm), offsets, w, at<void>(ws, L.y_perm), ws, s,
                            stage));
   }
