@@ -328,6 +328,41 @@ def test_expert_ffn_segments(lib, name):
     parity.check_output(cfg, y_perm, want)
 
 
+# Segment sizes on both sides of the tile boundaries of the grouped GEMMs (128
+# rows per tile; MMA N rounded up to 16 in the MXFP4 kernel), given directly
+# as offsets so that every size occurs.
+TILE_EDGE_SIZES = [0, 1, 15, 16, 17, 127, 128, 129, 255, 256, 257, 300]
+
+
+@pytest.mark.parametrize("name", ["mixtral", "mxfp4"])
+def test_expert_ffn_tile_edges(lib, name):
+    sizes = TILE_EDGE_SIZES
+    P = sum(sizes)
+    if name == "mixtral":
+        cfg = C["mixtral_bf16"].scaled(n=P, d=256, d_ff=384, E=len(sizes), k=1)
+    else:
+        cfg = C["gptoss_prefill_zipf_mxfp4"].scaled(n=P, d=256, d_ff=320, E=len(sizes), k=1)
+    inputs = moe_synth.make_inputs(cfg, seed=11, device="cuda")
+    oin = parity.oracle_inputs(inputs)
+    off = [0]
+    for c in sizes:
+        off.append(off[-1] + c)
+    x_perm = inputs["x"].contiguous()          # any rows: the segments are given
+    y_perm = torch.empty_like(x_perm)
+    ws = lib.alloc_workspace(cfg)
+    lib.moe_expert_ffn(cfg, x_perm, torch.tensor(off, dtype=torch.int32, device="cuda"),
+                       lib.make_weights(inputs), y_perm, ws)
+    assert lib.moe_status_check(ws)[0] == 0
+    want = torch.empty(P, cfg.d, dtype=torch.float64)
+    xp = O.to_f64(x_perm.cpu())
+    for e in range(cfg.E):
+        if off[e] == off[e + 1]:
+            continue
+        W1, W3, W2 = O.expert_weights(oin, cfg, e)
+        want[off[e]:off[e + 1]] = O.expert_ffn(xp[off[e]:off[e + 1]], W1, W2, cfg.act, W3)
+    parity.check_output(cfg, y_perm, want)
+
+
 # ------------------------------------------------------- routing statistics
 
 @pytest.mark.parametrize("name", ["mixtral_small", "prefill_zipf_small", "finegrained_small"])
