@@ -325,6 +325,15 @@ moe_status moe_status_clear(void *ws, void *stream);
 /* Static string for a status code. */
 const char *moe_status_string(moe_status s);
 
+/* Diagnostics for the device-side failure path.  Launches one warp that waits,
+ * with the same bounded wait the pipeline kernels use, on a barrier nothing
+ * arrives on; after limit_ns (1 .. 1e9) the wait gives up and the kernel sets
+ * MOE_ERR_TIMEOUT in the workspace status word (ws: a layer workspace, 256-byte
+ * aligned) and exits, leaving the context usable.  Asynchronous on stream;
+ * read the result with moe_status_check.  MOE_ERR_INVALID_ARG for a bad ws or
+ * limit. */
+moe_status moe_selftest_wait_timeout(void *ws, uint64_t limit_ns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

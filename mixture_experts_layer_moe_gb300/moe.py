@@ -83,6 +83,7 @@ def _load() -> ctypes.CDLL:
         "moe_forward_pooled_staged": [cfgp, P, wp, pp, P, P, P, P, P, SZ, P, STAGE_HOOK, P],
         "moe_status_check": [P, P, ctypes.POINTER(ctypes.c_int32)],
         "moe_status_clear": [P, P],
+        "moe_selftest_wait_timeout": [P, ctypes.c_uint64, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -264,6 +265,11 @@ def moe_status_check(ws, stream=None) -> tuple[int, int]:
 
 def moe_status_clear(ws, stream=None):
     _check(_lib.moe_status_clear(_ptr(ws), _stream(stream)), "moe_status_clear")
+
+
+def moe_selftest_wait_timeout(ws, limit_ns: int, stream=None):
+    _check(_lib.moe_selftest_wait_timeout(_ptr(ws), int(limit_ns), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def raw_call(name: str, *args) -> int:

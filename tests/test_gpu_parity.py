@@ -403,3 +403,18 @@ def test_route_stats_page_example(lib):
     assert lib.moe_status_check(ws)[0] == 0
     assert f.tolist() == [1.0, 0.0, 0.0, 0.0]
     assert abs(aux.item() - 2.33) < 1e-6 and round(aux.item(), 2) == 2.33
+
+
+# ------------------------------------------------------- failure detection
+
+def test_wait_timeout_reported(lib):
+    """A bounded device wait that nothing completes ends by itself with
+    MOE_ERR_TIMEOUT in the status word, and the context stays usable."""
+    cfg = SMALL["mixtral_small"]
+    ws = lib.alloc_workspace(cfg)
+    lib.moe_status_clear(ws)
+    lib.moe_selftest_wait_timeout(ws, 20_000_000)       # 20 ms
+    assert lib.moe_status_check(ws) == (6, -1)
+    lib.moe_status_clear(ws)
+    res = parity.full_parity(lib, cfg, seed=3)
+    assert res["err"] < 2e-2
