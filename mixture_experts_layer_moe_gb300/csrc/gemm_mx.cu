@@ -49,14 +49,11 @@ constexpr int GM = 128;                         // weight rows per tile (MMA M)
 constexpr int GN = 128;                         // tokens per tile at most (MMA N)
 constexpr int GK = 64;                          // k-block
 constexpr int GS = 4;                           // pipeline stages
-constexpr int G_BOX = GN;                       // token rows per TMA box (one box per k-block)
-constexpr int G_BOX_BYTES = G_BOX * GK * 2;     // 16 KB
 constexpr int G_B_BYTES = GN * GK * 2;          // token tile: 16 KB
 constexpr int G_C_BYTES = GM * GK / 2;          // codes of the k-block: 4 KB
 constexpr int G_STAGE = G_B_BYTES + G_C_BYTES;  // 20 KB
 constexpr int G_XFORM = 4;                      // transform warps
 constexpr int G_EPI = 4;                        // epilogue warps
-constexpr int G_TOK_PER_EPI = GN * 4 / G_EPI;   // tokens an epilogue warp drains
 constexpr int G_THREADS = 32 * (2 + G_EPI + G_XFORM);
 constexpr uint32_t G_TMEM_COLS = 256;           // two CTAs per SM
 constexpr uint32_t G_A_COL0 = GN;               // A stages after the accumulator
@@ -303,8 +300,6 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       for (int s = 0; s < GS; ++s) last_phase[s] = -1;
       for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
         const GTile tl = g_decode(sh, E, t);
-        const int ntok = min(GN, tl.seg_end - tl.row0);
-        const int nbox = (ntok + G_BOX - 1) / G_BOX;
         const int r_lo = tl.n_idx * N_OUT;
         const int r_hi = (EPI == 2) ? r_lo : r_lo + GM / 2;
         const bool hi_ok = EPI == 2 && r_hi < args.N;  // SwiGLU: the W3 box
@@ -312,10 +307,8 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
           if (!tc::mbar_wait(&sh.empty[stage], phase ^ 1u, abort)) break;
           uint8_t *sb = smem + stage * G_STAGE;
           uint8_t *sc = sb + G_B_BYTES;
-          tc::mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)(nbox * G_BOX_BYTES + G_C_BYTES));
-          for (int j = 0; j < nbox; ++j)
-            tc::tma_load_2d(&tmX, &sh.full[stage], sb + j * G_BOX_BYTES, kb * GK,
-                            tl.row0 + j * G_BOX);
+          tc::mbar_arrive_expect_tx(&sh.full[stage], (uint32_t)(G_B_BYTES + G_C_BYTES));
+          tc::tma_load_2d(&tmX, &sh.full[stage], sb, kb * GK, tl.row0);
           tc::tma_load_3d(&tmW, &sh.full[stage], sc, kb * (GK / 2), r_lo, tl.e);
           if (hi_ok)
             tc::tma_load_3d(EPI == 2 ? &tmW3 : &tmW, &sh.full[stage], sc + G_C_BYTES / 2,
@@ -365,14 +358,11 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       }
     }
   } else if (warp < 2 + G_EPI) {
-    // ---------------- epilogue: warp w drains TMEM lanes 32*(w%4) .. +31 over
-    // one 128-token half of the tile, 32 tokens per chunk, into bf16 pairs held
-    // in registers; the accumulator is then released and each thread writes
-    // its output column for its tokens (a warp's stores of one token are 64
-    // contiguous bytes, 2 x 32 for SwiGLU)
+    // ---------------- epilogue: warp w drains TMEM lanes 32*(w%4) .. +31, 32
+    // tokens per chunk, into bf16 pairs held in registers; the accumulator is
+    // then released and each thread writes its output column for its tokens
+    // (a warp's stores of one token are 64 contiguous bytes, 2 x 32 for SwiGLU)
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
-    const int tok_half = half * G_TOK_PER_EPI;
     const bool low = lane < 16;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
     int local = 0;
@@ -382,14 +372,13 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       const bool ok = tc::mbar_wait(&sh.tfull, local & 1, abort);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc::tc_fence_after();
-      const int my_end = min(ntok, tok_half + G_TOK_PER_EPI);   // this warp's tokens: [tok_half, my_end)
       // bf16 pairs: packed[c][q] = tokens 2q, 2q+1 of chunk c (SwiGLU: of the
       // lane's 16 tokens of the chunk, q < 8)
       uint32_t packed[4][EPI == 2 ? 8 : 16];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int col0 = tok_half + c * 32;
-        if (col0 < my_end) {
+        const int col0 = c * 32;
+        if (col0 < ntok) {
           if constexpr (EPI == 2) {
             uint32_t a[32];
             tc::tmem_ld32(lane_base + (uint32_t)col0, a);
@@ -437,8 +426,8 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         uint16_t *o = reinterpret_cast<uint16_t *>(args.out);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          if (tok_half + c * 32 < my_end) {
-            const int tok0 = tl.row0 + tok_half + c * 32 + tsub;
+          if (c * 32 < ntok) {
+            const int tok0 = tl.row0 + c * 32 + tsub;
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
               const int tok = tok0 + i;
@@ -568,7 +557,7 @@ cudaError_t launch_mx(const GemmStage &g, int *status, cudaStream_t s) {
   }
   CUtensorMap mX, mW, mW3;
   const uint64_t dX[2] = {(uint64_t)g.K, (uint64_t)g.rows};
-  const uint32_t bX[2] = {GK, G_BOX};
+  const uint32_t bX[2] = {GK, GN};
   if (!make_tensor_map(&mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.A, 2, dX, bX,
                        CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
