@@ -112,6 +112,95 @@ combine_kernel(const uint4 *__restrict__ y_perm, const int32_t *__restrict__ inv
   }
 }
 
+// Row-oriented variant: CTA (t, c) takes vectors [c * 256 * VB, ...) of token
+// t's row.  The token's k inverse indices and gates are loaded once into
+// shared memory; a thread then loads its VB vectors of the rows CR_SLOTS
+// slots at a time before summing them in slot order, as above.
+constexpr int CR_SLOTS = 4;
+template <typename T, int VB>
+__global__ void __launch_bounds__(256)
+combine_rows_kernel(const uint4 *__restrict__ y_perm, const int32_t *__restrict__ inv_perm,
+                    const float *__restrict__ gates, const uint4 *__restrict__ y_shared,
+                    uint4 *__restrict__ y, int n, int k, int vec_per_row, int *status) {
+  constexpr int V = Vec16<T>::N;
+  __shared__ int s_q[256];
+  __shared__ float s_g[256];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int P = n * k;
+  const int t = blockIdx.x;
+  for (int j = threadIdx.x; j < k; j += blockDim.x) {
+    int q = inv_perm[(int64_t)t * k + j];
+    if (q < 0 || q >= P) {
+      if (blockIdx.y == 0) set_status(status, MOE_ERR_BAD_INDEX, t * k + j);
+      q = -1;
+    }
+    s_q[j] = q;
+    s_g[j] = gates[(int64_t)t * k + j];
+  }
+  __syncthreads();
+  const int v0 = blockIdx.y * 256 * VB + threadIdx.x;
+  float acc[VB][V];
+#pragma unroll
+  for (int b = 0; b < VB; ++b)
+#pragma unroll
+    for (int c = 0; c < V; ++c) acc[b][c] = 0.f;
+  for (int j0 = 0; j0 < k; j0 += CR_SLOTS) {
+    uint4 r[CR_SLOTS][VB];
+#pragma unroll
+    for (int u = 0; u < CR_SLOTS; ++u) {
+      const int q = (j0 + u < k) ? s_q[j0 + u] : -1;
+#pragma unroll
+      for (int b = 0; b < VB; ++b)
+        if (q >= 0 && v0 + b * 256 < vec_per_row)
+          r[u][b] = y_perm[(int64_t)q * vec_per_row + v0 + b * 256];
+    }
+#pragma unroll
+    for (int u = 0; u < CR_SLOTS; ++u) {
+      if (j0 + u >= k || s_q[j0 + u] < 0) continue;
+      const float g = s_g[j0 + u];
+#pragma unroll
+      for (int b = 0; b < VB; ++b) {
+        if (v0 + b * 256 < vec_per_row) {
+          float f[V];
+          unpack16<T>(r[u][b], f);
+#pragma unroll
+          for (int c = 0; c < V; ++c) acc[b][c] = fmaf(g, f[c], acc[b][c]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < VB; ++b) {
+    const int v = v0 + b * 256;
+    if (v < vec_per_row) {
+      const int64_t i = (int64_t)t * vec_per_row + v;
+      if (y_shared) {
+        float f[V];
+        unpack16<T>(y_shared[i], f);
+#pragma unroll
+        for (int c = 0; c < V; ++c) acc[b][c] += f[c];
+      }
+      y[i] = pack16<T>(acc[b]);
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_rows(const void *y_perm, const int32_t *inv_perm, const float *gates,
+                        const void *y_shared, void *y, int n, int k, int vpr, int *status,
+                        cudaStream_t s) {
+  // two vectors per thread where that still leaves two CTAs per SM
+  const bool two = (int64_t)n * ((vpr + 511) / 512) >= 2 * 152;
+  if (two)
+    return launch_pdl(combine_rows_kernel<T, 2>, dim3((unsigned)n, (unsigned)((vpr + 511) / 512)),
+                      dim3(256), 0, s, (const uint4 *)y_perm, inv_perm, gates,
+                      (const uint4 *)y_shared, (uint4 *)y, n, k, vpr, status);
+  return launch_pdl(combine_rows_kernel<T, 1>, dim3((unsigned)n, (unsigned)((vpr + 255) / 256)),
+                    dim3(256), 0, s, (const uint4 *)y_perm, inv_perm, gates,
+                    (const uint4 *)y_shared, (uint4 *)y, n, k, vpr, status);
+}
+
 }  // namespace
 
 cudaError_t launch_combine(int act_dtype, const void *y_perm, const int32_t *inv_perm,
@@ -119,6 +208,13 @@ cudaError_t launch_combine(int act_dtype, const void *y_perm, const int32_t *inv
                            int d, int *status, cudaStream_t s) {
   const int esz = act_dtype == MOE_F32 ? 4 : 2;
   const int vpr = d * esz / 16;
+  // row-oriented once there are rows enough to fill the GPU (k <= 256: the
+  // indices fit shared memory)
+  if (n >= 2 * 152 && k <= 256) {
+    if (act_dtype == MOE_F32)
+      return launch_rows<float>(y_perm, inv_perm, gates, y_shared, y, n, k, vpr, status, s);
+    return launch_rows<__nv_bfloat16>(y_perm, inv_perm, gates, y_shared, y, n, k, vpr, status, s);
+  }
   const int64_t total = (int64_t)n * vpr;
   int64_t blocks = (total + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
