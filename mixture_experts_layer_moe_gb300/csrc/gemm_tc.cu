@@ -29,11 +29,22 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int THREADS = 192;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int DYN_SMEM = STAGES * STAGE_BYTES + 1024;
+constexpr int MAX_STAGES = 10;
+
+// Ring depth per variant: the router variants stage narrower B tiles, so the
+// same shared memory holds more k-blocks in flight (their A stream is the
+// whole cost of the router, and it is latency-bound at four stages).
+__host__ __device__ constexpr int stage_bytes(int epi) {
+  return A_BYTES + (epi == 4 ? 32 : (epi == 3 ? 128 : BN)) * BK * 2;
+}
+__host__ __device__ constexpr int num_stages(int epi) { return epi == 4 ? MAX_STAGES : (epi == 3 ? 6 : STAGES); }
+__host__ __device__ constexpr int dyn_smem_bytes(int epi) { return num_stages(epi) * stage_bytes(epi) + 1024; }
+// Epilogue warps: the 128-expert router drains a 128-column partial every
+// k-block, so two warps share each TMEM lane quarter (64 columns each).
+__host__ __device__ constexpr int epi_warps(int epi) { return epi == 3 ? 8 : 4; }
+__host__ __device__ constexpr int threads_of(int epi) { return 64 + 32 * epi_warps(epi); }
 constexpr int MAX_E = 256;
 constexpr uint32_t TMEM_COLS = 512;
 
@@ -46,13 +57,14 @@ struct TcArgs {
   void *out;       // bf16 [rows][N], fp32 for EPI 3
   const float *bias;
   int *status;
+  int ksplit;      // router: k ranges per row tile (> 1: partial sums, no bias)
 };
 
 struct TcShared {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
+  uint64_t tfull[8];    // accumulator ring: 2 (8 for the 32-column router)
+  uint64_t tempty[8];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -100,15 +112,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // instead drifted by ~2e-5 on d = 4096 rows, too close to the 1e-5 near-tie
 // margin of the routing decision.
 template <int EPI>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(threads_of(EPI), 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmB3, TcArgs args) {
-  constexpr bool KPART = (EPI == 3);                 // per-k-block partials
-  constexpr int BNT = KPART ? 128 : BN;              // MMA N = B rows per stage
+  constexpr bool KPART = (EPI == 3 || EPI == 4);    // per-k-block partials
+  // MMA N = B rows per stage: the router takes 128 experts per tile, or 32
+  // (EPI 4) when there are at most 32, so a layer with 8 experts does not
+  // drain 128 accumulator columns per k-block
+  constexpr int BNT = KPART ? (EPI == 4 ? 32 : 128) : BN;
+  // accumulators in flight and their TMEM column pitch: the routers keep
+  // four (128 columns) or eight (32 columns) partials in flight so the MMAs
+  // run ahead of the epilogue's drains
+  constexpr int NACC = (EPI == 4) ? 8 : (EPI == 3 ? 4 : 2);
+  constexpr int ACC_COLS = KPART ? BNT : BN;
+  constexpr int EPI_WARPS = epi_warps(EPI);
   constexpr int N_OUT = (EPI == 2) ? BN / 2 : BNT;   // output columns per tile
-  constexpr int NSTAGE = STAGES;
-  constexpr int SBYTES = STAGE_BYTES;
-  constexpr int NTHREADS = THREADS;
+  constexpr int NSTAGE = num_stages(EPI);
+  constexpr int SBYTES = stage_bytes(EPI);
+  constexpr int NTHREADS = threads_of(EPI);
   constexpr uint32_t TX_BYTES = A_BYTES + BNT * BK * 2;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ TcShared sh;
@@ -117,6 +138,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int E = args.offsets ? args.num_experts : 1;
   const int n_tiles = (args.N + N_OUT - 1) / N_OUT;
   const int KB = (args.K + BK - 1) / BK;
+  // work unit t: row/column tile t / KS over k-blocks [k_begin, k_end)
+  const int KS = KPART ? args.ksplit : 1;
+  auto k_begin = [&](int t) { return (int)((int64_t)(t % KS) * KB / KS); };
+  auto k_end = [&](int t) { return (int)((int64_t)(t % KS + 1) * KB / KS); };
 
   if (threadIdx.x == 0) {
     sh.failed_on_entry = status_failed(args.status) ? 1 : 0;
@@ -130,9 +155,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc::mbar_init(&sh.full[s], 1);
       tc::mbar_init(&sh.empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < NACC; ++a) {
       tc::mbar_init(&sh.tfull[a], 1);
-      tc::mbar_init(&sh.tempty[a], 128);
+      tc::mbar_init(&sh.tempty[a], 32 * EPI_WARPS);
     }
     tc::mbar_init(&sh.drain, 1);
     tc::fence_mbar_init();
@@ -169,7 +194,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int total = __shfl_sync(0xffffffffu, incl, 31);
     bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
-      sh.num_tiles = bad ? 0 : total;
+      sh.num_tiles = bad ? 0 : total * (KPART ? args.ksplit : 1);
       if (bad) set_status(args.status, MOE_ERR_BAD_INDEX, -1);
     }
   }
@@ -188,13 +213,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (EPI == 2) tc::prefetch_tmap(&tmB3);
       int stage = 0;
       uint32_t phase = 0;
-      int last_phase[STAGES];
+      int last_phase[NSTAGE];
 #pragma unroll
-      for (int s = 0; s < STAGES; ++s) last_phase[s] = -1;
+      for (int s = 0; s < NSTAGE; ++s) last_phase[s] = -1;
       for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
-        const Tile tl = decode_tile(sh, E, t);
+        const Tile tl = decode_tile(sh, E, t / KS);
         const int wrow = tl.n_idx * N_OUT;
-        for (int kb = 0; kb < KB; ++kb) {
+        const int kb1 = k_end(t);
+        for (int kb = k_begin(t); kb < kb1; ++kb) {
           if (!tc::mbar_wait(&sh.empty[stage], phase ^ 1u, abort)) break;
           uint8_t *sa = smem + stage * SBYTES;
           uint8_t *sb = sa + A_BYTES;
@@ -226,15 +252,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int local = 0;   // accumulator uses so far (tiles, or k-blocks with KPART)
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok && !*abort; t += gridDim.x) {
-        for (int kb = 0; kb < KB; ++kb) {
+        const int kb1 = k_end(t);
+        for (int kb = k_begin(t); kb < kb1; ++kb) {
           const bool fresh = KPART || kb == 0;
-          const int acc = local & 1;
+          const int acc = local % NACC;
           if (fresh) {
-            const uint32_t acc_phase = (local >> 1) & 1;
+            const uint32_t acc_phase = (local / NACC) & 1;
             if (!tc::mbar_wait(&sh.tempty[acc], acc_phase ^ 1u, abort)) { ok = false; break; }
             tc::tc_fence_after();
           }
-          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
           if (!tc::mbar_wait(&sh.full[stage], phase, abort)) { ok = false; break; }
           tc::tc_fence_after();
           const uint32_t sa = tc::smem_u32(smem + stage * SBYTES);
@@ -256,43 +283,52 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tc::mbar_wait_drain(&sh.drain, 0, 100000000ull);
       }
     }
-  } else if (warp < 6) {
-    // ---------------- epilogue: warps 2..5; warp w reads TMEM lanes 32*(w%4)..
+  } else if (warp < 2 + EPI_WARPS) {
+    // ---------------- epilogue: warps 2..; warp w reads TMEM lanes 32*(w%4)..
     const int quarter = warp & 3;
     const int r_local = quarter * 32 + lane;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
     int local = 0;
     if constexpr (KPART) {
+      // the warps of one lane quarter split the columns: NCOL from col_off
+      constexpr int NCOL = N_OUT / (EPI_WARPS / 4);
+      const int col_off = ((warp - 2) >> 2) * NCOL;
       for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-        const Tile tl = decode_tile(sh, E, t);
-        float sum[N_OUT];
+        const Tile tl = decode_tile(sh, E, t / KS);
+        float sum[NCOL];
 #pragma unroll
-        for (int i = 0; i < N_OUT; ++i) sum[i] = 0.f;
+        for (int i = 0; i < NCOL; ++i) sum[i] = 0.f;
         bool ok = true;
-        for (int kb = 0; kb < KB; ++kb, ++local) {
-          const int acc = local & 1;
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(&sh.tfull[acc], (local >> 1) & 1, abort));
+        const int kb1 = k_end(t);
+        for (int kb = k_begin(t); kb < kb1; ++kb, ++local) {
+          const int acc = local % NACC;
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(&sh.tfull[acc], (local / NACC) & 1, abort));
           if (!ok) break;
           tc::tc_fence_after();
+          uint32_t a[NCOL / 32][32];
 #pragma unroll
-          for (int c = 0; c < N_OUT / 32; ++c) {
-            uint32_t a[32];
-            tc::tmem_ld32(lane_base + (uint32_t)(acc * BN) + c * 32, a);
-            tc::tmem_ld_wait();
+          for (int c = 0; c < NCOL / 32; ++c)
+            tc::tmem_ld32(lane_base + (uint32_t)(acc * ACC_COLS + col_off + c * 32), a[c]);
+          tc::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sum[c * 32 + i] += __uint_as_float(a[i]);
-          }
+          for (int c = 0; c < NCOL / 32; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sum[c * 32 + i] += __uint_as_float(a[c][i]);
           tc::tc_fence_before();
           tc::mbar_arrive(&sh.tempty[acc]);
         }
         if (!ok) break;
         const int row = tl.row0 + r_local;
         if (row < tl.seg_end) {
-          float *orow = static_cast<float *>(args.out) + (size_t)row * args.N;
+          // k range p of a split writes its partial sums to plane p; the
+          // reader adds the planes in order, then the bias
+          const int p = t % KS;
+          float *orow = static_cast<float *>(args.out) + ((size_t)p * args.rows + row) * args.N;
+          const float *bias = KS > 1 ? nullptr : args.bias;
 #pragma unroll
-          for (int i = 0; i < N_OUT; ++i) {
-            const int col = tl.n_idx * N_OUT + i;
-            if (col < args.N) orow[col] = sum[i] + (args.bias ? args.bias[col] : 0.f);
+          for (int i = 0; i < NCOL; ++i) {
+            const int col = tl.n_idx * N_OUT + col_off + i;
+            if (col < args.N) orow[col] = sum[i] + (bias ? bias[col] : 0.f);
           }
         }
         __syncwarp();
@@ -365,7 +401,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
 template <int EPI>
 cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
-  const size_t smem = (size_t)DYN_SMEM;
+  const size_t smem = (size_t)dyn_smem_bytes(EPI);
   static size_t smem_set = 0;
   if (smem > smem_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI>,
@@ -377,7 +413,7 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
   CUtensorMap mA, mB, mB3;
   const uint64_t dA[2] = {(uint64_t)g.K, (uint64_t)g.rows};
   const uint32_t bA[2] = {BK, BM};
-  const int wrows = (EPI == 2) ? BN / 2 : (EPI == 3 ? 128 : BN);
+  const int wrows = (EPI == 2) ? BN / 2 : (EPI == 3 ? 128 : (EPI == 4 ? 32 : BN));
   if (!make_tensor_map(&mA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.A, 2, dA, bA,
                        CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
@@ -402,7 +438,8 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
   a.out = g.out;
   a.bias = g.col_bias;
   a.status = status;
-  gemm_tc_kernel<EPI><<<num_sms(), THREADS, smem, s>>>(mA, mB, mB3, a);
+  a.ksplit = (EPI == 3 || EPI == 4) && g.ksplit > 1 ? g.ksplit : 1;
+  gemm_tc_kernel<EPI><<<num_sms(), threads_of(EPI), smem, s>>>(mA, mB, mB3, a);
   return cudaGetLastError();
 }
 
@@ -414,7 +451,21 @@ bool gemm_tc_supported(const GemmStage &g) {
   if (g.b_dtype == MOE_MXFP4) return gemm_mx_supported(g);
   const bool out_ok = g.epi == 3 ? g.out_dtype == MOE_F32 : g.out_dtype == MOE_BF16;
   const bool n_ok = g.epi == 3 ? true : g.N % 8 == 0;
+  // (epi 3 with N <= 32 runs as the 32-column router variant)
   return g.a_dtype == MOE_BF16 && g.b_dtype == MOE_BF16 && out_ok && n_ok && g.K % 8 == 0;
+}
+
+int gemm_tc_router_ksplit(const GemmStage &g, size_t plane_room) {
+  // row tiles x expert tiles of the router; when they cover less than half
+  // the SMs, each tile's d range is split over up to four CTAs (at least
+  // eight k-blocks each), as far as the partial planes fit in plane_room
+  const int tiles = ((g.rows + BM - 1) / BM) * (g.N <= 32 ? 1 : (g.N + 127) / 128);
+  const int kb = (g.K + BK - 1) / BK;
+  int ks = num_sms() / tiles;
+  ks = ks > 4 ? 4 : ks;
+  ks = ks > kb / 8 ? kb / 8 : ks;
+  while (ks > 1 && (size_t)ks * g.rows * g.N * sizeof(float) > plane_room) --ks;
+  return ks < 2 ? 1 : ks;
 }
 
 cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s) {
@@ -423,7 +474,7 @@ cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s) {
     case 0: return launch_epi<0>(g, status, s);
     case 1: return launch_epi<1>(g, status, s);
     case 2: return launch_epi<2>(g, status, s);
-    default: return launch_epi<3>(g, status, s);
+    default: return g.N <= 32 ? launch_epi<4>(g, status, s) : launch_epi<3>(g, status, s);
   }
 }
 

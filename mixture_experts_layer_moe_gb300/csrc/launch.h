@@ -39,9 +39,11 @@ bool make_tensor_map(CUtensorMap *m, CUtensorMapDataType dtype, int elem_bytes, 
 int num_sms();
 
 // Router: logits (fp32 [n][E] scratch) -> softmax -> top-k -> gates.
+// parts (nullable, parts_bytes long) is scratch for partial logits when the
+// tensor-core router splits its reduction over more SMs.
 cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, const float *bias,
-                         float *logits, int32_t *topk_idx, float *topk_gate, float *probs,
-                         int *status, cudaStream_t s);
+                         float *logits, float *parts, size_t parts_bytes, int32_t *topk_idx,
+                         float *topk_gate, float *probs, int *status, cudaStream_t s);
 // The router's linear layer alone: logits [n][E] fp32.
 cudaError_t launch_route_logits(const moe_config &c, const void *x, const void *Wg,
                                 const float *bias, float *logits, int *status, cudaStream_t s);
@@ -99,6 +101,8 @@ struct GemmStage {
   void *out;            // [rows][N]
   const float *col_bias; // epi 3: per-column bias or nullptr
   void *out16;          // MXFP4 path: f16 copy of out (next projection's input) or nullptr
+  int ksplit;           // epi 3 on tensor cores: k ranges per row tile; > 1 writes
+                        // partial sums to planes out[p][rows][N] without the bias
 };
 cudaError_t launch_gemm_simt(const GemmStage &g, int *status, cudaStream_t s);
 
@@ -106,6 +110,9 @@ cudaError_t launch_gemm_simt(const GemmStage &g, int *status, cudaStream_t s);
 // TMEM, TMA-fed); gemm_tc_supported() says whether the shape/dtypes qualify.
 bool gemm_tc_supported(const GemmStage &g);
 cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s);
+// Split of the router's reduction that fills the SMs (1: no split), given
+// room in bytes for the fp32 partial planes.
+int gemm_tc_router_ksplit(const GemmStage &g, size_t plane_room);
 // MXFP4 grouped GEMM with the dequantised weights as the tcgen05 A operand in
 // tensor memory (f16 activation copies in, bf16 out; epi 0, 1 or 2).
 bool gemm_mx_supported(const GemmStage &g);

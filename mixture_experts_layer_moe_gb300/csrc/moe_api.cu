@@ -378,8 +378,11 @@ moe_status moe_route(const moe_config *cfg, const void *x, const moe_weights *w,
   if (probs != nullptr && !aligned(probs, 16)) return MOE_ERR_INVALID_ARG;
   MOE_TRY(check_ws(c, ws, ws_bytes));
   const Layout L = layout_of(c);
-  return cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits), topk_idx,
-                                  topk_gate, probs, at<int>(ws, L.status), as_stream(stream)));
+  // (the h region is scratch for the router's partial logits)
+  return cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits),
+                                  at<float>(ws, L.h), (size_t)c.n * c.top_k * c.d_ff * h_size(c),
+                                  topk_idx, topk_gate, probs, at<int>(ws, L.status),
+                                  as_stream(stream)));
 }
 
 moe_status moe_route_stats(const moe_config *cfg, const float *probs, const int32_t *topk_idx,
@@ -483,10 +486,12 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
   if (decode && decode_route_supported(c))
     return run_small_batch(c, x, w, nullptr, y, nullptr, nullptr, nullptr, ws, s, stage);
   stage(MOE_STAGE_ROUTE, 2);
-  MOE_TRY(cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits), topk_idx,
+  // (the h buffer is free until the FFN: scratch for the router's partial
+  // logits, then for a many-CTA sort)
+  MOE_TRY(cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits),
+                                   at<float>(ws, L.h), (size_t)P * c.d_ff * h_size(c), topk_idx,
                                    gates, nullptr, status, s)));
   stage(MOE_STAGE_DISPATCH, (decode || mx_tc) ? 1 : 2);
-  // (the h buffer is free until the FFN: scratch for a many-CTA sort)
   MOE_TRY(cuda_status(launch_dispatch(P, c.n_experts, topk_idx, at<int32_t>(ws, L.counts), offsets,
                                       perm, inv_perm, status, s, at<void>(ws, L.h),
                                       (size_t)P * c.d_ff * h_size(c))));

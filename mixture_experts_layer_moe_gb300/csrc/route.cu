@@ -157,23 +157,39 @@ route_logits_small_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat
   if (lane < nt) logits[(size_t)(t0 + lane) * E + e] = mine + (bias ? bias[e] : 0.f);
 }
 
-// One warp per token (selection and gates as in select_topk_warp).
+// One warp per token (selection and gates as in select_topk_warp).  With
+// nparts > 0 the logits are first assembled from the router's partial planes
+// parts[p][n][E], added in plane order, then the bias; they are stored to
+// logits before the selection reads them.
 __global__ void __launch_bounds__(256)
-route_select_kernel(const float *__restrict__ logits, int n, int E, int k, int gate_mode,
+route_select_kernel(float *__restrict__ logits, const float *__restrict__ parts, int nparts,
+                    const float *__restrict__ bias, int n, int E, int k, int gate_mode,
                     int32_t *__restrict__ topk_idx, float *__restrict__ topk_gate,
                     float *__restrict__ probs) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= n) return;
+  if (nparts > 0) {
+    for (int e = lane; e < E; e += 32) {
+      float v = parts[(size_t)warp * E + e];
+      for (int p = 1; p < nparts; ++p) v += parts[((size_t)p * n + warp) * E + e];
+      logits[(size_t)warp * E + e] = v + (bias ? bias[e] : 0.f);
+    }
+    __syncwarp();
+  }
   select_topk_warp(logits + (size_t)warp * E, E, k, gate_mode, lane, topk_idx + (size_t)warp * k,
                    topk_gate + (size_t)warp * k, probs ? probs + (size_t)warp * E : nullptr);
 }
 
 }  // namespace
 
-cudaError_t launch_route_logits(const moe_config &c, const void *x, const void *Wg,
-                                const float *bias, float *logits, int *status, cudaStream_t s) {
+// The router's linear layer into logits, or (return value nparts > 1) into
+// nparts partial planes at parts that the selection adds up.
+static cudaError_t route_logits(const moe_config &c, const void *x, const void *Wg,
+                                const float *bias, float *logits, float *parts,
+                                size_t parts_bytes, int *status, cudaStream_t s, int *nparts) {
   cudaError_t err = cudaSuccess;
+  *nparts = 1;
   GemmStage g{};
   g.a_dtype = c.act_dtype;
   g.b_dtype = c.act_dtype;
@@ -189,8 +205,14 @@ cudaError_t launch_route_logits(const moe_config &c, const void *x, const void *
   g.out = logits;
   g.col_bias = bias;
   dim3 grid((c.n + RT_M - 1) / RT_M, (c.n_experts + RT_E - 1) / RT_E);
-  if (c.n >= kTensorCoreRouterMinTokens && gemm_tc_supported(g))
+  if (c.n >= kTensorCoreRouterMinTokens && gemm_tc_supported(g)) {
+    g.ksplit = parts ? gemm_tc_router_ksplit(g, parts_bytes) : 1;
+    if (g.ksplit > 1) {
+      g.out = parts;
+      *nparts = g.ksplit;
+    }
     err = launch_gemm_tc(g, status, s);
+  }
   else if (c.act_dtype == MOE_BF16 && c.n <= kSmallRouterMaxTokens && c.d <= 32 * 8 * RS_MAXV)
     err = launch_pdl(route_logits_small_kernel,
                      dim3((c.n_experts + RS_WARPS - 1) / RS_WARPS, (c.n + RS_TOK - 1) / RS_TOK),
@@ -207,15 +229,22 @@ cudaError_t launch_route_logits(const moe_config &c, const void *x, const void *
   return err;
 }
 
+cudaError_t launch_route_logits(const moe_config &c, const void *x, const void *Wg,
+                                const float *bias, float *logits, int *status, cudaStream_t s) {
+  int nparts = 1;
+  return route_logits(c, x, Wg, bias, logits, nullptr, 0, status, s, &nparts);
+}
+
 cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, const float *bias,
-                         float *logits, int32_t *topk_idx, float *topk_gate, float *probs,
-                         int *status, cudaStream_t s) {
-  cudaError_t err = launch_route_logits(c, x, Wg, bias, logits, status, s);
+                         float *logits, float *parts, size_t parts_bytes, int32_t *topk_idx,
+                         float *topk_gate, float *probs, int *status, cudaStream_t s) {
+  int nparts = 1;
+  cudaError_t err = route_logits(c, x, Wg, bias, logits, parts, parts_bytes, status, s, &nparts);
   if (err != cudaSuccess) return err;
   const int warps_per_block = 8;
   route_select_kernel<<<(c.n + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0,
-                        s>>>(logits, c.n, c.n_experts, c.top_k, c.gate, topk_idx, topk_gate,
-                             probs);
+                        s>>>(logits, parts, nparts > 1 ? nparts : 0, bias, c.n, c.n_experts,
+                             c.top_k, c.gate, topk_idx, topk_gate, probs);
   return cudaGetLastError();
 }
 

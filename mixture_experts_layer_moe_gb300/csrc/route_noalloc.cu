@@ -71,7 +71,8 @@ extern "C" moe_status moe_route_noalloc(const moe_config *cfg, const void *x, co
   float *logits = nullptr;
   const moe_status ss = logits_scratch(&logits);
   if (ss != MOE_OK) return ss;
-  const cudaError_t e = launch_route(*cfg, x, w->Wg, w->router_bias, logits, topk_idx, topk_gate,
-                                     probs, nullptr, static_cast<cudaStream_t>(stream));
+  const cudaError_t e =
+      launch_route(*cfg, x, w->Wg, w->router_bias, logits, nullptr, 0, topk_idx, topk_gate, probs,
+                   nullptr, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
