@@ -389,13 +389,21 @@ cudaError_t launch_scatter_rows(const void *x, const int32_t *inv_perm, int P, i
   return cudaGetLastError();
 }
 
+// many CTAs once there is enough to share out and the scratch holds hist + base
+static bool dispatch_many(int P, int E, const void *scratch, size_t scratch_bytes) {
+  return P >= kDispatchManyMinPairs && scratch != nullptr &&
+         scratch_bytes >= (size_t)num_sms() * E * sizeof(int32_t);
+}
+
+int dispatch_kernels(int P, int E, const void *scratch, size_t scratch_bytes) {
+  return dispatch_many(P, E, scratch, scratch_bytes) ? 2 : 1;
+}
+
 cudaError_t launch_dispatch(int P, int E, const int32_t *topk_idx, int32_t *counts,
                             int32_t *offsets, int32_t *perm, int32_t *inv_perm, int *status,
                             cudaStream_t s, void *scratch, size_t scratch_bytes) {
-  // many CTAs once there is enough to share out and the scratch holds hist + base
   const int G = num_sms();
-  const size_t need = (size_t)G * E * sizeof(int32_t);
-  if (P >= kDispatchManyMinPairs && scratch != nullptr && scratch_bytes >= need) {
+  if (dispatch_many(P, E, scratch, scratch_bytes)) {
     int32_t *hist = static_cast<int32_t *>(scratch);
     const int range = (P + G - 1) / G;
     const size_t smem1 = (size_t)DM_WARPS * E * sizeof(int);

@@ -225,6 +225,13 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
   const int KBLK = args.K / 32;
 
   pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    // the tensor maps are kernel parameters: fetch them while the previous
+    // kernel finishes
+    tc::prefetch_tmap(&tmX);
+    tc::prefetch_tmap(&tmW);
+    if (EPI == 2) tc::prefetch_tmap(&tmW3);
+  }
   pdl_wait();
   if (threadIdx.x == 0) {
     sh.failed_on_entry = status_failed(args.status) ? 1 : 0;
@@ -290,9 +297,6 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
     if (lane == 0) {
       // ---------------- TMA producer: the tile's token boxes + the k-block's
       // codes of weight rows 0..63 and 64..127 (W1 and W3 rows for SwiGLU)
-      tc::prefetch_tmap(&tmX);
-      tc::prefetch_tmap(&tmW);
-      if (EPI == 2) tc::prefetch_tmap(&tmW3);
       int stage = 0;
       uint32_t phase = 0;
       int last_phase[GS];

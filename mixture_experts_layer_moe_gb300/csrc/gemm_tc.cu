@@ -78,7 +78,13 @@ struct Tile {
   int e, row0, seg_end, n_idx;
 };
 
-__device__ __forceinline__ Tile decode_tile(const TcShared &sh, int E, int t) {
+// Tile t of the list: expert-major, then (col_fast false) column block, then
+// row block, so CTAs running together share an expert's weight columns; or
+// (col_fast, the router) row block, then column block, so the CTAs that read
+// one block of rows for different experts run together and the rows come
+// from DRAM once.
+__device__ __forceinline__ Tile decode_tile(const TcShared &sh, int E, int t, int n_tiles = 0,
+                                            bool col_fast = false) {
   int lo = 0, hi = E;   // largest e with tile_start[e] <= t (skips empty experts)
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -89,8 +95,14 @@ __device__ __forceinline__ Tile decode_tile(const TcShared &sh, int E, int t) {
   const int beg = sh.offs[lo], end = sh.offs[lo + 1];
   const int m_tiles = (end - beg + BM - 1) / BM;
   const int local = t - sh.tile_start[lo];
-  tl.n_idx = local / m_tiles;
-  tl.row0 = beg + (local - tl.n_idx * m_tiles) * BM;
+  if (col_fast) {
+    const int m = local / n_tiles;
+    tl.n_idx = local - m * n_tiles;
+    tl.row0 = beg + m * BM;
+  } else {
+    tl.n_idx = local / m_tiles;
+    tl.row0 = beg + (local - tl.n_idx * m_tiles) * BM;
+  }
   tl.seg_end = end;
   return tl;
 }
@@ -144,6 +156,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   auto k_end = [&](int t) { return (int)((int64_t)(t % KS + 1) * KB / KS); };
 
   if (threadIdx.x == 0) {
+    // descriptor fetches overlap the setup below instead of the first copy
+    tc::prefetch_tmap(&tmA);
+    tc::prefetch_tmap(&tmB);
+    if (EPI == 2) tc::prefetch_tmap(&tmB3);
     sh.failed_on_entry = status_failed(args.status) ? 1 : 0;
     sh.abort = sh.failed_on_entry;
   }
@@ -208,16 +224,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
-      tc::prefetch_tmap(&tmA);
-      tc::prefetch_tmap(&tmB);
-      if (EPI == 2) tc::prefetch_tmap(&tmB3);
       int stage = 0;
       uint32_t phase = 0;
       int last_phase[NSTAGE];
 #pragma unroll
       for (int s = 0; s < NSTAGE; ++s) last_phase[s] = -1;
       for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
-        const Tile tl = decode_tile(sh, E, t / KS);
+        const Tile tl = decode_tile(sh, E, t / KS, n_tiles, KPART);
         const int wrow = tl.n_idx * N_OUT;
         const int kb1 = k_end(t);
         for (int kb = k_begin(t); kb < kb1; ++kb) {
@@ -294,7 +307,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       constexpr int NCOL = N_OUT / (EPI_WARPS / 4);
       const int col_off = ((warp - 2) >> 2) * NCOL;
       for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-        const Tile tl = decode_tile(sh, E, t / KS);
+        const Tile tl = decode_tile(sh, E, t / KS, n_tiles, KPART);
         float sum[NCOL];
 #pragma unroll
         for (int i = 0; i < NCOL; ++i) sum[i] = 0.f;

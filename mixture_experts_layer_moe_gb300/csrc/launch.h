@@ -62,6 +62,8 @@ constexpr int kDispatchManyMinPairs = 16384;
 cudaError_t launch_dispatch(int P, int E, const int32_t *topk_idx, int32_t *counts,
                             int32_t *offsets, int32_t *perm, int32_t *inv_perm, int *status,
                             cudaStream_t s, void *scratch = nullptr, size_t scratch_bytes = 0);
+// Kernels launch_dispatch launches for these arguments (1 or 2).
+int dispatch_kernels(int P, int E, const void *scratch, size_t scratch_bytes);
 
 // x_perm[q] = x[perm[q] / k]; rows of row_bytes (multiple of 16).
 // x_perm[inv_perm[t*k + j]] = x[t] in token order: each x row read once

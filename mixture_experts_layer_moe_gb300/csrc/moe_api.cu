@@ -491,7 +491,10 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
   MOE_TRY(cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits),
                                    at<float>(ws, L.h), (size_t)P * c.d_ff * h_size(c), topk_idx,
                                    gates, nullptr, status, s)));
-  stage(MOE_STAGE_DISPATCH, (decode || mx_tc) ? 1 : 2);
+  // (the sort, plus the copy of x rows into segment order on the bf16/fp32 path)
+  stage(MOE_STAGE_DISPATCH,
+        dispatch_kernels(P, c.n_experts, at<void>(ws, L.h), (size_t)P * c.d_ff * h_size(c)) +
+            ((decode || mx_tc) ? 0 : 1));
   MOE_TRY(cuda_status(launch_dispatch(P, c.n_experts, topk_idx, at<int32_t>(ws, L.counts), offsets,
                                       perm, inv_perm, status, s, at<void>(ws, L.h),
                                       (size_t)P * c.d_ff * h_size(c))));
