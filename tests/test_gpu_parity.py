@@ -140,9 +140,22 @@ def test_route_page_example(lib):
         assert torch.allclose(pr.cpu(), torch.tensor([probs]), atol=1e-6)
 
 
-@pytest.mark.parametrize("name", ["mixtral_small", "prefill_zipf_small", "finegrained_small"])
+# Router shapes whose d range is split over several CTAs (fp32 partial planes
+# added by the selection kernel): 32-column variant with 4 ranges; 128-column
+# partials with 2 ranges and the router bias; 200 experts (two column tiles,
+# the second ragged) over 4 ranges, with a 2-row last row tile.
+ROUTER_SPLIT = {
+    "router_split_e8": C["mixtral_bf16"].scaled(n=300, d=2048, d_ff=64, E=8),
+    "router_split_e64_bias": C["gptoss_prefill_zipf_mxfp4"].scaled(n=300, d=1024, d_ff=64, E=64),
+    "router_split_e200": C["finegrained_shared_bf16"].scaled(n=130, d=2048, d_ff=256, E=200,
+                                                             d_ff_shared=0),
+}
+
+
+@pytest.mark.parametrize("name", ["mixtral_small", "prefill_zipf_small", "finegrained_small"]
+                         + list(ROUTER_SPLIT))
 def test_route_probs(lib, name):
-    cfg = SMALL[name]
+    cfg = SMALL.get(name) or ROUTER_SPLIT[name]
     inputs = moe_synth.make_inputs(cfg, seed=5, device="cuda")
     w = lib.make_weights(inputs)
     ws = lib.alloc_workspace(cfg)
@@ -155,6 +168,10 @@ def test_route_probs(lib, name):
     parity.check_routing(cfg, r, idx.cpu(), g.cpu())
     assert (pr.cpu().double() - r["probs"]).abs().max().item() < 1e-5
     assert (pr.sum(1).cpu().double() - 1).abs().max().item() < 1e-5
+    # the logits the selection stored (assembled from the partial planes where split)
+    L = lib.moe_workspace_layout_of(cfg)
+    logits = parity.ws_view(ws, L, "logits", torch.float32, cfg.n * cfg.E).view(cfg.n, cfg.E)
+    assert (logits.cpu().double() - r["logits"]).abs().max().item() < 5e-6
 
 
 # ---------------------------------------------------------------- dispatch
