@@ -20,6 +20,15 @@
 // whole activation segment in L2.  The tile list is derived on the device
 // from the segment offsets; empty segments produce no tiles.
 //
+// The router's linear layer ("Routing: a router scores the experts, and the
+// top one runs") runs as EPI 3 (up to 128 experts per tile, 6-stage ring,
+// four 128-column partials in flight, eight epilogue warps) or EPI 4 (at most
+// 32 experts: MMA N = 32, ten stages, eight partials): each 64-wide k-block
+// is summed into a fresh TMEM partial and the partials are added in fp32
+// registers.  When the row tiles alone leave most SMs idle, a tile's k-blocks
+// are split over up to four CTAs that write fp32 partial planes; the router's
+// selection kernel adds them in plane order.
+//
 // MXFP4 weights run on gemm_mx.cu (dequantised into tensor memory).
 #include "common.cuh"
 #include "launch.h"
@@ -115,12 +124,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // EPI: 0 plain, 1 relu, 2 swiglu (B = W1 rows, B3 = W3 rows, 128 each),
-// 3 fp32 output + per-column bias (router logits).
+// 3 fp32 output + per-column bias (router logits), 4 the same for at most 32
+// columns.
 //
-// EPI 3 keeps the router's logits accurate to fp32 rounding: the tensor core
-// sums each 64-wide k-block into a fresh TMEM partial (N = 128 columns, two
-// partial buffers in flight), and the epilogue warps add the partials in fp32
-// registers with round-to-nearest.  Accumulating the whole reduction in TMEM
+// EPI 3 and 4 keep the router's logits accurate to fp32 rounding: the tensor
+// core sums each 64-wide k-block into a fresh TMEM partial (N = 128 or 32
+// columns, four or eight partials in flight), and the epilogue warps add the
+// partials in fp32 registers with round-to-nearest.  Accumulating the whole reduction in TMEM
 // instead drifted by ~2e-5 on d = 4096 rows, too close to the 1e-5 near-tie
 // margin of the routing decision.
 template <int EPI>
