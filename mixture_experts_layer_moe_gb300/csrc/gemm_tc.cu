@@ -43,13 +43,16 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int MAX_STAGES = 10;
 
 // Ring depth per variant: the router variants stage narrower B tiles, so the
-// same shared memory holds more k-blocks in flight (their A stream is the
-// whole cost of the router, and it is latency-bound at four stages).
+// same shared memory holds more k-blocks of their A stream in flight.
 __host__ __device__ constexpr int stage_bytes(int epi) {
   return A_BYTES + (epi == 4 ? 32 : (epi == 3 ? 128 : BN)) * BK * 2;
 }
-__host__ __device__ constexpr int num_stages(int epi) { return epi == 4 ? MAX_STAGES : (epi == 3 ? 6 : STAGES); }
-__host__ __device__ constexpr int dyn_smem_bytes(int epi) { return num_stages(epi) * stage_bytes(epi) + 1024; }
+__host__ __device__ constexpr int num_stages(int epi) {
+  return epi == 4 ? MAX_STAGES : (epi == 3 ? 6 : STAGES);
+}
+__host__ __device__ constexpr int dyn_smem_bytes(int epi) {
+  return num_stages(epi) * stage_bytes(epi) + 1024;
+}
 // Epilogue warps: the 128-expert router drains a 128-column partial every
 // k-block, so two warps share each TMEM lane quarter (64 columns each).
 __host__ __device__ constexpr int epi_warps(int epi) { return epi == 3 ? 8 : 4; }
@@ -63,7 +66,7 @@ struct TcArgs {
   int rows;
   int K;
   int N;           // output columns
-  void *out;       // bf16 [rows][N], fp32 for EPI 3
+  void *out;       // bf16 [rows][N], fp32 for EPI 3 and 4
   const float *bias;
   int *status;
   int ksplit;      // router: k ranges per row tile (> 1: partial sums, no bias)
@@ -72,7 +75,7 @@ struct TcArgs {
 struct TcShared {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
-  uint64_t tfull[8];    // accumulator ring: 2 (8 for the 32-column router)
+  uint64_t tfull[8];    // accumulator ring: 2, 4 (EPI 3) or 8 (EPI 4)
   uint64_t tempty[8];
   uint64_t drain;
   uint32_t tmem_base;
@@ -130,9 +133,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // EPI 3 and 4 keep the router's logits accurate to fp32 rounding: the tensor
 // core sums each 64-wide k-block into a fresh TMEM partial (N = 128 or 32
 // columns, four or eight partials in flight), and the epilogue warps add the
-// partials in fp32 registers with round-to-nearest.  Accumulating the whole reduction in TMEM
-// instead drifted by ~2e-5 on d = 4096 rows, too close to the 1e-5 near-tie
-// margin of the routing decision.
+// partials in fp32 registers with round-to-nearest.  Accumulating the whole
+// reduction in TMEM instead drifted by ~2e-5 on d = 4096 rows, too close to
+// the 1e-5 near-tie margin of the routing decision.
 template <int EPI>
 __global__ void __launch_bounds__(threads_of(EPI), 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
