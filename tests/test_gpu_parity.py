@@ -34,6 +34,10 @@ SMALL = {
     "mixtral_small": C["mixtral_bf16"].scaled(n=300, d=256, d_ff=512),
     "mixtral_E1": C["mixtral_bf16"].scaled(n=37, d=128, d_ff=256, E=1, k=1),
     "mixtral_k_eq_E": C["mixtral_bf16"].scaled(n=45, d=128, d_ff=192, E=5, k=5),
+    # every token picks every one of the largest expert count (k = E = 256)
+    "all_experts_256": C["mixtral_bf16"].scaled(n=5, d=128, d_ff=64, E=256, k=256),
+    # ReLU experts in bf16: the tensor-core kernel's ReLU epilogue
+    "mixtral_relu_small": C["mixtral_bf16"].scaled(n=300, d=256, d_ff=512, act="relu"),
     "decode_n1": C["gptoss_decode_mxfp4"].scaled(n=1),
     "decode_n4": C["gptoss_decode_mxfp4"].scaled(n=4),
     "decode_many_tokens_per_expert": C["gptoss_decode_mxfp4"].scaled(n=64, d=256, d_ff=320, E=4),
@@ -208,7 +212,7 @@ def test_dispatch_page_example(lib):
 
 
 @pytest.mark.parametrize("n,E,k", [(1, 1, 1), (7, 3, 2), (33, 8, 8), (1000, 256, 8),
-                                   (4096, 8, 2), (8192, 128, 4), (16384, 256, 8)])
+                                   (4096, 8, 2), (8192, 128, 4), (16384, 256, 8), (5, 256, 256)])
 def test_dispatch_random(lib, n, E, k):
     g = torch.Generator().manual_seed(n * 31 + E)
     logits = torch.randn(n, E, generator=g, dtype=torch.float64)
