@@ -341,7 +341,9 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         if (!tc::mbar_wait(&sh.tempty, (local & 1) ^ 1u, abort)) { ok = false; break; }
         tc::tc_fence_after();
         for (int kb = 0; kb < KB; ++kb) {
-          if (!tc::mbar_wait(&sh.full[stage], phase, abort)) { ok = false; break; }
+          // one wait per k-block: every transform thread waited for the
+          // stage's full barrier (its token box and codes land together)
+          // before arriving on aready, so aready's phase implies the tokens
           if (!tc::mbar_wait(&sh.aready[stage], phase, abort)) { ok = false; break; }
           tc::tc_fence_after();
           const uint32_t sb = tc::smem_u32(smem + stage * G_STAGE);
