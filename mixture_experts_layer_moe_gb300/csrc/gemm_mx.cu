@@ -176,17 +176,6 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Named barrier `id` over n threads, OR of pred over them (the same answer for all).
-__device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
 // silu(a) * b; the quotient by the fast reciprocal (h is rounded to bf16)
 __device__ __forceinline__ float silu_mul(float a, float b) {
   return __fdividef(a, 1.f + __expf(-a)) * b;
@@ -490,7 +479,7 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
       asm volatile("cp.async.wait_group 0;" ::: "memory");
       // this tile's scales are in; the transform warps also agree here on
       // stopping (a warp whose wait ran out has raised *abort)
-      if (bar_or(G_BAR_XFORM, XT, *abort != 0)) break;
+      if (tc::bar_or(G_BAR_XFORM, XT, *abort != 0)) break;
       if (t + (int)gridDim.x < num_tiles) fetch_scales(t + gridDim.x, buf ^ 1);
       const uint8_t *srow = scale_buf[buf] + (size_t)crow * KBLK;
       const GTile tl = g_decode(sh, E, t);

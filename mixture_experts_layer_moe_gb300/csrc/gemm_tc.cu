@@ -70,6 +70,15 @@ struct TcArgs {
   const float *bias;
   int *status;
   int ksplit;      // router: k ranges per row tile (> 1: partial sums, no bias)
+  // EPI 4 with sel_idx set: the router's selection runs in the epilogue.  With
+  // ksplit > 1 the CTA that completes a row tile's count (tile_count, zeroed
+  // before the launch) adds the partial planes in out and selects.
+  int *tile_count;
+  float *logits;   // [rows][N] logits (bias included)
+  int32_t *sel_idx;
+  float *sel_gate;
+  float *probs;    // [rows][N] softmax, or nullptr
+  int top_k, gate_mode;
 };
 
 struct TcShared {
@@ -82,6 +91,7 @@ struct TcShared {
   int abort;
   int failed_on_entry;
   int num_tiles;
+  int last;       // fused router selection: this CTA completed the row tile
   int offs[MAX_E + 1];
   int tile_start[MAX_E];
 };
@@ -124,6 +134,56 @@ __device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Selection of one router row by one thread (E <= 32 logits in registers),
+// the same choice and gates as the warp-wide selection of the router's
+// selection kernel ("How Mixture of Experts Scales Model Parameters",
+// sections "Routing: a router scores the experts, and the top one runs" and
+// "Top-K: several experts, added up by weight"): larger logit first, lower
+// index on equal values, NaN ranks below everything; softmax with the
+// maximum subtracted; top_prob gates divide by the full sum, renorm gates by
+// the sum over the chosen k (added in rank order).
+__device__ __forceinline__ void select_row(const float (&l)[32], int E, int k, int gate_mode,
+                                           int32_t *idx, float *gate, float *probs) {
+  float t[32];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    t[e] = (e < E && !isnan(l[e])) ? l[e] : -INFINITY;
+    mx = fmaxf(mx, t[e]);
+  }
+  float sum = 0.f;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    if (e < E) {
+      const float ex = expf(t[e] - mx);
+      sum += ex;
+      if (probs) probs[e] = ex;
+    }
+  }
+  if (probs)
+    for (int e = 0; e < E; ++e) probs[e] = probs[e] / sum;
+  uint32_t taken = 0;
+  float sel_sum = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      if (e < E && !((taken >> e) & 1u) && (t[e] > bv || (t[e] == bv && e < bi))) {
+        bv = t[e];
+        bi = e;
+      }
+    }
+    taken |= 1u << bi;
+    const float exj = expf(bv - mx);
+    sel_sum += exj;
+    idx[j] = bi;
+    gate[j] = exj;
+  }
+  const float denom = (gate_mode == MOE_GATE_RENORM) ? sel_sum : sum;
+  for (int j = 0; j < k; ++j) gate[j] = gate[j] / denom;
 }
 
 // EPI: 0 plain, 1 relu, 2 swiglu (B = W1 rows, B3 = W3 rows, 128 each),
@@ -343,9 +403,64 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           tc::tc_fence_before();
           tc::mbar_arrive(&sh.tempty[acc]);
         }
-        if (!ok) break;
         const int row = tl.row0 + r_local;
-        if (row < tl.seg_end) {
+        const bool row_ok = row < tl.seg_end;
+        if (EPI == 4 && args.sel_idx != nullptr) {
+          // selection fused here.  The four epilogue warps first agree on
+          // going on (a warp whose wait ran out has raised *abort), since
+          // they meet on named barrier 1 below.
+          if (tc::bar_or(1, 32 * EPI_WARPS, !ok || *abort != 0)) break;
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = sum[i];
+          bool last = true;
+          if (KS > 1) {
+            float *planes = static_cast<float *>(args.out);
+            if (row_ok) {
+              float *prow = planes + ((size_t)(t % KS) * args.rows + row) * args.N;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < args.N) prow[i] = sum[i];
+            }
+            // the planes this CTA wrote are visible before it counts itself
+            __threadfence();
+            tc::bar_or(1, 32 * EPI_WARPS, false);
+            if (warp == 2 && lane == 0)
+              sh.last = atomicAdd(&args.tile_count[t / KS], 1) == KS - 1 ? 1 : 0;
+            tc::bar_or(1, 32 * EPI_WARPS, false);
+            last = sh.last != 0;
+            if (last && row_ok) {
+              __threadfence();
+              // the planes in order, as the selection kernel adds them
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = 0.f;
+              for (int pp = 0; pp < KS; ++pp) {
+                const float *prow = planes + ((size_t)pp * args.rows + row) * args.N;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (i < args.N) v[i] += __ldcg(prow + i);
+              }
+            }
+          }
+          if (last && row_ok) {
+            float *lrow = args.logits + (size_t)row * args.N;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (i < args.N) {
+                v[i] = v[i] + (args.bias ? args.bias[i] : 0.f);
+                lrow[i] = v[i];
+              }
+            }
+            select_row(v, args.N, args.top_k, args.gate_mode,
+                       args.sel_idx + (size_t)row * args.top_k,
+                       args.sel_gate + (size_t)row * args.top_k,
+                       args.probs ? args.probs + (size_t)row * args.N : nullptr);
+          }
+          __syncwarp();
+          continue;
+        }
+        if (!ok) break;
+        if (row_ok) {
           // k range p of a split writes its partial sums to plane p; the
           // reader adds the planes in order, then the bias
           const int p = t % KS;
@@ -465,6 +580,15 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
   a.bias = g.col_bias;
   a.status = status;
   a.ksplit = (EPI == 3 || EPI == 4) && g.ksplit > 1 ? g.ksplit : 1;
+  if (EPI == 4 && gemm_tc_router_fuses(g)) {
+    a.sel_idx = g.sel_idx;
+    a.sel_gate = g.sel_gate;
+    a.probs = g.sel_probs;
+    a.logits = g.logits;
+    a.tile_count = g.tile_count;
+    a.top_k = g.top_k;
+    a.gate_mode = g.gate_mode;
+  }
   gemm_tc_kernel<EPI><<<num_sms(), threads_of(EPI), smem, s>>>(mA, mB, mB3, a);
   return cudaGetLastError();
 }
@@ -479,6 +603,12 @@ bool gemm_tc_supported(const GemmStage &g) {
   const bool n_ok = g.epi == 3 ? true : g.N % 8 == 0;
   // (epi 3 with N <= 32 runs as the 32-column router variant)
   return g.a_dtype == MOE_BF16 && g.b_dtype == MOE_BF16 && out_ok && n_ok && g.K % 8 == 0;
+}
+
+bool gemm_tc_router_fuses(const GemmStage &g) {
+  return g.epi == 3 && g.N <= 32 && g.sel_idx != nullptr && g.sel_gate != nullptr &&
+         g.logits != nullptr && g.top_k >= 1 && g.top_k <= g.N &&
+         (g.ksplit <= 1 || g.tile_count != nullptr) && gemm_tc_supported(g);
 }
 
 int gemm_tc_router_ksplit(const GemmStage &g, size_t plane_room) {

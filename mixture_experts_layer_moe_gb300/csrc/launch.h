@@ -41,9 +41,15 @@ int num_sms();
 // Router: logits (fp32 [n][E] scratch) -> softmax -> top-k -> gates.
 // parts (nullable, parts_bytes long) is scratch for partial logits when the
 // tensor-core router splits its reduction over more SMs.
+// tile_count (nullable): ceil(n / 128) zeroed ints, which let a router with
+// at most 32 experts and a split reduction run its selection in the GEMM.
 cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, const float *bias,
                          float *logits, float *parts, size_t parts_bytes, int32_t *topk_idx,
-                         float *topk_gate, float *probs, int *status, cudaStream_t s);
+                         float *topk_gate, float *probs, int *status, cudaStream_t s,
+                         int *tile_count = nullptr);
+// Kernels launch_route launches for these shapes (1 when the selection runs
+// in the router's GEMM, else 2).
+int route_kernels(const moe_config &c, size_t parts_bytes, bool have_counters);
 // The router's linear layer alone: logits [n][E] fp32.
 cudaError_t launch_route_logits(const moe_config &c, const void *x, const void *Wg,
                                 const float *bias, float *logits, int *status, cudaStream_t s);
@@ -105,6 +111,15 @@ struct GemmStage {
   void *out16;          // MXFP4 path: f16 copy of out (next projection's input) or nullptr
   int ksplit;           // epi 3 on tensor cores: k ranges per row tile; > 1 writes
                         // partial sums to planes out[p][rows][N] without the bias
+  // epi 3 with N <= 32 on tensor cores: top-k selection fused into the GEMM
+  // when sel_idx is set (logits [rows][N] written, probs optional); with
+  // ksplit > 1 it needs tile_count, one zeroed int per 128-row tile
+  int32_t *sel_idx;
+  float *sel_gate;
+  float *sel_probs;
+  float *logits;
+  int *tile_count;
+  int top_k, gate_mode;
 };
 cudaError_t launch_gemm_simt(const GemmStage &g, int *status, cudaStream_t s);
 
@@ -115,6 +130,8 @@ cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s);
 // Split of the router's reduction that fills the SMs (1: no split), given
 // room in bytes for the fp32 partial planes.
 int gemm_tc_router_ksplit(const GemmStage &g, size_t plane_room);
+// Whether launch_gemm_tc runs this router stage with the selection fused.
+bool gemm_tc_router_fuses(const GemmStage &g);
 // MXFP4 grouped GEMM with the dequantised weights as the tcgen05 A operand in
 // tensor memory (f16 activation copies in, bf16 out; epi 0, 1 or 2).
 bool gemm_mx_supported(const GemmStage &g);

@@ -81,8 +81,8 @@ moe_status check_expert_weights(const moe_config &c, const moe_weights *w) {
 }
 
 struct Layout {
-  size_t status, logits, topk_idx, topk_gate, counts, offsets, perm, inv_perm, x_perm, h, y_perm,
-      y_shared, h_shared, act16, total;
+  size_t status, route_count, logits, topk_idx, topk_gate, counts, offsets, perm, inv_perm,
+      x_perm, h, y_perm, y_shared, h_shared, act16, total;
 };
 
 Layout layout_of(const moe_config &c) {
@@ -95,6 +95,9 @@ Layout layout_of(const moe_config &c) {
     return at;
   };
   L.status = take(kAlign);
+  // right after the status word, so that one memset clears both: per 128-row
+  // router tile, the CTAs of a split reduction that have finished it
+  L.route_count = take(((size_t)c.n + 127) / 128 * 4);
   L.logits = take(n * E * 4);
   L.topk_idx = take(P * 4);
   L.topk_gate = take(P * 4);
@@ -475,7 +478,9 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
     if (hook) hook(id, launched, user);
     launched += kernels;
   };
-  MOE_TRY(cuda_status(cudaMemsetAsync(status, 0, 2 * sizeof(int), s)));
+  // the status word and the router's tile counts
+  MOE_TRY(cuda_status(cudaMemsetAsync(
+      status, 0, L.route_count - L.status + ((size_t)c.n + 127) / 128 * 4, s)));
   int32_t *topk_idx = at<int32_t>(ws, L.topk_idx);
   float *gates = at<float>(ws, L.topk_gate);
   int32_t *offsets = at<int32_t>(ws, L.offsets);
@@ -485,12 +490,12 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
   const bool mx_tc = mx_tc_path(c);
   if (decode && decode_route_supported(c))
     return run_small_batch(c, x, w, nullptr, y, nullptr, nullptr, nullptr, ws, s, stage);
-  stage(MOE_STAGE_ROUTE, 2);
   // (the h buffer is free until the FFN: scratch for the router's partial
   // logits, then for a many-CTA sort)
+  stage(MOE_STAGE_ROUTE, route_kernels(c, (size_t)P * c.d_ff * h_size(c), true));
   MOE_TRY(cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits),
                                    at<float>(ws, L.h), (size_t)P * c.d_ff * h_size(c), topk_idx,
-                                   gates, nullptr, status, s)));
+                                   gates, nullptr, status, s, at<int>(ws, L.route_count))));
   // (the sort, plus the copy of x rows into segment order on the bf16/fp32 path)
   stage(MOE_STAGE_DISPATCH,
         dispatch_kernels(P, c.n_experts, at<void>(ws, L.h), (size_t)P * c.d_ff * h_size(c)) +

@@ -183,13 +183,20 @@ route_select_kernel(float *__restrict__ logits, const float *__restrict__ parts,
 
 }  // namespace
 
-// The router's linear layer into logits, or (return value nparts > 1) into
-// nparts partial planes at parts that the selection adds up.
-static cudaError_t route_logits(const moe_config &c, const void *x, const void *Wg,
-                                const float *bias, float *logits, float *parts,
-                                size_t parts_bytes, int *status, cudaStream_t s, int *nparts) {
-  cudaError_t err = cudaSuccess;
-  *nparts = 1;
+// Selection outputs for a router whose selection may be fused into its GEMM.
+struct RouteSel {
+  int32_t *idx;
+  float *gate;
+  float *probs;
+  int *tile_count;   // zeroed [ceil(n / 128)] ints, or nullptr
+};
+
+// The tensor-core router stage for these shapes (rows >= 128, bf16), with the
+// reduction split when parts has room, and the selection fused when sel is
+// given and the GEMM can take it (at most 32 experts).
+static GemmStage router_stage(const moe_config &c, const void *x, const void *Wg,
+                              const float *bias, float *logits, float *parts, size_t parts_bytes,
+                              const RouteSel *sel) {
   GemmStage g{};
   g.a_dtype = c.act_dtype;
   g.b_dtype = c.act_dtype;
@@ -204,13 +211,40 @@ static cudaError_t route_logits(const moe_config &c, const void *x, const void *
   g.B = Wg;
   g.out = logits;
   g.col_bias = bias;
+  if (c.n < kTensorCoreRouterMinTokens || !gemm_tc_supported(g)) {
+    g.rows = 0;   // not on the tensor cores
+    return g;
+  }
+  g.ksplit = parts ? gemm_tc_router_ksplit(g, parts_bytes) : 1;
+  if (g.ksplit > 1) g.out = parts;
+  if (sel) {
+    g.sel_idx = sel->idx;
+    g.sel_gate = sel->gate;
+    g.sel_probs = sel->probs;
+    g.logits = logits;
+    g.tile_count = sel->tile_count;
+    g.top_k = c.top_k;
+    g.gate_mode = c.gate;
+    if (!gemm_tc_router_fuses(g)) g.sel_idx = nullptr;
+  }
+  return g;
+}
+
+// The router's linear layer into logits, or (*nparts > 1) into nparts partial
+// planes at parts that the selection adds up, or (*fused) with the selection
+// done as well.
+static cudaError_t route_logits(const moe_config &c, const void *x, const void *Wg,
+                                const float *bias, float *logits, float *parts,
+                                size_t parts_bytes, const RouteSel *sel, int *status,
+                                cudaStream_t s, int *nparts, bool *fused) {
+  cudaError_t err = cudaSuccess;
+  *nparts = 1;
+  *fused = false;
+  const GemmStage g = router_stage(c, x, Wg, bias, logits, parts, parts_bytes, sel);
   dim3 grid((c.n + RT_M - 1) / RT_M, (c.n_experts + RT_E - 1) / RT_E);
-  if (c.n >= kTensorCoreRouterMinTokens && gemm_tc_supported(g)) {
-    g.ksplit = parts ? gemm_tc_router_ksplit(g, parts_bytes) : 1;
-    if (g.ksplit > 1) {
-      g.out = parts;
-      *nparts = g.ksplit;
-    }
+  if (g.rows > 0) {
+    if (g.ksplit > 1) *nparts = g.ksplit;
+    *fused = g.sel_idx != nullptr;
     err = launch_gemm_tc(g, status, s);
   }
   else if (c.act_dtype == MOE_BF16 && c.n <= kSmallRouterMaxTokens && c.d <= 32 * 8 * RS_MAXV)
@@ -229,18 +263,34 @@ static cudaError_t route_logits(const moe_config &c, const void *x, const void *
   return err;
 }
 
+int route_kernels(const moe_config &c, size_t parts_bytes, bool have_counters) {
+  // (the pointers only need to be non-null to decide)
+  float dummy;
+  int32_t didx;
+  int dcount;
+  const RouteSel sel{&didx, &dummy, nullptr, have_counters ? &dcount : nullptr};
+  const GemmStage g = router_stage(c, &dummy, &dummy, nullptr, &dummy,
+                                   parts_bytes ? &dummy : nullptr, parts_bytes, &sel);
+  return (g.rows > 0 && g.sel_idx != nullptr) ? 1 : 2;
+}
+
 cudaError_t launch_route_logits(const moe_config &c, const void *x, const void *Wg,
                                 const float *bias, float *logits, int *status, cudaStream_t s) {
   int nparts = 1;
-  return route_logits(c, x, Wg, bias, logits, nullptr, 0, status, s, &nparts);
+  bool fused = false;
+  return route_logits(c, x, Wg, bias, logits, nullptr, 0, nullptr, status, s, &nparts, &fused);
 }
 
 cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, const float *bias,
                          float *logits, float *parts, size_t parts_bytes, int32_t *topk_idx,
-                         float *topk_gate, float *probs, int *status, cudaStream_t s) {
+                         float *topk_gate, float *probs, int *status, cudaStream_t s,
+                         int *tile_count) {
   int nparts = 1;
-  cudaError_t err = route_logits(c, x, Wg, bias, logits, parts, parts_bytes, status, s, &nparts);
-  if (err != cudaSuccess) return err;
+  bool fused = false;
+  const RouteSel sel{topk_idx, topk_gate, probs, tile_count};
+  cudaError_t err = route_logits(c, x, Wg, bias, logits, parts, parts_bytes, &sel, status, s,
+                                 &nparts, &fused);
+  if (err != cudaSuccess || fused) return err;
   const int warps_per_block = 8;
   route_select_kernel<<<(c.n + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0,
                         s>>>(logits, parts, nparts > 1 ? nparts : 0, bias, c.n, c.n_experts,

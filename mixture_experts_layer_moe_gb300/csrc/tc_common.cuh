@@ -101,6 +101,19 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap *m, uint64_t *bar,
       : "memory");
 }
 
+// Named barrier `id` over n threads, OR of pred over them (the same answer
+// for all).
+__device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
 // ---- tcgen05 -------------------------------------------------------------
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {

@@ -36,6 +36,9 @@ SMALL = {
     "mixtral_k_eq_E": C["mixtral_bf16"].scaled(n=45, d=128, d_ff=192, E=5, k=5),
     # every token picks every one of the largest expert count (k = E = 256)
     "all_experts_256": C["mixtral_bf16"].scaled(n=5, d=128, d_ff=64, E=256, k=256),
+    # router with 4 split d ranges and its selection fused into the GEMM (the
+    # last CTA of each row tile adds the partial planes), a 44-row last tile
+    "mixtral_router_split_fused": C["mixtral_bf16"].scaled(n=300, d=2048, d_ff=128),
     # ReLU experts in bf16: the tensor-core kernel's ReLU epilogue
     "mixtral_relu_small": C["mixtral_bf16"].scaled(n=300, d=256, d_ff=512, act="relu"),
     "decode_n1": C["gptoss_decode_mxfp4"].scaled(n=1),
