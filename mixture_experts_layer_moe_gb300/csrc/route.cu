@@ -157,10 +157,11 @@ route_logits_small_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat
   if (lane < nt) logits[(size_t)(t0 + lane) * E + e] = mine + (bias ? bias[e] : 0.f);
 }
 
-// One warp per token (selection and gates as in select_topk_warp).  With
-// nparts > 0 the logits are first assembled from the router's partial planes
-// parts[p][n][E], added in plane order, then the bias; they are stored to
-// logits before the selection reads them.
+// One warp per token (selection and gates as in select_topk_lanes; NV =
+// ceil(E / 32) logits per lane).  With nparts > 0 the logits are first
+// assembled from the router's partial planes parts[p][n][E], added in plane
+// order, then the bias; they are stored to logits and selected from registers.
+template <int NV>
 __global__ void __launch_bounds__(256)
 route_select_kernel(float *__restrict__ logits, const float *__restrict__ parts, int nparts,
                     const float *__restrict__ bias, int n, int E, int k, int gate_mode,
@@ -169,16 +170,24 @@ route_select_kernel(float *__restrict__ logits, const float *__restrict__ parts,
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= n) return;
-  if (nparts > 0) {
-    for (int e = lane; e < E; e += 32) {
-      float v = parts[(size_t)warp * E + e];
-      for (int p = 1; p < nparts; ++p) v += parts[((size_t)p * n + warp) * E + e];
-      logits[(size_t)warp * E + e] = v + (bias ? bias[e] : 0.f);
+  float v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = 0.f;
+    if (e < E) {
+      if (nparts > 0) {
+        float a = parts[(size_t)warp * E + e];
+        for (int p = 1; p < nparts; ++p) a += parts[((size_t)p * n + warp) * E + e];
+        v[i] = a + (bias ? bias[e] : 0.f);
+        logits[(size_t)warp * E + e] = v[i];
+      } else {
+        v[i] = logits[(size_t)warp * E + e];
+      }
     }
-    __syncwarp();
   }
-  select_topk_warp(logits + (size_t)warp * E, E, k, gate_mode, lane, topk_idx + (size_t)warp * k,
-                   topk_gate + (size_t)warp * k, probs ? probs + (size_t)warp * E : nullptr);
+  select_topk_lanes<NV>(v, E, k, gate_mode, lane, topk_idx + (size_t)warp * k,
+                        topk_gate + (size_t)warp * k, probs ? probs + (size_t)warp * E : nullptr);
 }
 
 }  // namespace
@@ -292,9 +301,21 @@ cudaError_t launch_route(const moe_config &c, const void *x, const void *Wg, con
                                  &nparts, &fused);
   if (err != cudaSuccess || fused) return err;
   const int warps_per_block = 8;
-  route_select_kernel<<<(c.n + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0,
-                        s>>>(logits, parts, nparts > 1 ? nparts : 0, bias, c.n, c.n_experts,
-                             c.top_k, c.gate, topk_idx, topk_gate, probs);
+  const dim3 grid((c.n + warps_per_block - 1) / warps_per_block), block(32 * warps_per_block);
+  const int np = nparts > 1 ? nparts : 0;
+  const int E = c.n_experts;
+  if (E <= 32)
+    route_select_kernel<1><<<grid, block, 0, s>>>(logits, parts, np, bias, c.n, E, c.top_k,
+                                                  c.gate, topk_idx, topk_gate, probs);
+  else if (E <= 64)
+    route_select_kernel<2><<<grid, block, 0, s>>>(logits, parts, np, bias, c.n, E, c.top_k,
+                                                  c.gate, topk_idx, topk_gate, probs);
+  else if (E <= 128)
+    route_select_kernel<4><<<grid, block, 0, s>>>(logits, parts, np, bias, c.n, E, c.top_k,
+                                                  c.gate, topk_idx, topk_gate, probs);
+  else
+    route_select_kernel<8><<<grid, block, 0, s>>>(logits, parts, np, bias, c.n, E, c.top_k,
+                                                  c.gate, topk_idx, topk_gate, probs);
   return cudaGetLastError();
 }
 

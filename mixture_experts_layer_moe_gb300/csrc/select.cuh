@@ -9,6 +9,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "moe.h"
 
 namespace moe {
@@ -20,15 +22,20 @@ namespace moe {
 //   renorm:   g_j = exp(l_j - m) / sum_{chosen} exp(l_c - m)
 // idx[j] and gate[j] (j < k) are written in rank order; probs (nullable) gets
 // the E softmax probabilities.
-__device__ __forceinline__ void select_topk_warp(const float *__restrict__ l, int E, int k,
-                                                 int gate_mode, int lane, int32_t *idx,
-                                                 float *gate, float *probs) {
-  float v[8];
+//
+// NV = ceil(E / 32) register slots per lane; l[i] is expert lane + 32 i (any
+// value where that is >= E).  The full softmax sum is formed only when the
+// gates or probs need it (renorm gates divide by the chosen k's sum alone).
+template <int NV>
+__device__ __forceinline__ void select_topk_lanes(const float (&l)[NV], int E, int k,
+                                                  int gate_mode, int lane, int32_t *idx,
+                                                  float *gate, float *probs) {
+  float v[NV];
   float mx = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
-    float t = (e < E) ? l[e] : -INFINITY;
+    float t = (e < E) ? l[i] : -INFINITY;
     if (isnan(t)) t = -INFINITY;
     v[i] = t;
     mx = fmaxf(mx, t);
@@ -36,29 +43,31 @@ __device__ __forceinline__ void select_topk_warp(const float *__restrict__ l, in
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   float sum = 0.f;
-  float ex[8];
+  if (gate_mode != MOE_GATE_RENORM || probs != nullptr) {
+    float ex[NV];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    ex[i] = (lane + 32 * i < E) ? expf(v[i] - mx) : 0.f;
-    sum += ex[i];
-  }
+    for (int i = 0; i < NV; ++i) {
+      ex[i] = (lane + 32 * i < E) ? expf(v[i] - mx) : 0.f;
+      sum += ex[i];
+    }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (probs) {
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (probs) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) probs[e] = ex[i] / sum;
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) probs[e] = ex[i] / sum;
+      }
     }
   }
   unsigned taken = 0;
-  float sel_ex[8];   // slot j kept by lane j % 32 at [j / 32]
+  float sel_ex[NV];   // slot j kept by lane j % 32 at [j / 32] (k <= E)
   float sel_sum = 0.f;
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
       if (e < E && !((taken >> i) & 1u)) {
         if (v[i] > bv || (v[i] == bv && e < bi)) { bv = v[i]; bi = e; }
@@ -73,15 +82,37 @@ __device__ __forceinline__ void select_topk_warp(const float *__restrict__ l, in
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
     const float exj = expf(bv - mx);
     sel_sum += exj;
-    if ((j & 31) == lane) sel_ex[j >> 5] = exj;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (j == lane + 32 * i) sel_ex[i] = exj;
     if (lane == 0) idx[j] = bi;
   }
   const float denom = (gate_mode == MOE_GATE_RENORM) ? sel_sum : sum;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int j = lane + 32 * i;
     if (j < k) gate[j] = sel_ex[i] / denom;
   }
+}
+
+// The same reading the E logits from memory (l[e]).
+__device__ __forceinline__ void select_topk_warp(const float *__restrict__ l, int E, int k,
+                                                 int gate_mode, int lane, int32_t *idx,
+                                                 float *gate, float *probs) {
+  auto run = [&](auto nv) {
+    constexpr int NV = decltype(nv)::value;
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? l[e] : -INFINITY;
+    }
+    select_topk_lanes<NV>(v, E, k, gate_mode, lane, idx, gate, probs);
+  };
+  if (E <= 32) run(std::integral_constant<int, 1>{});
+  else if (E <= 64) run(std::integral_constant<int, 2>{});
+  else if (E <= 128) run(std::integral_constant<int, 4>{});
+  else run(std::integral_constant<int, 8>{});
 }
 
 }  // namespace moe
