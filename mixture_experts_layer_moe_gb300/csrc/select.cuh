@@ -9,8 +9,6 @@
 #include <math.h>
 #include <stdint.h>
 
-#include <type_traits>
-
 #include "moe.h"
 
 namespace moe {
@@ -26,7 +24,10 @@ namespace moe {
 // NV = ceil(E / 32) register slots per lane; l[i] is expert lane + 32 i (any
 // value where that is >= E).  The full softmax sum is formed only when the
 // gates or probs need it (renorm gates divide by the chosen k's sum alone).
-template <int NV>
+// COMPACT keeps the chosen exponentials in an indexed array (local memory)
+// rather than unrolled registers: fewer registers for kernels that must stay
+// small, the same values.
+template <int NV, bool COMPACT = false>
 __device__ __forceinline__ void select_topk_lanes(const float (&l)[NV], int E, int k,
                                                   int gate_mode, int lane, int32_t *idx,
                                                   float *gate, float *probs) {
@@ -82,9 +83,13 @@ __device__ __forceinline__ void select_topk_lanes(const float (&l)[NV], int E, i
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
     const float exj = expf(bv - mx);
     sel_sum += exj;
+    if (COMPACT) {
+      if ((j & 31) == lane) sel_ex[j >> 5] = exj;
+    } else {
 #pragma unroll
-    for (int i = 0; i < NV; ++i)
-      if (j == lane + 32 * i) sel_ex[i] = exj;
+      for (int i = 0; i < NV; ++i)
+        if (j == lane + 32 * i) sel_ex[i] = exj;
+    }
     if (lane == 0) idx[j] = bi;
   }
   const float denom = (gate_mode == MOE_GATE_RENORM) ? sel_sum : sum;
@@ -95,24 +100,19 @@ __device__ __forceinline__ void select_topk_lanes(const float (&l)[NV], int E, i
   }
 }
 
-// The same reading the E logits from memory (l[e]).
+// The same reading the E logits from memory (l[e]), in the compact form for
+// any E <= 256 (the small-batch routing cluster, whose register count decides
+// how soon the next kernel's CTAs fit beside it).
 __device__ __forceinline__ void select_topk_warp(const float *__restrict__ l, int E, int k,
                                                  int gate_mode, int lane, int32_t *idx,
                                                  float *gate, float *probs) {
-  auto run = [&](auto nv) {
-    constexpr int NV = decltype(nv)::value;
-    float v[NV];
+  float v[8];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < E) ? l[e] : -INFINITY;
-    }
-    select_topk_lanes<NV>(v, E, k, gate_mode, lane, idx, gate, probs);
-  };
-  if (E <= 32) run(std::integral_constant<int, 1>{});
-  else if (E <= 64) run(std::integral_constant<int, 2>{});
-  else if (E <= 128) run(std::integral_constant<int, 4>{});
-  else run(std::integral_constant<int, 8>{});
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? l[e] : -INFINITY;
+  }
+  select_topk_lanes<8, true>(v, E, k, gate_mode, lane, idx, gate, probs);
 }
 
 }  // namespace moe
