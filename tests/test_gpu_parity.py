@@ -39,6 +39,9 @@ SMALL = {
     # router with 4 split d ranges and its selection fused into the GEMM (the
     # last CTA of each row tile adds the partial planes), a 44-row last tile
     "mixtral_router_split_fused": C["mixtral_bf16"].scaled(n=300, d=2048, d_ff=128),
+    # a mid-size layer with every output row checked: the up projection has
+    # fewer tiles (144) than SMs, the down projection 4.7 rounds of 720
+    "mixtral_mid_all_rows": C["mixtral_bf16"].scaled(n=4096, d=2560, d_ff=256),
     # ReLU experts in bf16: the tensor-core kernel's ReLU epilogue
     "mixtral_relu_small": C["mixtral_bf16"].scaled(n=300, d=256, d_ff=512, act="relu"),
     "decode_n1": C["gptoss_decode_mxfp4"].scaled(n=1),
