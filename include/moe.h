@@ -60,8 +60,11 @@ typedef enum {
   MOE_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, attribute, ...) */
   MOE_ERR_BAD_INDEX = 5,    /* device: expert index >= E or < 0, or perm entry out of range */
   MOE_ERR_TIMEOUT = 6,      /* device: a bounded pipeline wait ran out */
-  MOE_ERR_RANGE = 7         /* device: an MXFP4 block scale outside the range the
+  MOE_ERR_RANGE = 7,        /* device: an MXFP4 block scale outside the range the
                                tensor-core path applies exactly (E8M0 byte 113..142) */
+  MOE_ERR_F16_RANGE = 8     /* device: an activation (x or h) of an MXFP4 layer outside
+                               the f16 range its tensor-core operands use (|v| > 65504,
+                               or NaN); the value was clamped and y is not valid */
 } moe_status;
 
 /* NVFP4: the feed post "What is MXFP4?" names it as the block-of-16 variant
@@ -180,15 +183,27 @@ moe_status moe_route_stats(const moe_config *cfg, const float *probs, const int3
  * not capture-safe, plugins handed only their input and output buffers by a
  * host runtime that owns all device memory, fixed-arena embedded runtimes.
  * (An addition of this library; the pages have no counterpart.)
- * Same arguments and results as moe_route, minus ws/ws_bytes.  The logits
- * live in one file-scope device array of 16 MiB that every GPU loading the
- * library holds until exit; n * n_experts above 4,194,304 returns
- * MOE_ERR_WORKSPACE.  The first call on a device (with it current) looks up
- * the array's address; make that call before any stream capture.  All calls
- * share the array: calls that overlap on the GPU race and must be serialised
- * by the caller.  No allocation, no synchronisation. */
+ * Arguments as moe_route, minus ws/ws_bytes; the same selection rules.  The
+ * router's reduction is never split over extra CTAs here (that needs scratch
+ * for the partial sums), so on shapes where moe_route splits it the fp32
+ * logits, probs and gates may differ from moe_route's in the last bits, and a
+ * token whose top-k margin is at rounding level may rank differently.
+ * The logits live in one file-scope device array of 16 MiB, and device-side
+ * faults (a pipeline wait that ran out) in a file-scope status word; every GPU
+ * loading the library holds both until exit.  n * n_experts above 4,194,304
+ * returns MOE_ERR_WORKSPACE.  The first call on a device (with it current) in
+ * a CUDA context looks up the arrays' addresses; make that call before any
+ * stream capture.  Each call clears the status word on its stream first.  All
+ * calls share the arrays: calls that overlap on the GPU race and must be
+ * serialised by the caller.  No allocation, no synchronisation. */
 moe_status moe_route_noalloc(const moe_config *cfg, const void *x, const moe_weights *w,
                              int32_t *topk_idx, float *topk_gate, float *probs, void *stream);
+
+/* Synchronises `stream`, then returns the device status word of the last
+ * moe_route_noalloc on the current device (MOE_OK, or MOE_ERR_TIMEOUT when a
+ * wait of its router ran out and its outputs are not valid).  detail, if not
+ * NULL, receives the detail word.  Allocates nothing. */
+moe_status moe_route_noalloc_status(void *stream, int32_t *detail);
 
 /* Dispatch ("The forward pass: dispatch, then combine"): a stable counting
  * sort of the n*K (token, slot) pairs by expert.  Bit-exact.
@@ -328,10 +343,11 @@ const char *moe_status_string(moe_status s);
 /* Diagnostics for the device-side failure path.  Launches one warp that waits,
  * with the same bounded wait the pipeline kernels use, on a barrier nothing
  * arrives on; after limit_ns (1 .. 1e9) the wait gives up and the kernel sets
- * MOE_ERR_TIMEOUT in the workspace status word (ws: a layer workspace, 256-byte
- * aligned) and exits, leaving the context usable.  Asynchronous on stream;
- * read the result with moe_status_check.  MOE_ERR_INVALID_ARG for a bad ws or
- * limit. */
+ * MOE_ERR_TIMEOUT in the status word and exits, leaving the context usable.
+ * ws: a layer workspace (256-byte aligned; read the result with
+ * moe_status_check), or NULL for the status word of moe_route_noalloc on the
+ * current device (read it with moe_route_noalloc_status).  Asynchronous on
+ * stream.  MOE_ERR_INVALID_ARG for a misaligned ws or a bad limit. */
 moe_status moe_selftest_wait_timeout(void *ws, uint64_t limit_ns, void *stream);
 
 #ifdef __cplusplus

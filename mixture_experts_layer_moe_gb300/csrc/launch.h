@@ -54,6 +54,9 @@ int route_kernels(const moe_config &c, size_t parts_bytes, bool have_counters);
 cudaError_t launch_route_logits(const moe_config &c, const void *x, const void *Wg,
                                 const float *bias, float *logits, int *status, cudaStream_t s);
 
+// Device address of moe_route_noalloc's status word on the current device.
+moe_status noalloc_status_word(int **out);
+
 // Routing statistics: P [E], f [E] and aux (one float) from probs [n][E] and
 // the top-1 column of topk_idx.
 cudaError_t launch_route_stats(const moe_config &c, const float *probs, const int32_t *topk_idx,
@@ -132,6 +135,10 @@ cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s);
 int gemm_tc_router_ksplit(const GemmStage &g, size_t plane_room);
 // Whether launch_gemm_tc runs this router stage with the selection fused.
 bool gemm_tc_router_fuses(const GemmStage &g);
+// The bf16 grouped GEMM (epi 0, 1, 2) on SM pairs: tcgen05.mma.cta_group::2
+// with 256 weight rows on M and up to 256 tokens on N (gemm_t2.cu).
+bool gemm_t2_supported(const GemmStage &g);
+cudaError_t launch_gemm_t2(const GemmStage &g, int *status, cudaStream_t s);
 // MXFP4 grouped GEMM with the dequantised weights as the tcgen05 A operand in
 // tensor memory (f16 activation copies in, bf16 out; epi 0, 1 or 2).
 bool gemm_mx_supported(const GemmStage &g);

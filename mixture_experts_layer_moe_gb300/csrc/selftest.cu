@@ -1,7 +1,8 @@
 // Diagnostics: the bounded device wait every pipeline kernel uses, run
 // against an mbarrier that nothing arrives on, so that a test can check that
 // such a wait ends by itself and reports MOE_ERR_TIMEOUT through the status
-// word, with the context still usable afterwards.
+// word, with the context still usable afterwards.  The word is a workspace's,
+// or (ws == NULL) the one moe_route_noalloc reports through.
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -27,9 +28,13 @@ __global__ void __launch_bounds__(32) wait_timeout_kernel(uint64_t limit_ns, int
 }  // namespace moe
 
 extern "C" moe_status moe_selftest_wait_timeout(void *ws, uint64_t limit_ns, void *stream) {
-  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MOE_ERR_INVALID_ARG;
   if (limit_ns == 0 || limit_ns > 1000000000ull) return MOE_ERR_INVALID_ARG;
-  moe::wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
-      limit_ns, static_cast<int *>(ws));
+  int *word = static_cast<int *>(ws);
+  if (word == nullptr) {
+    const moe_status st = moe::noalloc_status_word(&word);
+    if (st != MOE_OK) return st;
+  }
+  moe::wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, word);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

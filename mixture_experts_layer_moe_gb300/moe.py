@@ -72,6 +72,7 @@ def _load() -> ctypes.CDLL:
         "moe_workspace_layout_of": [cfgp, ctypes.POINTER(moe_workspace_layout)],
         "moe_route": [cfgp, P, wp, P, P, P, P, SZ, P],
         "moe_route_noalloc": [cfgp, P, wp, P, P, P, P],
+        "moe_route_noalloc_status": [P, ctypes.POINTER(ctypes.c_int32)],
         "moe_route_stats": [cfgp, P, P, ctypes.c_float, P, P, P, P, SZ, P],
         "moe_dispatch": [cfgp, P, P, P, P, P, P, P, P, SZ, P],
         "moe_expert_ffn": [cfgp, P, P, wp, P, P, SZ, P],
@@ -186,6 +187,13 @@ def moe_route_noalloc(cfg, x, w: moe_weights, topk_idx, topk_gate, probs, stream
     _check(_lib.moe_route_noalloc(ctypes.byref(c), _ptr(x), ctypes.byref(w), _ptr(topk_idx),
                                   _ptr(topk_gate), _ptr(probs), _stream(stream)),
            "moe_route_noalloc")
+
+
+def moe_route_noalloc_status(stream=None) -> tuple[int, int]:
+    """(status, detail) of the last moe_route_noalloc on this device (synchronises the stream)."""
+    detail = ctypes.c_int32(0)
+    st = _lib.moe_route_noalloc_status(_stream(stream), ctypes.byref(detail))
+    return st, detail.value
 
 
 def moe_route_stats(cfg, probs, topk_idx, alpha, P, f, aux, ws, stream=None):

@@ -4,7 +4,11 @@ only receive their input/output buffers, fixed-arena runtimes).
 
 It is called through the C ABI directly (ctypes, raw device pointers) and must
 give the same routing as moe_route with a caller-owned workspace, on two calls
-in a row (the static scratch array keeps the previous call's contents).  This
+in a row (the static scratch array keeps the previous call's contents).  Its
+router never splits the reduction over extra CTAs (moe_route may), so the
+logits can differ in the last bits: indices are compared exactly on every
+token whose oracle top-k margin is above the near-tie threshold, and the
+near-tie tokens are checked as valid choices by parity.check_routing.  This
 file is collected last so that a failure here never hides another test."""
 import ctypes
 
@@ -62,12 +66,30 @@ def test_noalloc_route_matches_workspace_route(lib, name, seeds):
         assert lib.moe_status_check(ws)[0] == 0
         got = _outputs(cfg)
         assert _noalloc_raw(lib, cfg, inputs, got) == 0
-        assert torch.equal(got[0], ref[0])
-        assert (got[1] - ref[1]).abs().max().item() <= parity.GATE_ATOL
+        assert lib.moe_route_noalloc_status() == (0, 0)
+        r = O.route(cfg, parity.oracle_inputs(inputs))
+        clear = (r["margin"] >= parity.NEAR_TIE).cuda()
+        assert torch.equal(got[0][clear], ref[0][clear])
+        assert (got[1] - ref[1])[clear].abs().max().item() <= parity.GATE_ATOL
         assert (got[2] - ref[2]).abs().max().item() <= parity.GATE_ATOL
         # and against the oracle, under the same rules as the other routing tests
-        r = O.route(cfg, parity.oracle_inputs(inputs))
         parity.check_routing(cfg, r, got[0].cpu(), got[1].cpu())
+
+
+def test_noalloc_status_reports_a_wait_that_ran_out(lib):
+    """A bounded wait that nothing completes, reporting through the no-allocation
+    router's status word, is visible through moe_route_noalloc_status; the next
+    moe_route_noalloc call clears the word and succeeds."""
+    cfg = moe_synth.CONFIGS["mixtral_bf16"].scaled(n=300, d=256, d_ff=64)
+    inputs = moe_synth.make_inputs(cfg, seed=7, device="cuda")
+    lib.moe_selftest_wait_timeout(None, 20_000_000)         # 20 ms, status word of this device
+    st, _ = lib.moe_route_noalloc_status()
+    assert st == 6, lib.status_string(st)                  # MOE_ERR_TIMEOUT
+    got = _outputs(cfg)
+    assert _noalloc_raw(lib, cfg, inputs, got) == 0
+    assert lib.moe_route_noalloc_status() == (0, 0)
+    r = O.route(cfg, parity.oracle_inputs(inputs))
+    parity.check_routing(cfg, r, got[0].cpu(), got[1].cpu())
 
 
 def test_noalloc_route_rejects_oversize(lib):
