@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -25,6 +26,22 @@ __device__ __forceinline__ void set_status(int *st, int code, int detail) {
 
 __device__ __forceinline__ bool status_failed(const int *st) {
   return st != nullptr && *reinterpret_cast<const volatile int *>(st) != 0;
+}
+
+// -------------------------------------------------------- f16 operand staging
+// The MXFP4 paths feed the tensor cores f16 activations (E2M1 weights are
+// exact in f16).  A bf16 or fp32 value converts exactly when it is zero or
+// |v| lies in [2^-14, 65504]; a smaller magnitude rounds to an f16 subnormal
+// (absolute error at most 2^-25).  |v| > 65504 or NaN cannot be represented:
+// the value is clamped to +-65504 and MOE_ERR_F16_RANGE is recorded (detail:
+// the row), so the layer's result is reported invalid instead of being wrong.
+__device__ __forceinline__ uint16_t f16_bits_checked(float v, int *status, int row) {
+  if (!(fabsf(v) <= 65504.f)) {
+    set_status(status, MOE_ERR_F16_RANGE, row);
+    v = v > 0.f ? 65504.f : -65504.f;
+  }
+  const __half h = __float2half_rn(v);
+  return *reinterpret_cast<const uint16_t *>(&h);
 }
 
 // ------------------------------------------------- programmatic dependent launch

@@ -7,7 +7,7 @@ namespace moe {
 namespace {
 
 // Expert-ordered activation rows as f16: dst[q] = src[perm[q] / top_k] (perm
-// given) or src[q], values clamped to the f16 range.
+// given) or src[q] (f16_bits_checked: values beyond the f16 range are reported).
 __global__ void rows_to_f16_kernel(const __nv_bfloat16 *__restrict__ src,
                                    const int32_t *__restrict__ perm, int top_k, int P, int K,
                                    uint16_t *__restrict__ dst, int *status) {
@@ -27,7 +27,8 @@ __global__ void rows_to_f16_kernel(const __nv_bfloat16 *__restrict__ src,
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xffff0000u);
-      o[j] = (uint32_t)to_f16_bits(lo) | ((uint32_t)to_f16_bits(hi) << 16);
+      o[j] = (uint32_t)f16_bits_checked(lo, status, q) |
+             ((uint32_t)f16_bits_checked(hi, status, q) << 16);
     }
     *reinterpret_cast<uint4 *>(dst + (size_t)q * K + v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
   }
@@ -55,7 +56,8 @@ rows_to_f16_scatter_kernel(const __nv_bfloat16 *__restrict__ src,
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xffff0000u);
-            h[j] = (uint32_t)to_f16_bits(lo) | ((uint32_t)to_f16_bits(hi) << 16);
+            h[j] = (uint32_t)f16_bits_checked(lo, status, t) |
+                   ((uint32_t)f16_bits_checked(hi, status, t) << 16);
           }
           o[u] = make_uint4(h[0], h[1], h[2], h[3]);
         }

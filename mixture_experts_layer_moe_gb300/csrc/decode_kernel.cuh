@@ -22,7 +22,8 @@
 // scale and added to the fp32 accumulator.
 //
 // Activations enter the tensor core as f16 (E2M1 values are exact in f16);
-// an activation beyond the f16 range (|v| > 65504) is clamped to it.
+// an activation beyond the f16 range (|v| > 65504) is reported through the
+// status word (f16_bits_checked).
 #pragma once
 
 #include "common.cuh"
@@ -139,11 +140,6 @@ __device__ __forceinline__ void nv_block(float (&acc)[4], uint32_t wg, uint32_t 
             hmul2_bits(ah.v[3], sh), b.z, b.w);
 }
 
-__device__ __forceinline__ uint16_t to_f16_bits(float v) {
-  v = fminf(fmaxf(v, -65504.f), 65504.f);
-  const __half h = __float2half_rn(v);
-  return *reinterpret_cast<const uint16_t *>(&h);
-}
 
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
                                           uint64_t *bar) {
@@ -710,7 +706,9 @@ decode_mxfp4_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
           if (tk < cnt && row < R) {
             const __nv_bfloat16 hb = __float2bfloat16_rn(v);
             a.out[(size_t)(beg + tk) * R + row] = hb;
-            if (a.out16) a.out16[(size_t)(beg + tk) * R + row] = to_f16_bits(__bfloat162float(hb));
+            if (a.out16)
+              a.out16[(size_t)(beg + tk) * R + row] =
+                  f16_bits_checked(__bfloat162float(hb), a.status, beg + tk);
           }
         }
       }

@@ -21,19 +21,15 @@ constexpr int DR_THREADS = 256;
 constexpr int DR_WARPS = DR_THREADS / 32;
 constexpr int DR_UNROLL = 4;          // x vectors in flight per thread
 
-__device__ __forceinline__ uint16_t f16_bits_clamped(float v) {
-  v = fminf(fmaxf(v, -65504.f), 65504.f);
-  const __half h = __float2half_rn(v);
-  return *reinterpret_cast<const uint16_t *>(&h);
-}
-
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 raw) {
+// 8 bf16 values of row `row` -> f16 (f16_bits_checked: out-of-range values reported)
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 raw, int *status, int row) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
   uint32_t o[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xffff0000u);
-    o[j] = (uint32_t)f16_bits_clamped(lo) | ((uint32_t)f16_bits_clamped(hi) << 16);
+    o[j] = (uint32_t)f16_bits_checked(lo, status, row) |
+           ((uint32_t)f16_bits_checked(hi, status, row) << 16);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -124,15 +120,17 @@ decode_route_kernel(const float *__restrict__ logits, int n, int E, int k, int g
   const int P = n * k;
   pdl_launch_dependents();
   pdl_wait();
-  // the same answer in every CTA: nothing writes the status word meanwhile
+  // (the x conversion below may record MOE_ERR_F16_RANGE while other CTAs
+  // start, so CTAs can read different answers here: only the conversion
+  // depends on it; the selection and the dispatch arrays are always built)
   const bool failed = status_failed(status);
   const bool router = blockIdx.x < DR_CLUSTER;
 
+  if (router)
+    for (int t = blockIdx.x + DR_CLUSTER * warp; t < n; t += DR_CLUSTER * DR_WARPS)
+      select_topk_warp(logits + (size_t)t * E, E, k, gate_mode, lane, topk_idx + (size_t)t * k,
+                       topk_gate + (size_t)t * k, nullptr);
   if (!failed) {
-    if (router)
-      for (int t = blockIdx.x + DR_CLUSTER * warp; t < n; t += DR_CLUSTER * DR_WARPS)
-        select_topk_warp(logits + (size_t)t * E, E, k, gate_mode, lane,
-                         topk_idx + (size_t)t * k, topk_gate + (size_t)t * k, nullptr);
     const int nvec = n * (d / 8);
     const int stride = gridDim.x * DR_THREADS;
     const uint4 *xs = reinterpret_cast<const uint4 *>(x);
@@ -145,7 +143,8 @@ decode_route_kernel(const float *__restrict__ logits, int n, int E, int k, int g
         if (base + j * stride < nvec) r[j] = xs[base + j * stride];
 #pragma unroll
       for (int j = 0; j < DR_UNROLL; ++j)
-        if (base + j * stride < nvec) xd[base + j * stride] = bf16x8_to_f16x8(r[j]);
+        if (base + j * stride < nvec)
+          xd[base + j * stride] = bf16x8_to_f16x8(r[j], status, (base + j * stride) / (d / 8));
     }
   }
   if (!router) return;
@@ -154,12 +153,16 @@ decode_route_kernel(const float *__restrict__ logits, int n, int E, int k, int g
   // visible to CTA 0 after the wait
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
                    "memory");
-  if (failed || blockIdx.x != 0) return;
+  if (blockIdx.x != 0) return;
 
   for (int p = threadIdx.x; p < P; p += DR_THREADS) {
-    const int e = topk_idx[p];
+    int e = topk_idx[p];
+    if (e < 0 || e >= E) {   // (the selection writes indices in range)
+      set_status(status, MOE_ERR_BAD_INDEX, p);
+      e = -1;
+    }
     s_idx[p] = e;
-    atomicAdd(&s_cnt[e], 1);
+    if (e >= 0) atomicAdd(&s_cnt[e], 1);
   }
   __syncthreads();
   if (warp == 1 && pool.slot_of)

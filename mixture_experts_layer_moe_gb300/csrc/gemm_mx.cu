@@ -186,12 +186,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// bf16 bits -> f16 bits (clamped to the f16 range)
-__device__ __forceinline__ uint16_t f16_bits_of_bf16(uint32_t b) {
-  const float v = fminf(fmaxf(__uint_as_float(b << 16), -65504.f), 65504.f);
-  const __half h = __float2half_rn(v);
-  return *reinterpret_cast<const uint16_t *>(&h);
-}
 
 __host__ __device__ inline size_t g_scale_pitch(int K) {
   return ((size_t)GM * (K / 32) + 15) & ~(size_t)15;
@@ -430,7 +424,9 @@ gemm_mx_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
                 const uint32_t hb = (i & 1) ? (packed[c][i >> 1] >> 16)
                                             : (packed[c][i >> 1] & 0xffffu);
                 o[(size_t)tok * args.N + col] = (uint16_t)hb;
-                if (args.out16) args.out16[(size_t)tok * args.N + col] = f16_bits_of_bf16(hb);
+                if (args.out16)
+                  args.out16[(size_t)tok * args.N + col] =
+                      f16_bits_checked(__uint_as_float(hb << 16), args.status, tok);
               }
             }
           }

@@ -615,6 +615,8 @@ const char *moe_status_string(moe_status s) {
     case MOE_ERR_BAD_INDEX: return "MOE_ERR_BAD_INDEX: index out of range on the device";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: device pipeline wait ran out";
     case MOE_ERR_RANGE: return "MOE_ERR_RANGE: MXFP4 block scale outside the exact range";
+    case MOE_ERR_F16_RANGE:
+      return "MOE_ERR_F16_RANGE: MXFP4 layer activation outside the f16 operand range";
   }
   return "unknown moe_status";
 }
