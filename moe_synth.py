@@ -222,6 +222,41 @@ def make_inputs(cfg: MoEConfig, seed: int = 0, device="cpu") -> dict:
     return out
 
 
+# Scale applied to the matrices that read a layer's input (the router Wg and
+# the experts' gate and up matrices W1, W3) in the layers after the first of
+# a stack: the synthetic FP4 layers have a gain of about 2^5 (rms of y over
+# rms of x is 30-40), so each later layer sees inputs ~2^5 larger than the
+# first; without the scale the activations would leave every finite range
+# within a few layers and the router logits would grow with them.  A real
+# model keeps its activations at one scale with a normalisation before each
+# MoE layer; this stands in for it.
+STACK_GATE_UP_SCALE_LOG2 = -5
+
+
+def make_stack_inputs(cfg: MoEConfig, layer: int, seed: int = 0, device="cpu") -> dict:
+    """Inputs of layer `layer` of a stack: layer 0 is make_inputs(seed); layer
+    l > 0 draws its own weights from seed + 101 l, then scales Wg, W1 and W3 by
+    2^STACK_GATE_UP_SCALE_LOG2 (exact powers of two: Wg times 2^-5; MXFP4 E8M0
+    bytes of W1, W3 lowered by 5; NVFP4 matrix scales G1, G3 times 2^-5), so
+    that the stack's activations and router logits keep the scale of the
+    first layer's.  FP4 formats only: other stacks keep the plain draws."""
+    if layer == 0:
+        return make_inputs(cfg, seed=seed, device=device)
+    out = make_inputs(cfg, seed=seed + 101 * layer, device=device)
+    k = -STACK_GATE_UP_SCALE_LOG2
+    if cfg.weight_dtype in ("mxfp4", "nvfp4"):
+        out["Wg"] = (out["Wg"].float() * 2.0 ** -k).to(out["Wg"].dtype)
+    if cfg.weight_dtype == "mxfp4":
+        out["S1"] = out["S1"] - k
+        if out.get("S3") is not None:
+            out["S3"] = out["S3"] - k
+    elif cfg.weight_dtype == "nvfp4":
+        out["G1"] = out["G1"] * 2.0 ** -k
+        if out.get("G3") is not None:
+            out["G3"] = out["G3"] * 2.0 ** -k
+    return out
+
+
 def to_cpu(inputs: dict) -> dict:
     return {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inputs.items()}
 

@@ -136,9 +136,28 @@ def check_output(cfg, y_gpu: torch.Tensor, y_oracle: torch.Tensor):
     return ratio
 
 
+def sample_rows(cfg, topk_idx: torch.Tensor, sample: int, seed: int) -> torch.Tensor:
+    """Seeded sample of `sample` token rows (first and last included), widened so
+    that every expert some token selects has at least one of its tokens in it."""
+    g = torch.Generator().manual_seed(1234 + seed)
+    chosen = torch.zeros(cfg.n, dtype=torch.bool)
+    chosen[torch.randperm(cfg.n, generator=g)[:sample]] = True
+    chosen[0] = chosen[cfg.n - 1] = True
+    idx = topk_idx.to(torch.int64)
+    covered = torch.zeros(cfg.E, dtype=torch.bool)
+    covered[idx[chosen].reshape(-1)] = True
+    used = torch.bincount(idx.reshape(-1), minlength=cfg.E) > 0
+    for e in torch.nonzero(used & ~covered, as_tuple=True)[0].tolist():
+        t = torch.nonzero((idx == e).any(dim=1), as_tuple=True)[0][0].item()
+        chosen[t] = True
+        covered[idx[t]] = True
+    return torch.nonzero(chosen, as_tuple=True)[0]
+
+
 def full_parity(lib, cfg, seed=0, sample=None):
     """moe_forward vs oracle.  sample: number of token rows for the expert outputs
-    (None = all); routing and dispatch are always checked for every token."""
+    (None = all); a sample is widened to cover every expert with c_e > 0.
+    Routing and dispatch are always checked for every token."""
     inputs = moe_synth.make_inputs(cfg, seed=seed, device="cuda")
     y, ws, L, inter = run_forward(lib, cfg, inputs)
     oin = oracle_inputs(inputs)
@@ -149,12 +168,17 @@ def full_parity(lib, cfg, seed=0, sample=None):
     if sample is None or sample >= cfg.n:
         tokens = torch.arange(cfg.n)
     else:
-        g = torch.Generator().manual_seed(1234 + seed)
-        tokens = torch.sort(torch.randperm(cfg.n, generator=g)[:sample]).values
-        tokens[0] = 0
-        tokens[-1] = cfg.n - 1
+        tokens = sample_rows(cfg, inter["topk_idx"], sample, seed)
+    sel = inter["topk_idx"][tokens].to(torch.int64).reshape(-1)
+    covered = torch.bincount(sel, minlength=cfg.E) > 0
+    used = inter["counts"] > 0
+    assert torch.equal(covered, used), "the checked rows miss a non-empty expert"
     res = O.forward(cfg, oin, tokens=tokens, routing=r2)
     err = check_output(cfg, y[tokens.cuda()], res["y"])
     logit_err = (inter["logits"].double() - r["logits"]).abs().max().item()
-    return dict(err=err, near_ties=listed, counts=inter["counts"], y=y, inputs=inputs, ws=ws,
-                logit_err=logit_err)
+    ties = [dict(token=t, margin=float(r["margin"][t]),
+                 oracle=[int(v) for v in r["topk_idx"][t].tolist()],
+                 gpu=[int(v) for v in inter["topk_idx"][t].tolist()]) for t in listed]
+    return dict(err=err, near_ties=listed, near_tie_records=ties, counts=inter["counts"], y=y,
+                inputs=inputs, ws=ws, logit_err=logit_err, rows_checked=int(tokens.numel()),
+                experts_covered=int(covered.sum()), experts_used=int(used.sum()))

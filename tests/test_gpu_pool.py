@@ -168,3 +168,31 @@ def test_forward_pooled_staged_hook(lib):
     names = [lib.STAGES[st] for st, _ in seen]
     assert names == ["route", "dispatch", "ffn_up", "ffn_down", "combine", "end"]
     assert seen[-1][1] == 5                          # kernels launched
+
+
+@pytest.mark.parametrize("name", ["decode_n16", "decode_odd_blocks"])
+def test_forward_pooled_matches_oracle(lib, name):
+    """moe_forward_pooled against the fp64 oracle directly (every token), with
+    half of the experts resident, on a seed of its own."""
+    cfg = CASES[name]
+    inputs = moe_synth.make_inputs(cfg, seed=9, device="cuda")
+    n_slots = max(1, cfg.E // 2)
+    slot_of = moe_synth.make_slot_table(cfg.E, n_slots, n_slots, seed=13)
+    pool = moe_synth.make_pool(inputs, slot_of, n_slots, device="cuda")
+    slot_dev = slot_of.cuda()
+    y = torch.empty(cfg.n, cfg.d, dtype=torch.bfloat16, device="cuda")
+    state, miss, counts = _pool_outputs(cfg)
+    ws = lib.alloc_workspace(cfg)
+    lib.moe_forward_pooled(cfg, inputs["x"], lib.make_weights(inputs),
+                           lib.make_pool(slot_dev, pool), y, state, miss, counts, ws)
+    st, detail = lib.moe_status_check(ws)
+    assert st == 0, (lib.status_string(st), detail)
+    L = lib.moe_workspace_layout_of(cfg)
+    idx = parity.ws_view(ws, L, "topk_idx", torch.int32, cfg.n * cfg.k).view(cfg.n, cfg.k).cpu()
+    gate = parity.ws_view(ws, L, "topk_gate", torch.float32, cfg.n * cfg.k).view(cfg.n, cfg.k).cpu()
+    oin = parity.oracle_inputs(inputs)
+    r = O.route(cfg, oin)
+    listed = parity.check_routing(cfg, r, idx, gate)
+    ref = O.forward(cfg, oin, routing=parity.routing_with_gpu_ties(cfg, r, idx, listed))
+    parity.check_output(cfg, y, ref["y"])
+    _check_classification(lib, cfg, idx, slot_of, state, miss, counts)

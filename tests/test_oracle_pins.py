@@ -147,6 +147,32 @@ def test_topk_margin_examples():
     assert math.isinf(O.topk_margin(torch.zeros(1, 1, dtype=torch.float64), 1).item())
 
 
+def check_near_ties():
+    """near_ties lists exactly the rows whose top-k margin is strictly below the
+    threshold: gaps built from binary fractions so that "below" is exact."""
+    h = 2.0 ** -16                        # the threshold of this check
+    l = torch.tensor([[1.0, 1.0 - h, 0.0],            # margin h: not listed (not below)
+                      [1.0, 1.0 - h / 2, 0.0],        # margin h/2: listed
+                      [0.5, 0.5, 0.25],               # exact tie at rank 1: listed
+                      [0.75, 0.5, 0.5 - h / 4],       # k = 2: boundary gap h/4 (k = 1: 0.25)
+                      [0.0, 2.0, 1.0]], dtype=torch.float64)
+    r1 = {"margin": O.topk_margin(l, 1)}
+    assert O.near_ties(r1, h).tolist() == [1, 2]
+    r2 = {"margin": O.topk_margin(l, 2)}
+    assert O.near_ties(r2, h).tolist() == [1, 2, 3]
+    # default threshold of the parity rules (1e-5 in logit units)
+    r3 = {"margin": torch.tensor([0.0, 9.9e-6, 1e-5, 1.1e-5, math.inf], dtype=torch.float64)}
+    assert O.near_ties(r3).tolist() == [0, 1]
+
+
+def test_near_ties():
+    check_near_ties()
+
+
+def _bad_near_ties(routing, threshold=1e-5):       # "at most" instead of "below"
+    return torch.nonzero(routing["margin"] <= threshold, as_tuple=True)[0]
+
+
 # ------------------------------------------------------------- dispatch pins
 
 def check_dispatch_example(golden_dir):
@@ -666,6 +692,7 @@ MUTANTS = [
     ("nvfp4_decode", _bad_nvfp4, lambda gd: check_nvfp4_bruteforce()),
     ("classify_experts", _bad_classify, check_expert_cache_example),
     ("classify_experts", _bad_classify_slot0, lambda gd: check_classify_bruteforce()),
+    ("near_ties", _bad_near_ties, lambda gd: check_near_ties()),
 ]
 
 
