@@ -49,7 +49,7 @@ def test_single_process_helpers():
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.job_throughput(4096, 1, 0.5) == 8192.0
     args = bench.parse_args([])
-    assert args.gpus == 1 and args.warmup >= 3 and args.config == "mixtral_bf16"
+    assert args.gpus == 1 and args.warmup >= 3 and args.config == "finegrained_shared_bf16"
 
 
 def test_dominant_kernel_flops():
