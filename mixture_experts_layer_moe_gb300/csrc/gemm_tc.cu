@@ -626,6 +626,7 @@ int gemm_tc_router_ksplit(const GemmStage &g, size_t plane_room) {
 
 cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s) {
   if (g.b_dtype == MOE_MXFP4) return launch_gemm_mx(g, status, s);
+  if (g.epi <= 2 && gemm_t2_supported(g)) return launch_gemm_t2(g, status, s);
   switch (g.epi) {
     case 0: return launch_epi<0>(g, status, s);
     case 1: return launch_epi<1>(g, status, s);
