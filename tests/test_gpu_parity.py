@@ -77,6 +77,14 @@ SMALL = {
     "prefill_mx_cuda_core": C["gptoss_prefill_zipf_mxfp4"].scaled(n=500, d=256, d_ff=352, E=8),
     "finegrained_small": C["finegrained_shared_bf16"].scaled(n=500, d=256, d_ff=128, E=32,
                                                              d_ff_shared=192),
+    # whole layers with tensor-core routers of more than 32 experts: 200
+    # experts (two column tiles, the second ragged) with the reduction split
+    # over four CTAs and a 44-row last row tile; 64 experts with the router
+    # bias, unsplit; 40 of 64 experts chosen per token
+    "router_e200_split": C["finegrained_shared_bf16"].scaled(n=300, d=2048, d_ff=64, E=200,
+                                                             d_ff_shared=0),
+    "router_e64_bias": C["gptoss_prefill_zipf_mxfp4"].scaled(n=4000, d=256, d_ff=64, E=64),
+    "router_e64_k40": C["mixtral_bf16"].scaled(n=200, d=256, d_ff=64, E=64, k=40),
 }
 
 
