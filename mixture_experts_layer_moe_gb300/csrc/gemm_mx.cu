@@ -40,10 +40,13 @@
 // (256 columns per CTA): the accumulator, then GS stages of 32 columns of A.
 #include "common.cuh"
 #include "launch.h"
+#include "mx_common.cuh"
 #include "tc_common.cuh"
 
 namespace moe {
 namespace {
+
+using namespace mx;
 
 constexpr int GM = 128;                         // weight rows per tile (MMA M)
 constexpr int GN = 128;                         // tokens per tile at most (MMA N)
@@ -103,37 +106,6 @@ __device__ __forceinline__ GTile g_decode(const GShared &sh, int E, int t) {
   return tl;
 }
 
-__device__ __forceinline__ uint4 e2m1x8_to_f16x2x4(uint32_t w) {
-  uint4 r;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "r"(w));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// E8M0 byte -> 2^(s-127) as an f16 pair; 0 (and *bad set) outside f16's normal range.
-__device__ __forceinline__ uint32_t scale_f16x2(uint32_t s, bool &bad) {
-  if (s < 113u || s > 142u) {
-    bad = true;
-    return 0u;
-  }
-  const uint32_t h = (s - 112u) << 10;
-  return h | (h << 16);
-}
-
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src)
-               : "memory");
-}
-
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (f16 inputs, fp32 accumulate).
 __device__ __forceinline__ void mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -143,49 +115,6 @@ __device__ __forceinline__ void mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-
-// 32 lanes x 32 consecutive 32-bit columns from registers (thread l of the
-// warp -> lane 32*(warp%4) + l).
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
-          taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
-      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
-      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
-      "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-
-// 32 lanes x 16 consecutive 32-bit columns into registers.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_st_wait() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// silu(a) * b; the quotient by the fast reciprocal (h is rounded to bf16)
-__device__ __forceinline__ float silu_mul(float a, float b) {
-  return __fdividef(a, 1.f + __expf(-a)) * b;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t *>(&h);
-}
-
 
 __host__ __device__ inline size_t g_scale_pitch(int K) {
   return ((size_t)GM * (K / 32) + 15) & ~(size_t)15;

@@ -52,10 +52,13 @@
 // no tiles.
 #include "common.cuh"
 #include "launch.h"
+#include "pair_common.cuh"
 #include "tc_common.cuh"
 
 namespace moe {
 namespace {
+
+using namespace pair;
 
 constexpr int PM = 128;                         // weight rows per CTA (MMA M = 256 per pair)
 constexpr int PN = 256;                         // tokens per tile at most (MMA N)
@@ -144,96 +147,6 @@ __device__ __forceinline__ PTile p_decode(const PShared &sh, int E, int t, int n
   tl.ntok = min(bt, end - tl.tok0);
   tl.seg_end = min(end, tl.tok0 + bt);
   return tl;
-}
-
-// ---- cluster-pair primitives ----------------------------------------------
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Address of the same shared-memory object in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-// Arrive on an mbarrier of any CTA of the cluster (address from map_to_rank).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-// TMA tile loads into this CTA's shared memory whose completion is counted on
-// an mbarrier of either CTA of the pair (bar: shared::cluster address).
-__device__ __forceinline__ void tma2_load_2d(const CUtensorMap *m, uint32_t bar, void *dst, int x,
-                                             int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(tc::smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma2_load_3d(const CUtensorMap *m, uint32_t bar, void *dst, int x,
-                                             int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(tc::smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc2(uint32_t *dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   tc::smem_u32(dst_smem)),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
-// D[tmem of both CTAs] (+)= A[smem of both CTAs] * B[smem halves]^T, bf16 -> fp32.
-__device__ __forceinline__ void mma2_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrives on the barrier at this shared-memory offset in both CTAs of the
-// pair once every MMA issued before has completed.
-__device__ __forceinline__ void mma2_commit_both(uint64_t *bar) {
-  const uint16_t mask = 0x3;
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(tc::smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
-// Arrives on this CTA's barrier once every MMA issued before has completed.
-__device__ __forceinline__ void mma2_commit_self(uint64_t *bar) {
-  const uint16_t mask = 0x1;   // the first CTA of the pair: the only one issuing MMAs
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(tc::smem_u32(bar)),
-      "h"(mask)
-      : "memory");
 }
 
 __device__ __forceinline__ float silu_mul(float a, float b) {
@@ -382,7 +295,7 @@ gemm_t2_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ 
         const int ntok = tl.ntok;
         const uint32_t idesc = tc::idesc_bf16_f32(2 * PM, (ntok + 15) & ~15);
         const int acc = local & 1;
-        if (!tc::mbar_wait(&sh.tempty[acc], ((local >> 1) & 1) ^ 1u, abort)) { ok = false; break; }
+        if (!mbar_wait_cluster(&sh.tempty[acc], ((local >> 1) & 1) ^ 1u, abort)) { ok = false; break; }
         tc::tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * PN);
         for (int kb = 0; kb < KB; ++kb) {
