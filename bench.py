@@ -268,13 +268,19 @@ def run_ours(args):
         x = torch.randn(inputs["x"].shape, generator=g, device=device, dtype=torch.float32)
         inputs["x"] = (x * cfg.x_std).to(inputs["x"].dtype)
     w = moe.make_weights(inputs)
-    # further layers of the stack: their own seeded weights, same shapes
-    layer_inputs = [inputs] + [moe_synth.make_stack_inputs(cfg, l, seed=args.seed, device=device)
-                               for l in range(1, args.layers)]
-    layer_w = [w] + [moe.make_weights(li) for li in layer_inputs[1:]]
     ws = moe.alloc_workspace(cfg, device)
     y = torch.empty(cfg.n, cfg.d, dtype=inputs["x"].dtype, device=device)
     mid = [torch.empty_like(y) for _ in range(2)]
+    # further layers of the stack: their own seeded weights, same shapes.
+    # Each layer reads its own token batch (layer l of step i the batch
+    # i + l of the rotation) rather than the previous layer's output: a chain
+    # of these random layers, which has none of a model's residual
+    # connections, collapses onto a few experts (n = 64: 116 experts with
+    # tokens in layer 0, 8 from layer 9 on), a routing no model step has.
+    # The layers still run one after another on one stream.
+    layer_inputs = [inputs] + [moe_synth.make_stack_inputs(cfg, l, seed=args.seed, device=device)
+                               for l in range(1, args.layers)]
+    layer_w = [w] + [moe.make_weights(li) for li in layer_inputs[1:]]
 
     # expert-slot indirection: a seeded resident set per layer, copied into a
     # slot pool; the classification of every layer lands in its own counts
@@ -294,10 +300,12 @@ def run_ours(args):
         pool_state = torch.empty(cfg.E, dtype=torch.int32, device=device)
         pool_miss = torch.empty(cfg.E, dtype=torch.int32, device=device)
 
-    def run_layers(x_in, y_out, hook=None):
-        """Layer 0 .. L-1 in sequence; the stage hook instruments layer 0."""
-        cur = x_in
+    def run_layers(x_in, y_out, hook=None, active=None, batch=0):
+        """Layer 0 .. L-1 in sequence; the stage hook instruments layer 0.
+        Layer 0 reads x_in, layer l > 0 token batch batch + l of the rotation.
+        active (a list): receives each layer's count of experts with tokens."""
         for l in range(args.layers):
+            cur = x_in if l == 0 else x_pool[(batch + l) % len(x_pool)]
             out = y_out if l == args.layers - 1 else mid[l % 2]
             if pools:
                 if l == 0 and hook is not None:
@@ -310,7 +318,9 @@ def run_ours(args):
                 moe.moe_forward_staged(cfg, cur, layer_w[l], out, ws, hook, stream)
             else:
                 moe.moe_forward(cfg, cur, layer_w[l], out, ws, stream)
-            cur = out
+            if active is not None:
+                torch.cuda.synchronize(device)
+                active.append(int((counts > 0).sum().item()))
     # a non-default stream: CUDA graphs cannot be captured on the legacy default stream
     stream = torch.cuda.Stream(device)
     torch.cuda.set_stream(stream)
@@ -327,22 +337,25 @@ def run_ours(args):
         xr = torch.randn(inputs["x"].shape, generator=gr, device=device, dtype=torch.float32)
         x_pool.append((xr * cfg.x_std).to(inputs["x"].dtype))
 
-    def step(i, events=None):
+    def step(i, events=None, active=None):
         def hook(stage, kernels):
             if events is not None:
                 events[stage].record(stream)
             if stage == len(stage_names) - 1:
                 launches["n"] = kernels
-        run_layers(x_pool[i % n_batches], y, hook)
+        run_layers(x_pool[i % n_batches], y, hook, active, batch=i)
 
     L = moe.moe_workspace_layout_of(cfg)
     counts = ws[L["counts"]:L["counts"] + 4 * cfg.E].view(torch.int32)
-    active_per_batch, served = [], []
+    # experts with tokens, per token batch: layer 0 (the instrumented one) and
+    # the whole stack
+    active_per_batch, stack_active_per_batch, served = [], [], []
     for i in range(max(args.warmup, n_batches)):
-        step(i)
+        per_layer = [] if i < n_batches else None
+        step(i, active=per_layer)
         if i < n_batches:
-            torch.cuda.synchronize(device)
-            active_per_batch.append(int((counts > 0).sum().item()))
+            active_per_batch.append(per_layer[0])
+            stack_active_per_batch.append(per_layer)
             for pc in pool_counts:
                 c4 = pc.tolist()
                 served.append(c4[moe.POOL_SERVED] / c4[moe.POOL_LOOKUPS])
@@ -522,15 +535,20 @@ def run_ours(args):
     per_launch = ({"flops_per_launch": dom_units} if bound == "tensor"
                   else {"bytes_per_launch": dom_units, "active_experts_mean": active})
     if is_decode(cfg):
-        # the whole layer against HBM on its algorithmic bytes: the selected
-        # experts' weights once each, the router's weights, x in and y out
-        layer_bytes = (active * moe_synth.weight_bytes_per_expert(cfg)
-                       + cfg.E * cfg.d * 2 + 2 * cfg.n * cfg.d * 2) * args.layers
+        # the whole layer (stack) against HBM on its algorithmic bytes: each
+        # layer's selected experts' weights once each, the router's weights,
+        # x in and y out
+        stack_active = statistics.mean(sum(stack_active_per_batch[i % n_batches])
+                                       for i in range(args.steps))
+        layer_bytes = (stack_active * moe_synth.weight_bytes_per_expert(cfg)
+                       + (cfg.E * cfg.d * 2 + 2 * cfg.n * cfg.d * 2) * args.layers)
         layer_gbs = layer_bytes / (t_job / args.steps) / 1e9
         per_launch["whole_layer"] = {
             "bytes_per_step": layer_bytes, "achieved": layer_gbs, "unit": "GB/s",
             "frac": layer_gbs / peaks["hbm_gbs"],
-            "bytes": "selected experts' weights (codes + scales) + router weights + x + y"}
+            "bytes": "selected experts' weights (codes + scales) + router weights + x + y",
+            **({"active_experts_per_layer_first_batch": stack_active_per_batch[0]}
+               if args.layers > 1 else {})}
 
     out = {
         "metric": ("MoE-layer tokens/s" if args.layers == 1 else
@@ -550,6 +568,10 @@ def run_ours(args):
             "workload": workload_name(cfg),
             "tokens_per_rank": cfg.n,
             "layers_per_step": args.layers,
+            **({"stack": "independently seeded layers run in sequence on one stream; layer l "
+                         "reads its own token batch (a chain of these random layers without "
+                         "residual connections collapses onto a few experts)"}
+               if args.layers > 1 else {}),
             "parallelism": f"dp{world} (independent token batches, replicated weights)",
             "l2": l2_note,
             "timing": timing,

@@ -247,7 +247,8 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const moe_weights *
 /* Stages of moe_forward, in launch order. */
 typedef enum {
   MOE_STAGE_ROUTE = 0,     /* router logits, softmax, top-k, gates */
-  MOE_STAGE_DISPATCH = 1,  /* counting sort + gather of x rows */
+  MOE_STAGE_DISPATCH = 1,  /* counting sort + gather of x rows (for MXFP4 prefill, their
+                              f16 copies) */
   MOE_STAGE_FFN_UP = 2,    /* grouped GEMM x_perm -> h (activation fused) */
   MOE_STAGE_FFN_DOWN = 3,  /* grouped GEMM h -> y_perm */
   MOE_STAGE_SHARED = 4,    /* shared expert (only when d_ff_shared > 0) */

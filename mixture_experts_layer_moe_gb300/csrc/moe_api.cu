@@ -182,8 +182,9 @@ bool mx_tc_path(const moe_config &c) {
 }
 
 // MXFP4 prefill on tensor cores: f16 copies of the expert-ordered rows (x
-// scattered in token order through inv_perm, or x_perm converted in place),
-// then the up and down grouped GEMMs with on-the-fly dequantisation.
+// scattered in token order through inv_perm: the dispatch's gather of the
+// rows, run before the FFN stage begins; or x_perm converted in place), then
+// the up and down grouped GEMMs with on-the-fly dequantisation.
 template <typename StageFn>
 moe_status run_mx_ffn(const moe_config &c, const void *act, const int32_t *inv_perm,
                       const int32_t *offsets, const moe_weights *w, void *y_perm, void *ws,
@@ -192,13 +193,15 @@ moe_status run_mx_ffn(const moe_config &c, const void *act, const int32_t *inv_p
   int *status = at<int>(ws, L.status);
   GemmStage up, dn;
   mx_stages(c, offsets, w, ws, y_perm, up, dn);
-  stage(MOE_STAGE_FFN_UP, 2);
-  if (inv_perm)
+  if (inv_perm) {
     MOE_TRY(cuda_status(launch_rows_to_f16_scatter(act, inv_perm, c.top_k, c.n, c.d,
                                                    at<void>(ws, L.act16), status, s)));
-  else
+    stage(MOE_STAGE_FFN_UP, 1);
+  } else {
+    stage(MOE_STAGE_FFN_UP, 2);
     MOE_TRY(cuda_status(launch_rows_to_f16(act, nullptr, c.top_k, c.n * c.top_k, c.d,
                                            at<void>(ws, L.act16), status, s)));
+  }
   MOE_TRY(cuda_status(launch_gemm_tc(up, status, s)));
   stage(MOE_STAGE_FFN_DOWN, 1);
   return cuda_status(launch_gemm_tc(dn, status, s));
@@ -496,10 +499,11 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
   MOE_TRY(cuda_status(launch_route(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits),
                                    at<float>(ws, L.h), (size_t)P * c.d_ff * h_size(c), topk_idx,
                                    gates, nullptr, status, s, at<int>(ws, L.route_count))));
-  // (the sort, plus the copy of x rows into segment order on the bf16/fp32 path)
+  // (the sort, plus the copy of x rows into segment order: bf16/fp32 rows, or
+  // the f16 copies the MXFP4 tensor-core path reads)
   stage(MOE_STAGE_DISPATCH,
         dispatch_kernels(P, c.n_experts, at<void>(ws, L.h), (size_t)P * c.d_ff * h_size(c)) +
-            ((decode || mx_tc) ? 0 : 1));
+            (decode ? 0 : 1));
   MOE_TRY(cuda_status(launch_dispatch(P, c.n_experts, topk_idx, at<int32_t>(ws, L.counts), offsets,
                                       perm, inv_perm, status, s, at<void>(ws, L.h),
                                       (size_t)P * c.d_ff * h_size(c))));

@@ -222,39 +222,50 @@ def make_inputs(cfg: MoEConfig, seed: int = 0, device="cpu") -> dict:
     return out
 
 
-# Scale applied to the matrices that read a layer's input (the router Wg and
-# the experts' gate and up matrices W1, W3) in the layers after the first of
-# a stack: the synthetic FP4 layers have a gain of about 2^5 (rms of y over
-# rms of x is 30-40), so each later layer sees inputs ~2^5 larger than the
-# first; without the scale the activations would leave every finite range
-# within a few layers and the router logits would grow with them.  A real
-# model keeps its activations at one scale with a normalisation before each
-# MoE layer; this stands in for it.
-STACK_GATE_UP_SCALE_LOG2 = -5
+def make_stack_inputs(cfg: MoEConfig, layer: int, seed: int = 0, device="cpu",
+                      in_log2: int = 0) -> dict:
+    """Inputs of layer `layer` of a stack of MoE layers: layer 0 is
+    make_inputs(seed); layer l > 0 draws its own weights from seed + 101 l.
 
-
-def make_stack_inputs(cfg: MoEConfig, layer: int, seed: int = 0, device="cpu") -> dict:
-    """Inputs of layer `layer` of a stack: layer 0 is make_inputs(seed); layer
-    l > 0 draws its own weights from seed + 101 l, then scales Wg, W1 and W3 by
-    2^STACK_GATE_UP_SCALE_LOG2 (exact powers of two: Wg times 2^-5; MXFP4 E8M0
-    bytes of W1, W3 lowered by 5; NVFP4 matrix scales G1, G3 times 2^-5), so
-    that the stack's activations and router logits keep the scale of the
-    first layer's.  FP4 formats only: other stacks keep the plain draws."""
+    A stack feeds each layer's output to the next, and SwiGLU experts are
+    quadratic in their input, so without a normalisation between the layers
+    the activations leave every finite range within a few layers (the
+    synthetic gpt-oss layer turns rms 1 into rms ~38).  A real model
+    normalises each MoE layer's input; here the matrices that read the input
+    (the router Wg and the experts' W1 and W3) are scaled by 2^-in_log2
+    instead, in_log2 being the log2 of the previous layer's output rms
+    (rounded), so every layer sees its input at the scale of the first
+    layer's.  The scale is an exact power of two: Wg times 2^-in_log2, MXFP4
+    E8M0 bytes of W1 and W3 lowered by in_log2, NVFP4 matrix scales G1 and G3
+    times 2^-in_log2; bf16 and fp32 experts scale W1 and W3 themselves."""
     if layer == 0:
         return make_inputs(cfg, seed=seed, device=device)
     out = make_inputs(cfg, seed=seed + 101 * layer, device=device)
-    k = -STACK_GATE_UP_SCALE_LOG2
-    if cfg.weight_dtype in ("mxfp4", "nvfp4"):
-        out["Wg"] = (out["Wg"].float() * 2.0 ** -k).to(out["Wg"].dtype)
+    k = int(in_log2)
+    if k == 0:
+        return out
+    out["Wg"] = (out["Wg"].float() * 2.0 ** -k).to(out["Wg"].dtype)
     if cfg.weight_dtype == "mxfp4":
-        out["S1"] = out["S1"] - k
-        if out.get("S3") is not None:
-            out["S3"] = out["S3"] - k
+        for key in ("S1", "S3"):
+            if out.get(key) is not None:
+                out[key] = (out[key].to(torch.int32) - k).clamp(0, 254).to(torch.uint8)
     elif cfg.weight_dtype == "nvfp4":
-        out["G1"] = out["G1"] * 2.0 ** -k
-        if out.get("G3") is not None:
-            out["G3"] = out["G3"] * 2.0 ** -k
+        for key in ("G1", "G3"):
+            if out.get(key) is not None:
+                out[key] = out[key] * 2.0 ** -k
+    else:
+        for key in ("W1", "W3"):
+            if out.get(key) is not None:
+                out[key] = (out[key].float() * 2.0 ** -k).to(out[key].dtype)
     return out
+
+
+def stack_in_log2(y: torch.Tensor) -> int:
+    """The input scale exponent for the layer after one whose output is y: the
+    log2 of y's rms, rounded to an integer."""
+    import math
+    rms = float(y.float().pow(2).mean().sqrt())
+    return int(round(math.log2(rms))) if rms > 0 else 0
 
 
 def to_cpu(inputs: dict) -> dict:

@@ -5,9 +5,9 @@ Still Hits a Ceiling" and the setup section).
 
 Three gpt-oss-shaped decode layers with independently seeded weights run back
 to back in one captured graph, each reading the previous layer's bf16 output
-(layers after the first scale their gate and up matrices by 2^-5, as
-moe_synth.make_stack_inputs describes, in place of the normalisation a real
-model applies before each MoE layer).
+(layers after the first scale their router and gate/up matrices to the
+previous layer's output rms, as moe_synth.make_stack_inputs describes, in
+place of the normalisation a real model applies before each MoE layer).
 Each layer is compared with the fp64 oracle applied to the bf16 input that
 layer received (the previous layer's output, as the GPU rounded it), under the
 same rules as a single layer: routing and dispatch bit-exact (near ties
@@ -37,11 +37,20 @@ def lib():
 @pytest.mark.parametrize("n", [4, 64])
 def test_decode_stack_in_one_graph(lib, n):
     cfg = moe_synth.CONFIGS["gptoss_decode_mxfp4"].scaled(n=n)
-    layers = [moe_synth.make_stack_inputs(cfg, l, seed=0, device="cuda") for l in range(LAYERS)]
-    weights = [lib.make_weights(li) for li in layers]
     wss = [lib.alloc_workspace(cfg) for _ in range(LAYERS)]
-    x0 = layers[0]["x"]
     ys = [torch.empty(cfg.n, cfg.d, dtype=torch.bfloat16, device="cuda") for _ in range(LAYERS)]
+    # each later layer's input-reading matrices scaled to the previous output
+    layers = [moe_synth.make_stack_inputs(cfg, 0, seed=0, device="cuda")]
+    weights = [lib.make_weights(layers[0])]
+    x0 = layers[0]["x"]
+    cur = x0
+    for l in range(1, LAYERS):
+        lib.moe_forward(cfg, cur, weights[l - 1], ys[l - 1], wss[l - 1])
+        shift = moe_synth.stack_in_log2(ys[l - 1])
+        layers.append(moe_synth.make_stack_inputs(cfg, l, seed=0, device="cuda", in_log2=shift))
+        weights.append(lib.make_weights(layers[l]))
+        cur = ys[l - 1]
+    torch.cuda.synchronize()
     s = torch.cuda.Stream()
 
     def stack():
