@@ -181,17 +181,29 @@ def is_decode(cfg) -> bool:
     return cfg.weight_dtype in ("mxfp4", "nvfp4") and cfg.n * cfg.k <= DECODE_MAX_PAIRS
 
 
-def dominant_kernel(cfg, active_experts=None):
+def layer_bytes(cfg, active_experts):
+    """Algorithmic bytes of one small-batch layer: each selected expert's weights
+    (codes + scales) once, the router's weights, x in and y out."""
+    return (active_experts * moe_synth.weight_bytes_per_expert(cfg)
+            + cfg.E * cfg.d * 2 + 2 * cfg.n * cfg.d * 2)
+
+
+def dominant_kernel(cfg, active_experts=None, fused=False):
     """(stage name, bound, algorithmic units per launch, unit) of the dominant kernel.
 
     Tensor-bound workloads: the up-projection grouped GEMM (W1 and W3, 2/3 of the
     expert FLOPs with SwiGLU), FLOPs = 2 * (n*k) * d * d_ff * (2 for SwiGLU, else 1).
-    Small-batch FP4 (decode): the up-projection kernel streams the selected
-    experts' W1/W3 codes and scales once, reads the tokens' x rows and writes h:
-    bytes = u * mats * d_ff * (d/2 + d/32) + n*k*d*2 + n*k*d_ff*2 (MXFP4; NVFP4
-    has d/16 scale bytes per row and one fp32 scale per matrix).
+    Small-batch FP4 (decode) run as one fused launch: that launch, whose bytes are
+    the whole layer's (layer_bytes).  Small-batch FP4 run as chained launches: the
+    up-projection kernel streams the selected experts' W1/W3 codes and scales once,
+    reads the tokens' x rows and writes h: bytes = u * mats * d_ff * (d/2 + d/32)
+    + n*k*d*2 + n*k*d_ff*2 (MXFP4; NVFP4 has d/16 scale bytes per row and one fp32
+    scale per matrix).
     """
     mats = 2 if cfg.act == "swiglu" else 1
+    if is_decode(cfg) and fused:
+        u = active_experts if active_experts is not None else min(cfg.E, cfg.n * cfg.k)
+        return "fused", "hbm", layer_bytes(cfg, u), "GB/s"
     if is_decode(cfg):
         u = active_experts if active_experts is not None else min(cfg.E, cfg.n * cfg.k)
         P = cfg.n * cfg.k
@@ -338,11 +350,16 @@ def run_ours(args):
         xr = torch.randn(inputs["x"].shape, generator=gr, device=device, dtype=torch.float32)
         x_pool.append((xr * cfg.x_std).to(inputs["x"].dtype))
 
+    end_stage = stage_names.index("end")
+    seen_order = []   # stage ids in the order the hook reports them (one step)
+
     def step(i, events=None, active=None):
         def hook(stage, kernels):
             if events is not None:
                 events[stage].record(stream)
-            if stage == len(stage_names) - 1:
+            if not seen_order or seen_order[-1] != end_stage:
+                seen_order.append(stage)
+            if stage == end_stage:
                 launches["n"] = kernels
         run_layers(x_pool[i % n_batches], y, hook, active, batch=i)
 
@@ -364,10 +381,11 @@ def run_ours(args):
     st, detail = moe.moe_status_check(ws)
     if st != 0:
         raise RuntimeError(f"device status {moe.status_string(st)} ({detail})")
-    step_units = [dominant_kernel(cfg, active_per_batch[i % n_batches])[2]
+    fused = stage_names.index("fused") in seen_order
+    step_units = [dominant_kernel(cfg, active_per_batch[i % n_batches], fused)[2]
                   for i in range(args.steps)]
     active = statistics.mean(active_per_batch[i % n_batches] for i in range(args.steps))
-    dom_stage, bound, _, dom_unit = dominant_kernel(cfg)
+    dom_stage, bound, _, dom_unit = dominant_kernel(cfg, fused=fused)
     dom_units = statistics.mean(step_units)
 
     # The timed region: K steps captured into one CUDA graph (external event
@@ -422,17 +440,13 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device status {moe.status_string(st)} ({detail})")
 
-    # per-stage durations (CUDA events on the launching stream, inside the timed region)
-    dom_idx = stage_names.index(dom_stage)
-    present = [s for s in range(len(stage_names) - 1)
-               if s != stage_names.index("shared") or cfg.d_ff_shared]
+    # per-stage durations (CUDA events on the launching stream, inside the
+    # timed region): each stage runs from its event to the next stage's
     stage_ms = {}
-    for s in present:
-        nxt = next((t for t in range(s + 1, len(stage_names))
-                    if t in present or t == len(stage_names) - 1))
+    for s, nxt in zip(seen_order, seen_order[1:]):
         stage_ms[stage_names[s]] = statistics.mean(
             ev[i][s].elapsed_time(ev[i][nxt]) for i in range(args.steps))
-    dom_ms = sum(ev[i][dom_idx].elapsed_time(ev[i][dom_idx + 1]) for i in range(args.steps)) / args.steps
+    dom_ms = stage_ms[dom_stage]
     del graph, plain
 
     # end to end: every step copies its x from pinned host memory, runs the
@@ -541,11 +555,11 @@ def run_ours(args):
         # x in and y out
         stack_active = statistics.mean(sum(stack_active_per_batch[i % n_batches])
                                        for i in range(args.steps))
-        layer_bytes = (stack_active * moe_synth.weight_bytes_per_expert(cfg)
+        stack_bytes = (stack_active * moe_synth.weight_bytes_per_expert(cfg)
                        + (cfg.E * cfg.d * 2 + 2 * cfg.n * cfg.d * 2) * args.layers)
-        layer_gbs = layer_bytes / (t_job / args.steps) / 1e9
+        layer_gbs = stack_bytes / (t_job / args.steps) / 1e9
         per_launch["whole_layer"] = {
-            "bytes_per_step": layer_bytes, "achieved": layer_gbs, "unit": "GB/s",
+            "bytes_per_step": stack_bytes, "achieved": layer_gbs, "unit": "GB/s",
             "frac": layer_gbs / peaks["hbm_gbs"],
             "bytes": "selected experts' weights (codes + scales) + router weights + x + y",
             **({"active_experts_per_layer_first_batch": stack_active_per_batch[0]}

@@ -253,7 +253,9 @@ typedef enum {
   MOE_STAGE_FFN_DOWN = 3,  /* grouped GEMM h -> y_perm */
   MOE_STAGE_SHARED = 4,    /* shared expert (only when d_ff_shared > 0) */
   MOE_STAGE_COMBINE = 5,   /* gate scaling + un-permute */
-  MOE_STAGE_END = 6        /* after the last launch */
+  MOE_STAGE_END = 6,       /* after the last launch */
+  MOE_STAGE_FUSED = 7      /* the whole layer in one launch (small-batch MXFP4 SwiGLU layers
+                              with n <= 16 and d <= 3072): in place of stages 0..5 */
 } moe_stage;
 
 /* Host callback run by moe_forward_staged on the calling thread just before

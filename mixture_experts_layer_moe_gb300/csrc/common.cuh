@@ -44,6 +44,45 @@ __device__ __forceinline__ uint16_t f16_bits_checked(float v, int *status, int r
   return *reinterpret_cast<const uint16_t *>(&h);
 }
 
+// 8 bf16 values of row `row` -> f16 bit patterns, each through f16_bits_checked.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_checked(uint4 raw, int *status, int row) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xffff0000u);
+    o[j] = (uint32_t)f16_bits_checked(lo, status, row) |
+           ((uint32_t)f16_bits_checked(hi, status, row) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ----------------------------------------------------------- router dot product
+// One 8-element piece of a bf16 router row against the same piece of a bf16 x
+// row: a fresh fp32 partial, products added with fmaf in element order.  The
+// small-batch router kernels add these partials piece by piece (lane l takes
+// pieces l, l + 32, ...) and then combine the 32 lane sums with
+// warp_sum_xor, so that every kernel that computes router logits this way
+// gets the same bits.
+__device__ __forceinline__ float bf16x8_dot(const uint4 &w, const uint4 &x) {
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  const uint32_t xx[4] = {x.x, x.y, x.z, x.w};
+  float part = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    part = fmaf(__uint_as_float(ww[i] << 16), __uint_as_float(xx[i] << 16), part);
+    part = fmaf(__uint_as_float(ww[i] & 0xffff0000u), __uint_as_float(xx[i] & 0xffff0000u), part);
+  }
+  return part;
+}
+
+// Sum over the warp by a butterfly (xor 16, 8, 4, 2, 1): every lane gets it.
+__device__ __forceinline__ float warp_sum_xor(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 // ------------------------------------------------- programmatic dependent launch
 // A kernel launched with launch_pdl may start while the previous kernel in the
 // stream is still running: it calls pdl_launch_dependents() to let the next

@@ -195,6 +195,26 @@ cudaError_t launch_decode_route(const moe_config &c, const float *logits, const 
                                 int *status, cudaStream_t s,
                                 const moe_expert_pool *pool = nullptr, int32_t *state = nullptr,
                                 int32_t *miss_list = nullptr, int32_t *pool_counts = nullptr);
+// The whole small-batch layer in one cooperative launch (decode_layer.cu):
+// router, selection, dispatch, both expert projections and combine, for
+// MXFP4 SwiGLU experts with n <= 16 tokens and d <= 3072 (the chained
+// launches above cover the rest, and are faster from about 32 tokens on).  Workspace arrays it writes, as the chained
+// path does; sync is decode_layer_sync_bytes() of zeroed counters.
+struct DecodeLayerBuffers {
+  float *logits;
+  int32_t *topk_idx;
+  float *topk_gate;
+  int32_t *counts, *offsets, *perm, *inv_perm;
+  void *act16, *h, *y_perm, *y;
+  int *sync;
+  int *status;
+  int32_t *state, *miss_list, *pool_counts;   // with a pool (each nullable)
+};
+bool decode_layer_supported(const moe_config &c);
+size_t decode_layer_sync_bytes();
+cudaError_t launch_decode_layer(const moe_config &c, const void *x, const moe_weights &w,
+                                const moe_expert_pool *pool, const DecodeLayerBuffers &b,
+                                cudaStream_t s);
 // Hit/miss classification of topk_idx against slot_of (one CTA; E <= 256).
 cudaError_t launch_classify(const moe_config &c, const int32_t *topk_idx, const int32_t *slot_of,
                             int n_slots, int32_t *state, int32_t *miss_list, int32_t *counts,

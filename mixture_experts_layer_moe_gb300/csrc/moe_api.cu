@@ -81,7 +81,7 @@ moe_status check_expert_weights(const moe_config &c, const moe_weights *w) {
 }
 
 struct Layout {
-  size_t status, route_count, logits, topk_idx, topk_gate, counts, offsets, perm, inv_perm,
+  size_t status, route_count, sync, logits, topk_idx, topk_gate, counts, offsets, perm, inv_perm,
       x_perm, h, y_perm, y_shared, h_shared, act16, total;
 };
 
@@ -95,9 +95,11 @@ Layout layout_of(const moe_config &c) {
     return at;
   };
   L.status = take(kAlign);
-  // right after the status word, so that one memset clears both: per 128-row
-  // router tile, the CTAs of a split reduction that have finished it
+  // right after the status word, so that one memset clears them all: per
+  // 128-row router tile, the CTAs of a split reduction that have finished it;
+  // then the counters of the fused small-batch layer launch
   L.route_count = take(((size_t)c.n + 127) / 128 * 4);
+  L.sync = take(decode_layer_sync_bytes());
   L.logits = take(n * E * 4);
   L.topk_idx = take(P * 4);
   L.topk_gate = take(P * 4);
@@ -128,6 +130,10 @@ moe_status check_ws(const moe_config &c, const void *ws, size_t ws_bytes) {
 }
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Bytes from the status word through the per-launch counters (one memset
+// clears them all before a forward pass).
+size_t cleared_bytes(const Layout &L) { return L.sync - L.status + decode_layer_sync_bytes(); }
 
 #define MOE_TRY(expr)                   \
   do {                                  \
@@ -257,10 +263,12 @@ moe_status run_expert_ffn(const moe_config &c, const void *x_perm, const int32_t
   return cuda_status(launch_gemm(dn, status, s));
 }
 
-// The small-batch forward: the router's linear layer, selection + dispatch +
-// f16 x rows in one launch (plus the hit/miss classification against the
-// pool, if any), the two FFN kernels streaming the selected experts (from
-// their pool slots where resident), combine.
+// The small-batch forward.  MXFP4 SwiGLU layers within the fused kernel's
+// range run as one cooperative launch (decode_layer.cu).  Otherwise: the
+// router's linear layer, selection + dispatch + f16 x rows in one launch
+// (plus the hit/miss classification against the pool, if any), the two FFN
+// kernels streaming the selected experts (from their pool slots where
+// resident), combine.  Both write the same workspace arrays.
 template <typename StageFn>
 moe_status run_small_batch(const moe_config &c, const void *x, const moe_weights *w,
                            const moe_expert_pool *pool, void *y, int32_t *state,
@@ -272,6 +280,29 @@ moe_status run_small_batch(const moe_config &c, const void *x, const moe_weights
   int32_t *perm = at<int32_t>(ws, L.perm);
   int32_t *inv_perm = at<int32_t>(ws, L.inv_perm);
   float *gates = at<float>(ws, L.topk_gate);
+  if (decode_layer_supported(c)) {
+    DecodeLayerBuffers b{};
+    b.logits = at<float>(ws, L.logits);
+    b.topk_idx = at<int32_t>(ws, L.topk_idx);
+    b.topk_gate = gates;
+    b.counts = at<int32_t>(ws, L.counts);
+    b.offsets = offsets;
+    b.perm = perm;
+    b.inv_perm = inv_perm;
+    b.act16 = at<void>(ws, L.act16);
+    b.h = at<void>(ws, L.h);
+    b.y_perm = at<void>(ws, L.y_perm);
+    b.y = y;
+    b.sync = at<int>(ws, L.sync);
+    b.status = status;
+    b.state = state;
+    b.miss_list = miss_list;
+    b.pool_counts = pool_counts;
+    stage(MOE_STAGE_FUSED, 1);
+    MOE_TRY(cuda_status(launch_decode_layer(c, x, *w, pool, b, s)));
+    stage(MOE_STAGE_END, 0);
+    return MOE_OK;
+  }
   stage(MOE_STAGE_ROUTE, 1);
   MOE_TRY(cuda_status(launch_route_logits(c, x, w->Wg, w->router_bias, at<float>(ws, L.logits),
                                           status, s)));
@@ -481,9 +512,8 @@ moe_status moe_forward_staged(const moe_config *cfg, const void *x, const moe_we
     if (hook) hook(id, launched, user);
     launched += kernels;
   };
-  // the status word and the router's tile counts
-  MOE_TRY(cuda_status(cudaMemsetAsync(
-      status, 0, L.route_count - L.status + ((size_t)c.n + 127) / 128 * 4, s)));
+  // the status word, the router's tile counts and the fused layer's counters
+  MOE_TRY(cuda_status(cudaMemsetAsync(status, 0, cleared_bytes(L), s)));
   int32_t *topk_idx = at<int32_t>(ws, L.topk_idx);
   float *gates = at<float>(ws, L.topk_gate);
   int32_t *offsets = at<int32_t>(ws, L.offsets);
@@ -585,7 +615,7 @@ moe_status moe_forward_pooled_staged(const moe_config *cfg, const void *x, const
   MOE_TRY(check_ws(c, ws, ws_bytes));
   const Layout L = layout_of(c);
   cudaStream_t s = as_stream(stream);
-  MOE_TRY(cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, 2 * sizeof(int), s)));
+  MOE_TRY(cuda_status(cudaMemsetAsync(at<int>(ws, L.status), 0, cleared_bytes(L), s)));
   int launched = 0;
   auto stage = [&](int id, int kernels) {
     if (hook) hook(id, launched, user);

@@ -129,29 +129,15 @@ route_logits_small_kernel(const __nv_bfloat16 *__restrict__ x, const __nv_bfloat
 #pragma unroll
   for (int v = 0; v < RS_MAXV; ++v) {
     if (v < nv) {
-      const uint32_t ww[4] = {wv[v].x, wv[v].y, wv[v].z, wv[v].w};
 #pragma unroll
-      for (int j = 0; j < RS_TOK; ++j) {
-        if (j < nt) {
-          const uint4 xv = xs[j * vpr + lane + 32 * v];
-          const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
-          float part = 0.f;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            part = fmaf(__uint_as_float(ww[i] << 16), __uint_as_float(xx[i] << 16), part);
-            part = fmaf(__uint_as_float(ww[i] & 0xffff0000u), __uint_as_float(xx[i] & 0xffff0000u),
-                        part);
-          }
-          acc[j] += part;
-        }
-      }
+      for (int j = 0; j < RS_TOK; ++j)
+        if (j < nt) acc[j] += bf16x8_dot(wv[v], xs[j * vpr + lane + 32 * v]);
     }
   }
   float mine = 0.f;
 #pragma unroll
   for (int j = 0; j < RS_TOK; ++j) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
+    acc[j] = warp_sum_xor(acc[j]);
     if (lane == j) mine = acc[j];
   }
   if (lane < nt) logits[(size_t)(t0 + lane) * E + e] = mine + (bias ? bias[e] : 0.f);

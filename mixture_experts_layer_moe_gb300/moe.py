@@ -27,7 +27,7 @@ class MoEError(RuntimeError):
 
 
 STAGE_HOOK = ctypes.CFUNCTYPE(None, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p)
-STAGES = ("route", "dispatch", "ffn_up", "ffn_down", "shared", "combine", "end")
+STAGES = ("route", "dispatch", "ffn_up", "ffn_down", "shared", "combine", "end", "fused")
 
 
 class moe_config(ctypes.Structure):

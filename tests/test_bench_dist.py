@@ -58,3 +58,18 @@ def test_dominant_kernel_flops():
     stage, bound, flops, unit = bench.dominant_kernel(cfg)
     assert stage == "ffn_up" and bound == "tensor"
     assert flops == 2 * 4096 * 2 * 4096 * 14336 * 2
+
+
+def test_dominant_kernel_fused_decode_bytes():
+    """A small-batch layer run as one launch is measured on the whole layer's
+    bytes: the selected experts' codes and scales once, the router's weights,
+    x in and y out."""
+    import moe_synth
+    cfg = moe_synth.CONFIGS["gptoss_decode_mxfp4"].scaled(n=4)
+    stage, bound, nbytes, unit = bench.dominant_kernel(cfg, active_experts=15, fused=True)
+    assert (stage, bound, unit) == ("fused", "hbm", "GB/s")
+    per_expert = 3 * (2880 * 2880 // 2 + 2880 * 2880 // 32)
+    assert nbytes == 15 * per_expert + 128 * 2880 * 2 + 2 * 4 * 2880 * 2
+    # the chained launches: the up-projection kernel
+    stage, bound, _, _ = bench.dominant_kernel(cfg, active_experts=15)
+    assert (stage, bound) == ("ffn_up", "hbm")
