@@ -19,10 +19,12 @@
 //      grid, with the per-piece fp32 arithmetic of the small-batch router
 //      kernel (bf16x8_dot, warp_sum_xor: the same logits); every CTA also
 //      converts a share of the x rows to f16;
-//   2. grid barrier; selection of token t by one warp of CTA t; grid barrier;
-//   3. every CTA builds the stable dispatch from the n x k selections itself
-//      (the same code on the same selections in every CTA, hence the same
-//      arrays); CTA 0 writes them out;
+//   2. grid barrier;
+//   3. every CTA selects for all n tokens and builds the stable dispatch
+//      itself (the same code on the same logits in every CTA, hence the same
+//      arrays); CTA 0 writes them out.  The first units' weights start
+//      streaming as soon as the experts with tokens are known, before the
+//      per-token positions are done;
 //   4. work units -- 16 * RG rows of W1 and W3 of one selected expert ("up"),
 //      or 32 * RG rows of its W2 ("down", two 16-row halves per group) -- are
 //      claimed from a global counter in a fixed order: all up units, then all
@@ -61,9 +63,9 @@ constexpr int LY_MAX_D = 32 * 8 * LY_RW;
 // compute the same logits.)
 constexpr int LY_MAX_TOKENS = 16;
 
-// Per-launch counters, zeroed before the launch: the three grid barriers,
-// the unit queue, and per expert the up-unit groups whose h rows are stored.
-enum { SY_BAR1 = 0, SY_BAR2 = 1, SY_QUEUE = 2, SY_BAR3 = 3, SY_UPDONE = 4 };
+// Per-launch counters, zeroed before the launch: the two grid barriers, the
+// unit queue, and per expert the up-unit groups whose h rows are stored.
+enum { SY_BAR1 = 0, SY_BAR2 = 1, SY_QUEUE = 2, SY_UPDONE = 4 };
 
 struct LayerArgs {
   const __nv_bfloat16 *x, *Wg;   // [n][d], [E][d]
@@ -288,34 +290,37 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   // ---- 2. every logit and f16 row is stored
   grid_barrier(&a.sync[SY_BAR1], a.status, &s_flag);
 
-  // ---- 3. selection: token t by warp 0 of CTA t (mod the grid), from its
-  // logits row staged in shared memory; topk_idx and topk_gate go out
-  for (int t = blockIdx.x; t < n; t += gridDim.x) {
-    if (warp == 0) {
-      float *lrow = reinterpret_cast<float *>(smem);
-      for (int e = lane; e < E; e += 32)
-        lrow[e] = __uint_as_float(ld_cg_u32(a.logits + (size_t)t * E + e));
-      __syncwarp();
-      select_topk_warp(lrow, E, k, a.gate_mode, lane, a.topk_idx + (size_t)t * k,
-                       a.topk_gate + (size_t)t * k, nullptr);
-      __syncwarp();
-    }
-  }
-  grid_barrier(&a.sync[SY_BAR2], a.status, &s_flag);
-
-  // ---- 4. the stable dispatch, in every CTA (the same arithmetic on the
-  // same selections: the same arrays); CTA 0 writes them out
+  // ---- 3. selection and the stable dispatch, in every CTA: the same code on
+  // the same logits gives the same arrays in every CTA; CTA 0 writes them
+  // out.  Warp w selects tokens w, w + 8 (at most 16 tokens) from the logits
+  // staged in shared memory (the ring, before the first weight box).
   {
-    for (int p = tid; p < P; p += LY_THREADS) {
-      s_idx[p] = (int32_t)ld_cg_u32(a.topk_idx + p);
-      s_gate[p] = __uint_as_float(ld_cg_u32(a.topk_gate + p));
+    float *lg = reinterpret_cast<float *>(smem);   // [n][E]
+    {
+      // all of a thread's logits in flight at once (n * E <= 16 * 256)
+      constexpr int LB = LY_MAX_TOKENS * 256 / LY_THREADS;
+      uint32_t r[LB];
+#pragma unroll
+      for (int j = 0; j < LB; ++j)
+        if (tid + j * LY_THREADS < n * E) r[j] = ld_cg_u32(a.logits + tid + j * LY_THREADS);
+#pragma unroll
+      for (int j = 0; j < LB; ++j)
+        if (tid + j * LY_THREADS < n * E) lg[tid + j * LY_THREADS] = __uint_as_float(r[j]);
     }
     for (int e = tid; e < 256; e += LY_THREADS) s_ecnt[e] = 0;
+    __syncthreads();
+    for (int t = warp; t < n; t += DV_WARPS)
+      select_topk_warp(lg + (size_t)t * E, E, k, a.gate_mode, lane, s_idx + t * k, s_gate + t * k,
+                       nullptr);
     __syncthreads();
     for (int p = tid; p < P; p += LY_THREADS) {
       const int e = s_idx[p];
       if (e >= 0 && e < E) atomicAdd(&s_ecnt[e], 1);
       else if (blockIdx.x == 0) set_status(a.status, MOE_ERR_BAD_INDEX, p);   // (never: selection)
+      if (blockIdx.x == 0) {
+        a.topk_idx[p] = e;
+        a.topk_gate[p] = s_gate[p];
+      }
     }
     __syncthreads();
     if (warp == 0) {
@@ -360,29 +365,6 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
         seen += __popc(m);
       }
       if (lane == 0) s_nactive = seen;
-      __syncwarp();
-      // stable positions: a pair's rank among equal experts is the number of
-      // earlier pairs with that expert
-      for (int p0 = 0; p0 < P; p0 += 32) {
-        const int p = p0 + lane;
-        int e = p < P ? s_idx[p] : -1;
-        if (e >= E) e = -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0) {
-          const int pos = s_eoff[e] + __popc(peers & lanemask_lt());
-          s_row[pos] = (int16_t)(p / k);
-          s_inv[p] = (int16_t)pos;
-          if (blockIdx.x == 0) {
-            a.perm[pos] = p;
-            a.inv_perm[p] = pos;
-          }
-        } else if (p < P) {
-          s_inv[p] = -1;
-        }
-        __syncwarp();
-        if (e >= 0 && lane == __ffs(peers) - 1) s_eoff[e] += __popc(peers);
-        __syncwarp();
-      }
     }
     if constexpr (POOL) {
       if (warp == 1 && blockIdx.x == 0)
@@ -405,7 +387,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     __syncthreads();
   }
 
-  // ---- 5. the expert units
+  // ---- 4. the expert units
   const int A = s_nactive;
   const int nbu = (d_ff + UROWS - 1) / UROWS, nbd = (d + DROWS - 1) / DROWS;
   const int total = A * (nbu + nbd);
@@ -558,9 +540,35 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     s_nclaimed = NRAW;
   }
   __syncthreads();
+  // the first units' weights start streaming while warp 0 finishes the
+  // dispatch: stable positions, a pair's rank among equal experts being the
+  // number of earlier pairs with that expert
   if (tid == 0)
     for (int j = 0; j < NRAW; ++j) fetch_raw(j);
   if (lane == 0) fill(0);
+  if (warp == 0) {
+    for (int p0 = 0; p0 < P; p0 += 32) {
+      const int p = p0 + lane;
+      int e = p < P ? s_idx[p] : -1;
+      if (e >= E) e = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0) {
+        const int pos = s_eoff[e] + __popc(peers & lanemask_lt());
+        s_row[pos] = (int16_t)(p / k);
+        s_inv[p] = (int16_t)pos;
+        if (blockIdx.x == 0) {
+          a.perm[pos] = p;
+          a.inv_perm[p] = pos;
+        }
+      } else if (p < P) {
+        s_inv[p] = -1;
+      }
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(peers) - 1) s_eoff[e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
   int consumed = 0, npass = 0;
   int pending = -1;   // expert of an up unit whose h rows are stored but not yet counted
   int16_t pend[LY_NPEND];   // (the group's counting thread) experts noted, not yet counted
@@ -864,8 +872,8 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     }
   }
 
-  // ---- 6. every y_perm row is stored; combine
-  grid_barrier(&a.sync[SY_BAR3], a.status, &s_flag);
+  // ---- 5. every y_perm row is stored; combine
+  grid_barrier(&a.sync[SY_BAR2], a.status, &s_flag);
   {
     const int vpr = d / 8;
     const uint4 *yp = reinterpret_cast<const uint4 *>(a.y_perm);
