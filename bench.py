@@ -41,6 +41,10 @@ MEASURED_TRAFFIC = {
     ("mixtral_bf16", 4096, "ffn_up"): 1.973e9 + 0.229e9,
     ("gptoss_prefill_zipf_mxfp4", 8192, "ffn_up"): 1.080e9 + 0.368e9,
     ("gptoss_decode_mxfp4", 64, "ffn_up"): 1.03e9 + 0.00734e9,
+    # the fused small-batch launch (one launch of the rotation's first batch)
+    ("gptoss_decode_mxfp4", 1, "fused"): 53.92e6 + 0.216e6,
+    ("gptoss_decode_mxfp4", 4, "fused"): 201.9e6 + 3.96e6,
+    ("gptoss_decode_mxfp4", 16, "fused"): 710.4e6 + 5.03e6,
 }
 L2_BYTES = 129 * 1024 * 1024
 # a timed loop at least this long runs at the power-capped clock: the sustained
