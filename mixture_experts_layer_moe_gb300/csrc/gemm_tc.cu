@@ -1,35 +1,26 @@
-// Grouped expert GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+// The router's linear layer on the 5th-generation tensor cores (tcgen05 +
+// TMEM + TMA): logits = x Wg^T (+ b) in fp32 ("How Mixture of Experts Scales
+// Model Parameters", section "Routing: a router scores the experts, and the
+// top one runs": the router is one linear layer whose scores go through a
+// softmax).  The expert projections run elsewhere: bf16 on SM pairs
+// (gemm_t2.cu), MXFP4 with the weights dequantised into tensor memory
+// (gemm_mx.cu); launch_gemm_tc sends them there.
 //
-// Each expert runs its FFN projection on its own dispatched segment ("How
-// Mixture of Experts Scales Model Parameters", sections "Dense models" and
-// "The forward pass: dispatch, then combine"):
-//   out[q][j] = epi( sum_i A[q][i] * W_e[j][i] )   for q in segment e,
-// with the SwiGLU form h = silu(A W1_e^T) * (A W3_e^T) fused in the epilogue.
-//
-// Design (one CTA per SM, persistent):
-//   warp 0      TMA producer: A tile 128 x 64 (rows of the segment) and B tile
-//               256 x 64 (W rows of expert e; for SwiGLU 128 rows of W1 then
-//               128 rows of W3) per stage, 128-byte swizzle, 4-stage ring.
+// One CTA per SM, persistent:
+//   warp 0      TMA producer: x tile 128 x 64 (rows) and Wg tile 128 x 64 (EPI
+//               3, up to 128 experts per tile, 6-stage ring) or 32 x 64 (EPI
+//               4, at most 32 experts, 10 stages), 128-byte swizzle.
 //   warp 1      allocates 512 TMEM columns; one thread issues
-//               tcgen05.mma.kind::f16 M=128 N=256 K=16 (fp32 accumulate),
-//               double-buffered accumulators (2 x 256 columns).
-//   warps 2-5   epilogue: tcgen05.ld rows of the accumulator, activation,
-//               bf16 rounding, 16-byte stores masked to the segment.
-// Tiles are ordered expert-major, then output column block, then row block,
-// so CTAs working at the same time share one expert's weight columns and its
-// whole activation segment in L2.  The tile list is derived on the device
-// from the segment offsets; empty segments produce no tiles.
-//
-// The router's linear layer ("Routing: a router scores the experts, and the
-// top one runs") runs as EPI 3 (up to 128 experts per tile, 6-stage ring,
-// four 128-column partials in flight, eight epilogue warps) or EPI 4 (at most
-// 32 experts: MMA N = 32, ten stages, eight partials): each 64-wide k-block
-// is summed into a fresh TMEM partial and the partials are added in fp32
-// registers.  When the row tiles alone leave most SMs idle, a tile's k-blocks
-// are split over up to four CTAs that write fp32 partial planes; the router's
-// selection kernel adds them in plane order.
-//
-// MXFP4 weights run on gemm_mx.cu (dequantised into tensor memory).
+//               tcgen05.mma.kind::f16 M=128 N=128 or 32, K=16 (fp32).
+//   warps 2..   epilogue: tcgen05.ld of each partial, fp32 sums in registers.
+// Each 64-wide k-block is summed into a fresh TMEM partial (four 128-column
+// or eight 32-column partials in flight) and the partials are added in fp32
+// registers.  Tiles run row block first, then expert block, so the CTAs that
+// read one block of x rows for different experts run together and the rows
+// come from DRAM once.  When the row tiles alone leave most SMs idle, a
+// tile's k-blocks are split over up to four CTAs that write fp32 partial
+// planes; the selection (the selection kernel, or for at most 32 experts the
+// CTA that completes the row tile) adds them in plane order.
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -37,19 +28,16 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
 constexpr int MAX_STAGES = 10;
 
-// Ring depth per variant: the router variants stage narrower B tiles, so the
-// same shared memory holds more k-blocks of their A stream in flight.
+// Ring depth per variant: with 32 experts the B tile is narrower, so the same
+// shared memory holds more k-blocks of the x stream in flight.
 __host__ __device__ constexpr int stage_bytes(int epi) {
-  return A_BYTES + (epi == 4 ? 32 : (epi == 3 ? 128 : BN)) * BK * 2;
+  return A_BYTES + (epi == 4 ? 32 : 128) * BK * 2;
 }
-__host__ __device__ constexpr int num_stages(int epi) {
-  return epi == 4 ? MAX_STAGES : (epi == 3 ? 6 : STAGES);
-}
+__host__ __device__ constexpr int num_stages(int epi) { return epi == 4 ? MAX_STAGES : 6; }
 __host__ __device__ constexpr int dyn_smem_bytes(int epi) {
   return num_stages(epi) * stage_bytes(epi) + 1024;
 }
@@ -66,7 +54,7 @@ struct TcArgs {
   int rows;
   int K;
   int N;           // output columns
-  void *out;       // bf16 [rows][N], fp32 for EPI 3 and 4
+  void *out;       // fp32 [rows][N] logits, or [ksplit][rows][N] partial planes
   const float *bias;
   int *status;
   int ksplit;      // router: k ranges per row tile (> 1: partial sums, no bias)
@@ -84,7 +72,7 @@ struct TcArgs {
 struct TcShared {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
-  uint64_t tfull[8];    // accumulator ring: 2, 4 (EPI 3) or 8 (EPI 4)
+  uint64_t tfull[8];    // partial ring: 4 (EPI 3) or 8 (EPI 4)
   uint64_t tempty[8];
   uint64_t drain;
   uint32_t tmem_base;
@@ -100,13 +88,10 @@ struct Tile {
   int e, row0, seg_end, n_idx;
 };
 
-// Tile t of the list: expert-major, then (col_fast false) column block, then
-// row block, so CTAs running together share an expert's weight columns; or
-// (col_fast, the router) row block, then column block, so the CTAs that read
-// one block of rows for different experts run together and the rows come
-// from DRAM once.
-__device__ __forceinline__ Tile decode_tile(const TcShared &sh, int E, int t, int n_tiles = 0,
-                                            bool col_fast = false) {
+// Tile t of the list: row block, then column block (the router's experts),
+// so the CTAs that read one block of rows for different experts run together
+// and the rows come from DRAM once.
+__device__ __forceinline__ Tile decode_tile(const TcShared &sh, int E, int t, int n_tiles) {
   int lo = 0, hi = E;   // largest e with tile_start[e] <= t (skips empty experts)
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -115,25 +100,12 @@ __device__ __forceinline__ Tile decode_tile(const TcShared &sh, int E, int t, in
   Tile tl;
   tl.e = lo;
   const int beg = sh.offs[lo], end = sh.offs[lo + 1];
-  const int m_tiles = (end - beg + BM - 1) / BM;
   const int local = t - sh.tile_start[lo];
-  if (col_fast) {
-    const int m = local / n_tiles;
-    tl.n_idx = local - m * n_tiles;
-    tl.row0 = beg + m * BM;
-  } else {
-    tl.n_idx = local / m_tiles;
-    tl.row0 = beg + (local - tl.n_idx * m_tiles) * BM;
-  }
+  const int m = local / n_tiles;
+  tl.n_idx = local - m * n_tiles;
+  tl.row0 = beg + m * BM;
   tl.seg_end = end;
   return tl;
-}
-
-__device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + __expf(-a)) * b; }
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 // Selection of one router row by one thread (E <= 32 logits in registers),
@@ -186,11 +158,10 @@ __device__ __forceinline__ void select_row(const float (&l)[32], int E, int k, i
   for (int j = 0; j < k; ++j) gate[j] = gate[j] / denom;
 }
 
-// EPI: 0 plain, 1 relu, 2 swiglu (B = W1 rows, B3 = W3 rows, 128 each),
-// 3 fp32 output + per-column bias (router logits), 4 the same for at most 32
-// columns.
+// EPI 3: fp32 logits + per-column bias, up to 128 experts per tile; EPI 4:
+// the same for at most 32 experts (and optionally the selection).
 //
-// EPI 3 and 4 keep the router's logits accurate to fp32 rounding: the tensor
+// Both keep the router's logits accurate to fp32 rounding: the tensor
 // core sums each 64-wide k-block into a fresh TMEM partial (N = 128 or 32
 // columns, four or eight partials in flight), and the epilogue warps add the
 // partials in fp32 registers with round-to-nearest.  Accumulating the whole
@@ -199,19 +170,17 @@ __device__ __forceinline__ void select_row(const float (&l)[32], int E, int k, i
 template <int EPI>
 __global__ void __launch_bounds__(threads_of(EPI), 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmB3, TcArgs args) {
-  constexpr bool KPART = (EPI == 3 || EPI == 4);    // per-k-block partials
-  // MMA N = B rows per stage: the router takes 128 experts per tile, or 32
-  // (EPI 4) when there are at most 32, so a layer with 8 experts does not
-  // drain 128 accumulator columns per k-block
-  constexpr int BNT = KPART ? (EPI == 4 ? 32 : 128) : BN;
-  // accumulators in flight and their TMEM column pitch: the routers keep
-  // four (128 columns) or eight (32 columns) partials in flight so the MMAs
-  // run ahead of the epilogue's drains
-  constexpr int NACC = (EPI == 4) ? 8 : (EPI == 3 ? 4 : 2);
-  constexpr int ACC_COLS = KPART ? BNT : BN;
+               TcArgs args) {
+  static_assert(EPI == 3 || EPI == 4, "router variants");
+  // MMA N = B rows per stage: 128 experts per tile, or 32 (EPI 4) when there
+  // are at most 32, so a layer with 8 experts does not drain 128 accumulator
+  // columns per k-block
+  constexpr int BNT = EPI == 4 ? 32 : 128;
+  // partials in flight, so the MMAs run ahead of the epilogue's drains
+  constexpr int NACC = EPI == 4 ? 8 : 4;
+  constexpr int ACC_COLS = BNT;
   constexpr int EPI_WARPS = epi_warps(EPI);
-  constexpr int N_OUT = (EPI == 2) ? BN / 2 : BNT;   // output columns per tile
+  constexpr int N_OUT = BNT;   // output columns per tile
   constexpr int NSTAGE = num_stages(EPI);
   constexpr int SBYTES = stage_bytes(EPI);
   constexpr int NTHREADS = threads_of(EPI);
@@ -224,7 +193,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int n_tiles = (args.N + N_OUT - 1) / N_OUT;
   const int KB = (args.K + BK - 1) / BK;
   // work unit t: row/column tile t / KS over k-blocks [k_begin, k_end)
-  const int KS = KPART ? args.ksplit : 1;
+  const int KS = args.ksplit;
   auto k_begin = [&](int t) { return (int)((int64_t)(t % KS) * KB / KS); };
   auto k_end = [&](int t) { return (int)((int64_t)(t % KS + 1) * KB / KS); };
 
@@ -232,7 +201,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // descriptor fetches overlap the setup below instead of the first copy
     tc::prefetch_tmap(&tmA);
     tc::prefetch_tmap(&tmB);
-    if (EPI == 2) tc::prefetch_tmap(&tmB3);
     sh.failed_on_entry = status_failed(args.status) ? 1 : 0;
     sh.abort = sh.failed_on_entry;
   }
@@ -283,7 +251,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int total = __shfl_sync(0xffffffffu, incl, 31);
     bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
-      sh.num_tiles = bad ? 0 : total * (KPART ? args.ksplit : 1);
+      sh.num_tiles = bad ? 0 : total * args.ksplit;
       if (bad) set_status(args.status, MOE_ERR_BAD_INDEX, -1);
     }
   }
@@ -303,7 +271,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
       for (int s = 0; s < NSTAGE; ++s) last_phase[s] = -1;
       for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
-        const Tile tl = decode_tile(sh, E, t / KS, n_tiles, KPART);
+        const Tile tl = decode_tile(sh, E, t / KS, n_tiles);
         const int wrow = tl.n_idx * N_OUT;
         const int kb1 = k_end(t);
         for (int kb = k_begin(t); kb < kb1; ++kb) {
@@ -312,12 +280,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           uint8_t *sb = sa + A_BYTES;
           tc::mbar_arrive_expect_tx(&sh.full[stage], TX_BYTES);
           tc::tma_load_2d(&tmA, &sh.full[stage], sa, kb * BK, tl.row0);
-          if (EPI == 2) {
-            tc::tma_load_3d(&tmB, &sh.full[stage], sb, kb * BK, wrow, tl.e);
-            tc::tma_load_3d(&tmB3, &sh.full[stage], sb + B_BYTES / 2, kb * BK, wrow, tl.e);
-          } else {
-            tc::tma_load_3d(&tmB, &sh.full[stage], sb, kb * BK, wrow, tl.e);
-          }
+          tc::tma_load_3d(&tmB, &sh.full[stage], sb, kb * BK, wrow, tl.e);
           last_phase[stage] = (int)phase;
           if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
         }
@@ -335,18 +298,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BNT);
       int stage = 0;
       uint32_t phase = 0;
-      int local = 0;   // accumulator uses so far (tiles, or k-blocks with KPART)
+      int local = 0;   // partials used so far (one per k-block)
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok && !*abort; t += gridDim.x) {
         const int kb1 = k_end(t);
         for (int kb = k_begin(t); kb < kb1; ++kb) {
-          const bool fresh = KPART || kb == 0;
           const int acc = local % NACC;
-          if (fresh) {
-            const uint32_t acc_phase = (local / NACC) & 1;
-            if (!tc::mbar_wait(&sh.tempty[acc], acc_phase ^ 1u, abort)) { ok = false; break; }
-            tc::tc_fence_after();
-          }
+          const uint32_t acc_phase = (local / NACC) & 1;
+          if (!tc::mbar_wait(&sh.tempty[acc], acc_phase ^ 1u, abort)) { ok = false; break; }
+          tc::tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
           if (!tc::mbar_wait(&sh.full[stage], phase, abort)) { ok = false; break; }
           tc::tc_fence_after();
@@ -355,13 +315,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             tc::mma_bf16(d_tmem, tc::smem_desc_sw128(sa + k * 32), tc::smem_desc_sw128(sb + k * 32),
-                         idesc, (k != 0 || (!KPART && kb != 0)) ? 1u : 0u);
+                         idesc, k != 0 ? 1u : 0u);
           tc::mma_commit(&sh.empty[stage]);
           if (++stage == NSTAGE) { stage = 0; phase ^= 1u; }
-          if (KPART || kb == KB - 1) {
-            tc::mma_commit(&sh.tfull[acc]);
-            ++local;
-          }
+          tc::mma_commit(&sh.tfull[acc]);
+          ++local;
         }
       }
       if (*abort) {
@@ -375,12 +333,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int r_local = quarter * 32 + lane;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
     int local = 0;
-    if constexpr (KPART) {
+    {
       // the warps of one lane quarter split the columns: NCOL from col_off
       constexpr int NCOL = N_OUT / (EPI_WARPS / 4);
       const int col_off = ((warp - 2) >> 2) * NCOL;
       for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-        const Tile tl = decode_tile(sh, E, t / KS, n_tiles, KPART);
+        const Tile tl = decode_tile(sh, E, t / KS, n_tiles);
         float sum[NCOL];
 #pragma unroll
         for (int i = 0; i < NCOL; ++i) sum[i] = 0.f;
@@ -474,56 +432,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         __syncwarp();
       }
-    } else {
-      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
-        const Tile tl = decode_tile(sh, E, t);
-        const int acc = local & 1;
-        const uint32_t acc_phase = (local >> 1) & 1;
-        const bool ok = tc::mbar_wait(&sh.tfull[acc], acc_phase, abort);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        tc::tc_fence_after();
-        const uint32_t tb = lane_base + (uint32_t)(acc * BN);
-        const int row = tl.row0 + r_local;
-        const bool row_ok = row < tl.seg_end;
-        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(args.out) + (size_t)row * args.N;
-        constexpr int CHUNKS = N_OUT / 32;
-#pragma unroll 1
-        for (int c = 0; c < CHUNKS; ++c) {
-          uint32_t a[32];
-          uint32_t b[EPI == 2 ? 32 : 1];
-          tc::tmem_ld32(tb + c * 32, a);
-          if constexpr (EPI == 2) tc::tmem_ld32(tb + N_OUT + c * 32, b);
-          tc::tmem_ld_wait();
-          if (c == CHUNKS - 1) {
-            tc::tc_fence_before();
-            tc::mbar_arrive(&sh.tempty[acc]);
-          }
-          const int col0 = tl.n_idx * N_OUT + c * 32;
-          if (row_ok && col0 < args.N) {
-            uint32_t packed[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float v0 = __uint_as_float(a[2 * i]), v1 = __uint_as_float(a[2 * i + 1]);
-              if constexpr (EPI == 1) {
-                v0 = fmaxf(v0, 0.f);
-                v1 = fmaxf(v1, 0.f);
-              } else if constexpr (EPI == 2) {
-                v0 = silu_mul(v0, __uint_as_float(b[2 * i]));
-                v1 = silu_mul(v1, __uint_as_float(b[2 * i + 1]));
-              }
-              packed[i] = pack_bf16x2(v0, v1);
-            }
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              if (col0 + v * 8 < args.N) {
-                *reinterpret_cast<uint4 *>(orow + col0 + v * 8) = make_uint4(
-                    packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-              }
-            }
-          }
-          __syncwarp();
-        }
-      }
     }
   }
 
@@ -551,10 +459,10 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
     smem_set = smem;
   }
   const int E = g.offsets ? g.num_experts : 1;
-  CUtensorMap mA, mB, mB3;
+  CUtensorMap mA, mB;
   const uint64_t dA[2] = {(uint64_t)g.K, (uint64_t)g.rows};
   const uint32_t bA[2] = {BK, BM};
-  const int wrows = (EPI == 2) ? BN / 2 : (EPI == 3 ? 128 : (EPI == 4 ? 32 : BN));
+  const int wrows = EPI == 3 ? 128 : 32;
   if (!make_tensor_map(&mA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.A, 2, dA, bA,
                        CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
@@ -563,13 +471,6 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
   if (!make_tensor_map(&mB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.B, 3, dB, bB,
                        CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if (EPI == 2) {
-    if (!make_tensor_map(&mB3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.B3, 3, dB, bB,
-                         CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  } else {
-    mB3 = mB;
-  }
   TcArgs a{};
   a.offsets = g.offsets;
   a.num_experts = g.num_experts;
@@ -579,7 +480,7 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
   a.out = g.out;
   a.bias = g.col_bias;
   a.status = status;
-  a.ksplit = (EPI == 3 || EPI == 4) && g.ksplit > 1 ? g.ksplit : 1;
+  a.ksplit = g.ksplit > 1 ? g.ksplit : 1;
   if (EPI == 4 && gemm_tc_router_fuses(g)) {
     a.sel_idx = g.sel_idx;
     a.sel_gate = g.sel_gate;
@@ -589,7 +490,7 @@ cudaError_t launch_epi(const GemmStage &g, int *status, cudaStream_t s) {
     a.top_k = g.top_k;
     a.gate_mode = g.gate_mode;
   }
-  gemm_tc_kernel<EPI><<<num_sms(), threads_of(EPI), smem, s>>>(mA, mB, mB3, a);
+  gemm_tc_kernel<EPI><<<num_sms(), threads_of(EPI), smem, s>>>(mA, mB, a);
   return cudaGetLastError();
 }
 
@@ -599,10 +500,11 @@ bool gemm_tc_supported(const GemmStage &g) {
   if (g.rows <= 0 || !tensor_maps_available()) return false;
   // MXFP4: the weights-in-tensor-memory kernel of gemm_mx.cu
   if (g.b_dtype == MOE_MXFP4) return gemm_mx_supported(g);
-  const bool out_ok = g.epi == 3 ? g.out_dtype == MOE_F32 : g.out_dtype == MOE_BF16;
-  const bool n_ok = g.epi == 3 ? true : g.N % 8 == 0;
-  // (epi 3 with N <= 32 runs as the 32-column router variant)
-  return g.a_dtype == MOE_BF16 && g.b_dtype == MOE_BF16 && out_ok && n_ok && g.K % 8 == 0;
+  // bf16 expert projections: the SM-pair kernel of gemm_t2.cu
+  if (g.epi <= 2) return gemm_t2_supported(g);
+  // the router (epi 3; with N <= 32 the 32-column variant)
+  return g.epi == 3 && g.a_dtype == MOE_BF16 && g.b_dtype == MOE_BF16 &&
+         g.out_dtype == MOE_F32 && g.K % 8 == 0;
 }
 
 bool gemm_tc_router_fuses(const GemmStage &g) {
@@ -626,13 +528,8 @@ int gemm_tc_router_ksplit(const GemmStage &g, size_t plane_room) {
 
 cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s) {
   if (g.b_dtype == MOE_MXFP4) return launch_gemm_mx(g, status, s);
-  if (g.epi <= 2 && gemm_t2_supported(g)) return launch_gemm_t2(g, status, s);
-  switch (g.epi) {
-    case 0: return launch_epi<0>(g, status, s);
-    case 1: return launch_epi<1>(g, status, s);
-    case 2: return launch_epi<2>(g, status, s);
-    default: return g.N <= 32 ? launch_epi<4>(g, status, s) : launch_epi<3>(g, status, s);
-  }
+  if (g.epi <= 2) return launch_gemm_t2(g, status, s);
+  return g.N <= 32 ? launch_epi<4>(g, status, s) : launch_epi<3>(g, status, s);
 }
 
 }  // namespace moe

@@ -126,8 +126,10 @@ struct GemmStage {
 };
 cudaError_t launch_gemm_simt(const GemmStage &g, int *status, cudaStream_t s);
 
-// The same stage on tcgen05 tensor cores (bf16 operands, fp32 accumulate in
-// TMEM, TMA-fed); gemm_tc_supported() says whether the shape/dtypes qualify.
+// The same stage on tcgen05 tensor cores (fp32 accumulate in TMEM, TMA-fed):
+// MXFP4 weights go to gemm_mx.cu, bf16 expert projections (epi 0-2) to the
+// SM-pair kernel of gemm_t2.cu, the router (epi 3) to gemm_tc.cu;
+// gemm_tc_supported() says whether the shape/dtypes qualify.
 bool gemm_tc_supported(const GemmStage &g);
 cudaError_t launch_gemm_tc(const GemmStage &g, int *status, cudaStream_t s);
 // Split of the router's reduction that fills the SMs (1: no split), given
