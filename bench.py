@@ -255,7 +255,7 @@ def time_oracle_step(scfg, sub):
 def default_cpu_sample(cfg):
     return {"tiny_switch_fp32": 256, "mixtral_bf16": 4096, "gptoss_decode_mxfp4": cfg.n,
             "gptoss_decode_nvfp4": cfg.n,
-            "gptoss_prefill_zipf_mxfp4": 256, "finegrained_shared_bf16": 64}.get(cfg.name, 64)
+            "gptoss_prefill_zipf_mxfp4": 256, "finegrained_shared_bf16": 2048}.get(cfg.name, 64)
 
 
 # ----------------------------------------------------------------- our arm
