@@ -55,8 +55,8 @@ constexpr int LY_RW = 12;        // router: Wg pieces per lane
 constexpr int LY_MAX_D = 32 * 8 * LY_RW;
 // Batches up to this many tokens run as one launch.  Measured on the gpt-oss
 // decode shape (d = d_ff = 2880, 128 experts, top-4; microseconds per layer,
-// one launch against the chained kernels): n = 1 42 / 46, 4 72 / 82, 8 107 /
-// 113, 16 168 / 169, 32 256 / 249, 64 348 / 332.  From about 32 tokens the
+// one launch against the chained kernels): n = 1 40 / 46, 4 72 / 82, 8 107 /
+// 113, 16 171 / 169, 32 256 / 249, 64 348 / 332.  From about 32 tokens the
 // one launch's serial head (router, selection, dispatch: 25 us at 64 tokens)
 // costs more than the launches it saves, and the chain is faster.  (Within
 // this range the chain's router is the small-batch kernel, so both paths
@@ -156,10 +156,6 @@ __device__ __forceinline__ uint32_t ld_cg_u32(const void *p) {
   return r;
 }
 
-__device__ __forceinline__ void red_release_add(int *p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ int ld_acquire(const int *p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -169,25 +165,22 @@ __device__ __forceinline__ int ld_acquire(const int *p) {
 // Barrier over the grid's CTAs on a zeroed per-launch counter.  A wait that
 // runs out records MOE_ERR_TIMEOUT and lets the CTA go on (its results are
 // then reported invalid).
-__device__ void grid_barrier(int *ctr, int *status, int *s_flag) {
+__device__ void grid_barrier(int *ctr, int *status) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     atomicAdd(ctr, 1);
     const int target = (int)gridDim.x;
-    int ok = 1;
     if (ld_acquire(ctr) < target) {
       const uint64_t t0 = tc::globaltimer();
       while (ld_acquire(ctr) < target) {
         if (tc::globaltimer() - t0 > tc::kWaitLimitNs) {
-          ok = 0;
           set_status(status, MOE_ERR_TIMEOUT, -1);
           break;
         }
       }
     }
     __threadfence();
-    *s_flag = ok;
   }
   __syncthreads();
 }
@@ -205,7 +198,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ uint64_t full[DV_WARPS][DV_STAGES];
   __shared__ uint64_t sbar[2];
-  __shared__ int s_abort, s_nactive, s_flag, s_nclaimed;
+  __shared__ int s_abort, s_nactive, s_nclaimed;
   __shared__ unsigned s_raw_done;
   __shared__ int s_claim[LY_NQ];
   // per active expert: id, segment start and length (< 2^15); per segment
@@ -288,7 +281,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   }
 
   // ---- 2. every logit and f16 row is stored
-  grid_barrier(&a.sync[SY_BAR1], a.status, &s_flag);
+  grid_barrier(&a.sync[SY_BAR1], a.status);
 
   // ---- 3. selection and the stable dispatch, in every CTA: the same code on
   // the same logits gives the same arrays in every CTA; CTA 0 writes them
@@ -873,7 +866,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   }
 
   // ---- 5. every y_perm row is stored; combine
-  grid_barrier(&a.sync[SY_BAR2], a.status, &s_flag);
+  grid_barrier(&a.sync[SY_BAR2], a.status);
   {
     const int vpr = d / 8;
     const uint4 *yp = reinterpret_cast<const uint4 *>(a.y_perm);
