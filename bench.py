@@ -45,6 +45,8 @@ MEASURED_TRAFFIC = {
     ("gptoss_decode_mxfp4", 1, "fused"): 53.92e6 + 0.216e6,
     ("gptoss_decode_mxfp4", 4, "fused"): 201.9e6 + 3.96e6,
     ("gptoss_decode_mxfp4", 16, "fused"): 710.4e6 + 5.03e6,
+    ("gptoss_decode_nvfp4", 1, "fused"): 57.04e6 + 0.230e6,
+    ("gptoss_decode_nvfp4", 8, "fused"): 407.5e6 + 3.79e6,
 }
 L2_BYTES = 129 * 1024 * 1024
 # a timed loop at least this long runs at the power-capped clock: the sustained

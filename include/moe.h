@@ -254,8 +254,9 @@ typedef enum {
   MOE_STAGE_SHARED = 4,    /* shared expert (only when d_ff_shared > 0) */
   MOE_STAGE_COMBINE = 5,   /* gate scaling + un-permute */
   MOE_STAGE_END = 6,       /* after the last launch */
-  MOE_STAGE_FUSED = 7      /* the whole layer in one launch (small-batch MXFP4 SwiGLU layers
-                              with n <= 16 and d <= 3072): in place of stages 0..5 */
+  MOE_STAGE_FUSED = 7      /* the whole layer in one launch (small-batch SwiGLU layers with
+                              d <= 3072: MXFP4 with n <= 16, NVFP4 without a pool with
+                              n <= 8): in place of stages 0..5 */
 } moe_stage;
 
 /* Host callback run by moe_forward_staged on the calling thread just before

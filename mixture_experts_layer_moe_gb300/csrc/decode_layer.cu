@@ -1,4 +1,5 @@
-// The small-batch MoE layer over MXFP4 experts in one cooperative launch:
+// The small-batch MoE layer over MXFP4 or NVFP4 experts in one cooperative
+// launch:
 // router logits, top-k selection and gates, the stable dispatch, the selected
 // experts' up (SwiGLU) and down projections, and the combine.
 //
@@ -62,6 +63,10 @@ constexpr int LY_MAX_D = 32 * 8 * LY_RW;
 // this range the chain's router is the small-batch kernel, so both paths
 // compute the same logits.)
 constexpr int LY_MAX_TOKENS = 16;
+// NVFP4 experts, on the same shape (an E4M3 scale per 16 elements, so units
+// of at most 32 rows: twice the MXFP4 units at 16 tokens): n = 1 42 / 47,
+// 4 80 / 89, 8 125 / 125, 16 207 / 191.
+constexpr int LY_MAX_TOKENS_NV = 8;
 
 // Per-launch counters, zeroed before the launch: the two grid barriers, the
 // unit queue, and per expert the up-unit groups whose h rows are stored.
@@ -70,7 +75,8 @@ enum { SY_BAR1 = 0, SY_BAR2 = 1, SY_QUEUE = 2, SY_UPDONE = 4 };
 struct LayerArgs {
   const __nv_bfloat16 *x, *Wg;   // [n][d], [E][d]
   const float *bias;             // [E] or nullptr
-  const uint8_t *S1, *S3, *S2;   // E8M0 scales of W1, W3 [E][d_ff][d/32], W2 [E][d][d_ff/32]
+  const uint8_t *S1, *S3, *S2;   // block scales of W1, W3 [E][d_ff][d/32 or d/16], W2 likewise
+  const float *G1, *G3, *G2;     // NVFP4: one fp32 scale per expert matrix [E]
   int n, d, d_ff, E, k, gate_mode;
   float *logits;                 // [n][E]
   int32_t *topk_idx;             // [n][k]
@@ -104,7 +110,7 @@ struct LayerPlan {
 
 __host__ __device__ inline int imax(int a, int b) { return a > b ? a : b; }
 
-__host__ __device__ inline LayerPlan layer_plan(int d, int d_ff, int rg) {
+__host__ __device__ inline LayerPlan layer_plan(int d, int d_ff, int rg, int fmt) {
   LayerPlan p;
   const int ks = DV_WARPS / rg;
   p.KBu = d / 32;
@@ -114,7 +120,8 @@ __host__ __device__ inline LayerPlan layer_plan(int d, int d_ff, int rg) {
   p.bpsd = (((p.KBd + ks - 1) / ks) + 1) & ~1;
   p.PP = (imax(p.bpsu, p.bpsd) + 7) & ~7;
   if (p.PP % 32 == 0) p.PP += 8;   // rows g and g + 1 of a quarter-warp on other banks
-  p.sc_pitch = (16 * rg * imax(p.KBu, p.KBd) + 15) & ~15;
+  // (NVFP4: two E4M3 scale bytes per 16-byte chunk of 32 elements)
+  p.sc_pitch = (16 * rg * imax(p.KBu, p.KBd) * (fmt == 1 ? 2 : 1) + 15) & ~15;
   p.nraw = rg == 1 ? 2 : 1;
   p.raw_off = (size_t)DV_WARPS * DV_STAGES * 2 * DV_BOX;
   p.pairs_off = p.raw_off + (size_t)p.nraw * 2 * p.sc_pitch;
@@ -185,7 +192,9 @@ __device__ void grid_barrier(int *ctr, int *status) {
   __syncthreads();
 }
 
-template <int RG, bool POOL>
+// FMT: 0 MXFP4 (E8M0 scale per 32 elements), 1 NVFP4 (E4M3 scale per 16, fp32
+// scale per matrix), as in the two-kernel FFN.
+template <int RG, bool POOL, int FMT>
 __global__ void __launch_bounds__(LY_THREADS, 2)
 decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_constant__ CUtensorMap tm3,
                     const __grid_constant__ CUtensorMap tm2, const __grid_constant__ CUtensorMap tp1,
@@ -211,7 +220,8 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   const int n = a.n, d = a.d, d_ff = a.d_ff, E = a.E, k = a.k, P = n * k;
   uint8_t *smem = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   volatile int *abort = &s_abort;
-  const LayerPlan plan = layer_plan(d, d_ff, RG);
+  const LayerPlan plan = layer_plan(d, d_ff, RG, FMT);
+  constexpr int SPC = FMT == 1 ? 2 : 1;   // scale bytes per 16-byte code chunk
   // until the units start, the reduction buffer holds the selection's
   // indices and the per-expert counts and offsets
   int32_t *s_idx = reinterpret_cast<int32_t *>(smem + plan.red_off);   // [kDecodeMaxPairs]
@@ -429,18 +439,18 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     uint8_t *dst = smem + plan.raw_off + (size_t)b * 2 * scp;
     if (w.kind == 0) {
       const int r0 = w.rb * UROWS, rows = min(UROWS, d_ff - r0);   // rows % 16 == 0
-      const uint32_t bytes = (uint32_t)rows * plan.KBu;
+      const uint32_t bytes = (uint32_t)rows * plan.KBu * SPC;
       const size_t row = (size_t)(ps >= 0 ? ps : e) * d_ff + r0;
       const uint8_t *S1 = ps >= 0 ? a.PS1 : a.S1, *S3 = ps >= 0 ? a.PS3 : a.S3;
       tc::mbar_arrive_expect_tx(&sbar[b], 2 * bytes);
-      bulk_load(dst, S1 + row * plan.KBu, bytes, &sbar[b]);
-      bulk_load(dst + scp, S3 + row * plan.KBu, bytes, &sbar[b]);
+      bulk_load(dst, S1 + row * plan.KBu * SPC, bytes, &sbar[b]);
+      bulk_load(dst + scp, S3 + row * plan.KBu * SPC, bytes, &sbar[b]);
     } else {
       const int r0 = w.rb * DROWS, rows = min(DROWS, d - r0);
-      const uint32_t bytes = (uint32_t)rows * plan.KBd;
+      const uint32_t bytes = (uint32_t)rows * plan.KBd * SPC;
       const size_t row = (size_t)(ps >= 0 ? ps : e) * d + r0;
       tc::mbar_arrive_expect_tx(&sbar[b], bytes);
-      bulk_load(dst, (ps >= 0 ? a.PS2 : a.S2) + row * plan.KBd, bytes, &sbar[b]);
+      bulk_load(dst, (ps >= 0 ? a.PS2 : a.S2) + row * plan.KBd * SPC, bytes, &sbar[b]);
     }
     if (b) raw_mine1 = j;
     else raw_mine0 = j;
@@ -622,19 +632,39 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     };
     if (kind == 0) prefetch_first();
 
-    // decode this warp's part of the scales into bf16 pairs (row g | row
-    // g + 8); the last warp done claims the unit that reuses the buffer and
-    // issues its copy
+    // decode this warp's part of the scales (MXFP4: bf16 pairs row g | row
+    // g + 8; NVFP4: byte pairs per block parity, as the two-kernel FFN); the
+    // last warp done claims the unit that reuses the buffer and issues its copy
     {
       // matrix m of the warp's group: W1 / W3 (up), or rows 0..15 / 16..31 of
       // the group (down), at the warp's first block
       const uint8_t *buf = smem + plan.raw_off + (size_t)(i % NRAW) * 2 * scp;
       const int gg = lane >> 2, q = lane & 3;
+      auto raw_row = [&](int m) -> const uint8_t * {
+        return kind ? buf + ((size_t)(grp * 32 + 16 * m + gg) * KB + bb) * SPC
+                    : buf + (size_t)m * scp + ((size_t)(grp * 16 + gg) * KB + bb) * SPC;
+      };
+      if constexpr (FMT == 1) {
+        // lane (gg, q) takes chunks q, q + 4, ... of row pair gg; a chunk's two
+        // scale bytes of row gg and of row gg + 8 become two byte pairs, one
+        // per block parity, stored [matrix][row pair][parity][chunk]
+        uint16_t *pw16 = reinterpret_cast<uint16_t *>(pw);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const uint8_t *src = raw_row(m);
+          uint16_t *dst16 = pw16 + (size_t)(m * 8 + gg) * 2 * PP;
+          for (int b = q; b < nbl; b += 4) {
+            const uint32_t x = *reinterpret_cast<const uint16_t *>(src + 2 * b);
+            const uint32_t y = *reinterpret_cast<const uint16_t *>(src + 2 * b + 16 * KB);
+            dst16[b] = (uint16_t)__byte_perm(x, y, 0x0040);
+            dst16[PP + b] = (uint16_t)__byte_perm(x, y, 0x0051);
+          }
+        }
+      } else {
       const bool even = (KB & 1) == 0;
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
-        const uint8_t *src = kind ? buf + (size_t)(grp * 32 + 16 * m + gg) * KB + bb
-                                  : buf + (size_t)m * scp + (size_t)(grp * 16 + gg) * KB + bb;
+        const uint8_t *src = raw_row(m);
         uint32_t *dstp = pw + (m * 8 + gg) * PP;
         for (int b = 2 * q; b < nbl; b += 8) {
           const bool two = b + 1 < nbl;
@@ -652,6 +682,7 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
           if (two) *reinterpret_cast<uint2 *>(dstp + b) = make_uint2(p0, p1);
           else dstp[b] = p0;
         }
+      }
       }
     }
     __syncwarp();
@@ -697,6 +728,15 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     }
     const uint32_t *pr1 = pw + g * PP;
     const uint32_t *pr3 = pr1 + 8 * PP;
+    // NVFP4: this lane's block parity (t / 2) row of byte pairs, and the
+    // unit's matrix scales (W1 and W3, or W2 for both halves)
+    const uint16_t *pn1 = reinterpret_cast<const uint16_t *>(pw) + (size_t)(g * 2 + (t >> 1)) * PP;
+    const uint16_t *pn3 = pn1 + (size_t)8 * 2 * PP;
+    float gs1 = 1.f, gs3 = 1.f;
+    if constexpr (FMT == 1) {
+      gs1 = kind ? a.G2[e] : a.G1[e];
+      gs3 = kind ? gs1 : a.G3[e];
+    }
 
     for (int tg = 0; tg < cnt; tg += DV_TOK, ++npass) {
       // token g of this pass, or the pass's last token where g is past it (its
@@ -723,6 +763,35 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
       // the 8-block group at local block cb: matrix 1 in box sw, matrix 3
       // (W3, or the group's rows 16..31) in the box after it
       auto compute8 = [&](const uint8_t *sw, int cb, int nb) {
+        if constexpr (FMT == 1) {
+          const uint4 n1 = *reinterpret_cast<const uint4 *>(pn1 + cb);
+          const uint4 n3 = *reinterpret_cast<const uint4 *>(pn3 + cb);
+          // the eight chunks' scale pairs {s_g, s_g+8} as f16x2
+          const uint2 f1a = e4m3x4_to_f16x2x2(n1.x), f1b = e4m3x4_to_f16x2x2(n1.y),
+                      f1c = e4m3x4_to_f16x2x2(n1.z), f1d = e4m3x4_to_f16x2x2(n1.w);
+          const uint2 f3a = e4m3x4_to_f16x2x2(n3.x), f3b = e4m3x4_to_f16x2x2(n3.y),
+                      f3c = e4m3x4_to_f16x2x2(n3.z), f3d = e4m3x4_to_f16x2x2(n3.w);
+          const uint32_t f1[8] = {f1a.x, f1a.y, f1b.x, f1b.y, f1c.x, f1c.y, f1d.x, f1d.y};
+          const uint32_t f3[8] = {f3a.x, f3a.y, f3b.x, f3b.y, f3c.x, f3c.y, f3d.x, f3d.y};
+          auto block = [&](int bl) {
+            const uint8_t *wp = sw + (lane_off ^ (uint32_t)(bl << 4));
+            const uint32_t wg = *reinterpret_cast<const uint32_t *>(wp);
+            const uint32_t wh = *reinterpret_cast<const uint32_t *>(wp + 8 * DV_BOXB);
+            nv_block(acc1, wg, wh, f1[bl], bx[bl]);
+            const uint32_t vg = *reinterpret_cast<const uint32_t *>(wp + DV_BOX);
+            const uint32_t vh = *reinterpret_cast<const uint32_t *>(wp + DV_BOX + 8 * DV_BOXB);
+            nv_block(acc3, vg, vh, f3[bl], bx[bl]);
+          };
+          if (nb == 8) {
+#pragma unroll
+            for (int bl = 0; bl < 8; ++bl) block(bl);
+          } else {
+#pragma unroll
+            for (int bl = 0; bl < 8; ++bl)
+              if (bl < nb) block(bl);
+          }
+          return;
+        }
         const uint4 s1a = *reinterpret_cast<const uint4 *>(pr1 + cb);
         const uint4 s1b = *reinterpret_cast<const uint4 *>(pr1 + cb + 4);
         const uint4 s3a = *reinterpret_cast<const uint4 *>(pr3 + cb);
@@ -832,11 +901,11 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
           if (tk >= cnt) continue;
           if (kind) {
             // rows r0 + frow (f1) and r0 + 16 + frow (f3) of y_perm
-            a.y_perm[(size_t)(beg + tk) * d + r0 + frow] = __float2bfloat16_rn(f1[q]);
-            a.y_perm[(size_t)(beg + tk) * d + r0 + 16 + frow] = __float2bfloat16_rn(f3[q]);
+            a.y_perm[(size_t)(beg + tk) * d + r0 + frow] = __float2bfloat16_rn(f1[q] * gs1);
+            a.y_perm[(size_t)(beg + tk) * d + r0 + 16 + frow] = __float2bfloat16_rn(f3[q] * gs3);
           } else {
             const int row = r0 + frow;
-            const float a1 = f1[q], a3 = f3[q];
+            const float a1 = f1[q] * gs1, a3 = f3[q] * gs3;   // NVFP4 matrix scales (else 1)
             const float v = a1 / (1.f + __expf(-a1)) * a3;
             if (row < R) {
               const __nv_bfloat16 hb = __float2bfloat16_rn(v);
@@ -911,21 +980,23 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
 // still gives every CTA two units on average, else 2 when every CTA gets one,
 // else 1.  (The active experts are bounded by min(n k, E) here.)
 int layer_rg(const moe_config &c, int ctas) {
+  // NVFP4 units stay at 32 rows a side: their scale rows are twice as long
+  const int max_rg = c.weight_dtype == MOE_NVFP4 ? 2 : 4;
   const long slots = (long)c.n * c.top_k < c.n_experts ? (long)c.n * c.top_k : c.n_experts;
   auto units = [&](int rg) {
     return slots * ((c.d_ff + 16 * rg - 1) / (16 * rg) + (c.d + 32 * rg - 1) / (32 * rg));
   };
-  if (units(4) >= 2L * ctas) return 4;
+  if (max_rg == 4 && units(4) >= 2L * ctas) return 4;
   if (units(2) >= ctas) return 2;
   return 1;
 }
 
-template <int RG, bool POOL>
+template <int RG, bool POOL, int FMT>
 cudaError_t launch_layer(const LayerArgs &a, const CUtensorMap (&maps)[6], cudaStream_t s) {
-  const size_t smem = 1024 + layer_plan(a.d, a.d_ff, RG).bytes;
+  const size_t smem = 1024 + layer_plan(a.d, a.d_ff, RG, FMT).bytes;
   static size_t smem_set = 0;
   static int per_sm = 0;
-  auto kern = decode_layer_kernel<RG, POOL>;
+  auto kern = decode_layer_kernel<RG, POOL, FMT>;
   if (smem > smem_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -953,10 +1024,11 @@ cudaError_t launch_layer(const LayerArgs &a, const CUtensorMap (&maps)[6], cudaS
 
 }  // namespace
 
-bool decode_layer_supported(const moe_config &c) {
-  if (!decode_route_supported(c) || c.weight_dtype != MOE_MXFP4 || c.act != MOE_ACT_SWIGLU)
+bool decode_layer_supported(const moe_config &c, bool pooled) {
+  const bool fmt_ok = c.weight_dtype == MOE_MXFP4 || (c.weight_dtype == MOE_NVFP4 && !pooled);
+  if (!decode_route_supported(c) || !fmt_ok || c.act != MOE_ACT_SWIGLU) return false;
+  if (c.n > (c.weight_dtype == MOE_NVFP4 ? LY_MAX_TOKENS_NV : LY_MAX_TOKENS) || c.d > LY_MAX_D)
     return false;
-  if (c.n > LY_MAX_TOKENS || c.d > LY_MAX_D) return false;
   if (!tensor_maps_available()) return false;
   int dev = 0, coop = 0;
   return cudaGetDevice(&dev) == cudaSuccess &&
@@ -975,6 +1047,9 @@ cudaError_t launch_decode_layer(const moe_config &c, const void *x, const moe_we
   a.S1 = w.S1;
   a.S3 = w.S3;
   a.S2 = w.S2;
+  a.G1 = w.G1;
+  a.G3 = w.G3;
+  a.G2 = w.G2;
   a.n = c.n;
   a.d = c.d;
   a.d_ff = c.d_ff;
@@ -1024,14 +1099,19 @@ cudaError_t launch_decode_layer(const moe_config &c, const void *x, const moe_we
     a.pool_counts = b.pool_counts;
   }
   const int rg = layer_rg(c, 2 * num_sms());
-  if (pool) {
-    if (rg == 4) return launch_layer<4, true>(a, maps, s);
-    if (rg == 2) return launch_layer<2, true>(a, maps, s);
-    return launch_layer<1, true>(a, maps, s);
+  if (c.weight_dtype == MOE_NVFP4) {
+    if (pool) return cudaErrorNotSupported;
+    if (rg == 2) return launch_layer<2, false, 1>(a, maps, s);
+    return launch_layer<1, false, 1>(a, maps, s);
   }
-  if (rg == 4) return launch_layer<4, false>(a, maps, s);
-  if (rg == 2) return launch_layer<2, false>(a, maps, s);
-  return launch_layer<1, false>(a, maps, s);
+  if (pool) {
+    if (rg == 4) return launch_layer<4, true, 0>(a, maps, s);
+    if (rg == 2) return launch_layer<2, true, 0>(a, maps, s);
+    return launch_layer<1, true, 0>(a, maps, s);
+  }
+  if (rg == 4) return launch_layer<4, false, 0>(a, maps, s);
+  if (rg == 2) return launch_layer<2, false, 0>(a, maps, s);
+  return launch_layer<1, false, 0>(a, maps, s);
 }
 
 }  // namespace moe

@@ -199,9 +199,11 @@ cudaError_t launch_decode_route(const moe_config &c, const float *logits, const 
                                 int32_t *miss_list = nullptr, int32_t *pool_counts = nullptr);
 // The whole small-batch layer in one cooperative launch (decode_layer.cu):
 // router, selection, dispatch, both expert projections and combine, for
-// MXFP4 SwiGLU experts with n <= 16 tokens and d <= 3072 (the chained
-// launches above cover the rest, and are faster from about 32 tokens on).  Workspace arrays it writes, as the chained
-// path does; sync is decode_layer_sync_bytes() of zeroed counters.
+// SwiGLU experts with d <= 3072: MXFP4 (also from a pool) with n <= 16
+// tokens, NVFP4 (no pool) with n <= 8.  The chained launches above cover the
+// rest, and are faster beyond those sizes.  It writes the workspace
+// arrays the chained path writes; sync is decode_layer_sync_bytes() of
+// zeroed counters.
 struct DecodeLayerBuffers {
   float *logits;
   int32_t *topk_idx;
@@ -212,7 +214,7 @@ struct DecodeLayerBuffers {
   int *status;
   int32_t *state, *miss_list, *pool_counts;   // with a pool (each nullable)
 };
-bool decode_layer_supported(const moe_config &c);
+bool decode_layer_supported(const moe_config &c, bool pooled);
 size_t decode_layer_sync_bytes();
 cudaError_t launch_decode_layer(const moe_config &c, const void *x, const moe_weights &w,
                                 const moe_expert_pool *pool, const DecodeLayerBuffers &b,

@@ -280,7 +280,7 @@ moe_status run_small_batch(const moe_config &c, const void *x, const moe_weights
   int32_t *perm = at<int32_t>(ws, L.perm);
   int32_t *inv_perm = at<int32_t>(ws, L.inv_perm);
   float *gates = at<float>(ws, L.topk_gate);
-  if (decode_layer_supported(c)) {
+  if (decode_layer_supported(c, pool != nullptr)) {
     DecodeLayerBuffers b{};
     b.logits = at<float>(ws, L.logits);
     b.topk_idx = at<int32_t>(ws, L.topk_idx);

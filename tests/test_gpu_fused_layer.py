@@ -1,14 +1,16 @@
 """GPU: the small-batch MoE layer as one cooperative launch.
 
-moe_forward runs MXFP4 SwiGLU layers with at most 16 tokens and d <= 3072 as a
-single launch (router, selection, dispatch, both expert projections and the
+moe_forward runs SwiGLU layers with d <= 3072 as a single launch when they have
+MXFP4 experts and at most 16 tokens, or NVFP4 experts and at most 8 tokens (router, selection, dispatch, both expert projections and the
 combine; csrc/decode_layer.cu).  These tests pin which layers take that launch
 (through the stage hook) and check it against the fp64 oracle at the edges of
 its range and in shapes that exercise its scheduling:
 - reduction splits that own no MX block;
 - one expert holding every token, every token choosing every expert;
 - k = 1 with the Zipf router bias, and top-prob gates;
-- 256 experts with 256 pairs, most experts holding one.
+- 256 experts with 256 pairs, most experts holding one;
+- NVFP4 weights (E4M3 scales per 16 elements, a scale per matrix) at the same
+  edges.
 The work units are claimed at run time, so the result must also be the same
 bits from run to run, and a workspace reused across calls must give the same
 result as a fresh one.  Routing follows the pages: "How Mixture of Experts
@@ -26,6 +28,7 @@ pytestmark = pytest.mark.gpu
 
 C = moe_synth.CONFIGS
 D = C["gptoss_decode_mxfp4"]
+NV = C["gptoss_decode_nvfp4"]
 
 CHAIN = ["route", "dispatch", "ffn_up", "ffn_down", "combine", "end"]
 PATH_CASES = {
@@ -37,7 +40,10 @@ PATH_CASES = {
     "d_3072": (D.scaled(n=4, d=3072, d_ff=256, E=16), True),
     "d_3104": (D.scaled(n=4, d=3104, d_ff=256, E=16), False),
     "relu": (D.scaled(n=4, d=256, d_ff=256, E=16, act="relu"), False),
-    "nvfp4": (C["gptoss_decode_nvfp4"].scaled(n=4), False),
+    "nvfp4_n4": (NV.scaled(n=4), True),
+    "nvfp4_n8": (NV.scaled(n=8), True),
+    "nvfp4_n9": (NV.scaled(n=9), False),
+    "nvfp4_relu": (NV.scaled(n=4, d=256, d_ff=256, E=16, act="relu"), False),
 }
 
 PARITY_CASES = {
@@ -50,6 +56,11 @@ PARITY_CASES = {
     "top_prob_gates": D.scaled(n=16, d=256, d_ff=256, E=16, k=2, gate="top_prob"),
     # 256 experts, 256 pairs (most experts with one token)
     "e256_k16": D.scaled(n=16, d=128, d_ff=128, E=256, k=16),
+    # NVFP4: 8 tokens at d = 3072; odd chunk counts (3 and 5 a row) that
+    # leave most reduction splits empty; 128 pairs over 256 experts
+    "nvfp4_edge_n8_d3072": NV.scaled(n=8, k=2, d=3072, d_ff=512, E=32),
+    "nvfp4_odd_chunks": NV.scaled(n=8, d=96, d_ff=160, E=4, k=4),
+    "nvfp4_e256_k16": NV.scaled(n=8, d=128, d_ff=128, E=256, k=16),
 }
 
 
