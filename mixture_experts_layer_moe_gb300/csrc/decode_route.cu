@@ -74,8 +74,8 @@ decode_route_kernel(const float *__restrict__ logits, int n, int E, int k, int g
 
   if (router)
     for (int t = blockIdx.x + DR_CLUSTER * warp; t < n; t += DR_CLUSTER * DR_WARPS)
-      select_topk_warp(logits + (size_t)t * E, E, k, gate_mode, lane, topk_idx + (size_t)t * k,
-                       topk_gate + (size_t)t * k, nullptr);
+      select_topk_warp_shfl(logits + (size_t)t * E, E, k, gate_mode, lane,
+                            topk_idx + (size_t)t * k, topk_gate + (size_t)t * k, nullptr);
   if (!failed) {
     const int nvec = n * (d / 8);
     const int stride = gridDim.x * DR_THREADS;
