@@ -251,13 +251,37 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
   // ---- 1. router logits and the f16 x rows.  Pair (token t, expert e) =
   // t * E + e goes to warp (pair mod the grid's warps), spread over the CTAs
   // first; a warp keeps its expert's router row in registers while the
-  // expert stays the same.
+  // expert stays the same.  With at most one pair per CTA, the CTA's threads
+  // stage the pair's router row and x row in shared memory instead (one round
+  // of loads rather than a warp's three), and warp 0 adds them up in the
+  // same per-lane piece order: the same logits.
   {
     const int vpr = d / 8, nv = (vpr - lane + 31) / 32;   // lane's pieces: lane + 32 v
     const int nw = (int)gridDim.x * DV_WARPS;
+    const bool staged = n * E <= (int)gridDim.x;
+    if (staged && (int)blockIdx.x < n * E) {
+      const int t = (int)blockIdx.x / E, e = (int)blockIdx.x - t * E;
+      uint4 *sw = reinterpret_cast<uint4 *>(smem);   // [vpr] in the ring, unused until step 3
+      uint4 *sx = sw + vpr;                          // [vpr]
+      const uint4 *wrow = reinterpret_cast<const uint4 *>(a.Wg + (size_t)e * d);
+      const uint4 *xrow = reinterpret_cast<const uint4 *>(a.x + (size_t)t * d);
+      for (int i = tid; i < vpr; i += LY_THREADS) {
+        sw[i] = __ldg(wrow + i);
+        sx[i] = __ldg(xrow + i);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        float acc = 0.f;
+#pragma unroll
+        for (int v = 0; v < LY_RW; ++v)
+          if (v < nv) acc += bf16x8_dot(sw[lane + 32 * v], sx[lane + 32 * v]);
+        acc = warp_sum_xor(acc);
+        if (lane == 0) a.logits[(size_t)t * E + e] = acc + (a.bias ? a.bias[e] : 0.f);
+      }
+    }
     uint4 wv[LY_RW];
     int cur = -1;
-    for (int pr = warp * (int)gridDim.x + (int)blockIdx.x; pr < n * E; pr += nw) {
+    for (int pr = staged ? n * E : warp * (int)gridDim.x + (int)blockIdx.x; pr < n * E; pr += nw) {
       const int t = pr / E, e = pr - t * E;
       if (e != cur) {
         const uint4 *wrow = reinterpret_cast<const uint4 *>(a.Wg + (size_t)e * d);
@@ -543,13 +567,13 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     s_nclaimed = NRAW;
   }
   __syncthreads();
-  // the first units' weights start streaming while warp 0 finishes the
-  // dispatch: stable positions, a pair's rank among equal experts being the
-  // number of earlier pairs with that expert
+  // the first units' weights start streaming while the last warp finishes
+  // the dispatch: stable positions, a pair's rank among equal experts being
+  // the number of earlier pairs with that expert
   if (tid == 0)
     for (int j = 0; j < NRAW; ++j) fetch_raw(j);
   if (lane == 0) fill(0);
-  if (warp == 0) {
+  if (warp == DV_WARPS - 1) {   // (not warp 0, whose thread 0 issued the scale copies)
     for (int p0 = 0; p0 < P; p0 += 32) {
       const int p = p0 + lane;
       int e = p < P ? s_idx[p] : -1;
