@@ -42,11 +42,11 @@ MEASURED_TRAFFIC = {
     ("gptoss_prefill_zipf_mxfp4", 8192, "ffn_up"): 1.080e9 + 0.368e9,
     ("gptoss_decode_mxfp4", 64, "ffn_up"): 1.03e9 + 0.00734e9,
     # the fused small-batch launch (one launch of the rotation's first batch)
-    ("gptoss_decode_mxfp4", 1, "fused"): 53.92e6 + 0.216e6,
-    ("gptoss_decode_mxfp4", 4, "fused"): 201.9e6 + 3.96e6,
-    ("gptoss_decode_mxfp4", 16, "fused"): 710.4e6 + 5.03e6,
-    ("gptoss_decode_nvfp4", 1, "fused"): 57.04e6 + 0.230e6,
-    ("gptoss_decode_nvfp4", 8, "fused"): 407.5e6 + 3.79e6,
+    ("gptoss_decode_mxfp4", 1, "fused"): 53.94e6 + 0.247e6,
+    ("gptoss_decode_mxfp4", 4, "fused"): 201.95e6 + 4.56e6,
+    ("gptoss_decode_mxfp4", 16, "fused"): 710.3e6 + 6.21e6,
+    ("gptoss_decode_nvfp4", 1, "fused"): 57.05e6 + 0.138e6,
+    ("gptoss_decode_nvfp4", 8, "fused"): 407.5e6 + 4.95e6,
 }
 L2_BYTES = 129 * 1024 * 1024
 # a timed loop at least this long runs at the power-capped clock: the sustained
