@@ -129,3 +129,30 @@ def test_fused_workspace_reuse(lib):
         assert lib.moe_status_check(ws)[0] == 0
         y_ref, _, _, _ = parity.run_forward(lib, cfg, inputs)
         assert torch.equal(y, y_ref)
+
+
+@pytest.mark.parametrize("name,cfg", [
+    ("n1_staged_router", D.scaled(n=1)),
+    ("n2_staged_router", D.scaled(n=2, router_bias="zipf")),
+    ("n3_warp_router", D.scaled(n=3)),
+    ("n16", D.scaled(n=16, router_bias="zipf")),
+    ("nvfp4_n4", NV.scaled(n=4)),
+])
+def test_fused_logits_equal_route(lib, name, cfg):
+    """The one launch's router gives the route-only entry point's logits bit for
+    bit (the same per-lane piece order and butterfly sum, whether a CTA stages
+    a lone pair's rows in shared memory or a warp loads them itself), and so
+    the same selection and gates."""
+    inputs = moe_synth.make_inputs(cfg, seed=9, device="cuda")
+    w = lib.make_weights(inputs)
+    assert [s for s, _ in _stages(lib, cfg, seed=9)] == ["fused", "end"]
+    _, ws_f, L, inter = parity.run_forward(lib, cfg, inputs)
+    ws_r = lib.alloc_workspace(cfg)
+    idx = torch.empty(cfg.n, cfg.k, dtype=torch.int32, device="cuda")
+    gate = torch.empty(cfg.n, cfg.k, dtype=torch.float32, device="cuda")
+    lib.moe_route(cfg, inputs["x"], w, idx, gate, None, ws_r)
+    assert lib.moe_status_check(ws_r)[0] == 0
+    logits_r = parity.ws_view(ws_r, L, "logits", torch.float32, cfg.n * cfg.E).view(cfg.n, cfg.E)
+    assert torch.equal(inter["logits"].view(torch.int32), logits_r.cpu().view(torch.int32))
+    assert torch.equal(inter["topk_idx"], idx.cpu())
+    assert torch.equal(inter["topk_gate"].view(torch.int32), gate.cpu().view(torch.int32))
