@@ -525,6 +525,56 @@ def test_f16_range_is_reported(lib, name):
     assert lib.moe_status_check(ws)[0] == 0
 
 
+# ------------------------------------------------- NaN block scales
+# An E8M0 byte of 255 and an E4M3 byte 0x7f / 0xff encode NaN (OCP MX v1.0 and
+# the E4M3 table; the oracle decodes them to NaN, so the rows that meet one
+# are NaN).  The MXFP4 prefill path cannot stage such a scale in its f16
+# operands and reports MOE_ERR_RANGE.  The small-batch paths apply the scale
+# as given (E8M0 255 as +inf, E4M3 NaN as NaN): met in W1, it makes h
+# non-finite, whose f16 staging for the down projection reports
+# MOE_ERR_F16_RANGE; met in W2, the output column it scales comes out
+# non-finite in every row, as the oracle's does, and the rest stays finite.
+# Row 0's first block scale of every expert's matrix is set, so whichever
+# experts the tokens choose meet it.
+
+NAN_SCALE_CASES = {
+    "mxfp4_one_launch": (C["gptoss_decode_mxfp4"].scaled(n=2, d=256, d_ff=320, E=16), 255),
+    "mxfp4_chained": (C["gptoss_decode_mxfp4"].scaled(n=32, d=256, d_ff=320, E=16), 255),
+    "mxfp4_prefill": (C["gptoss_prefill_zipf_mxfp4"].scaled(n=600, d=256, d_ff=320, E=16), 255),
+    "nvfp4_one_launch": (C["gptoss_decode_nvfp4"].scaled(n=2, d=256, d_ff=320, E=16), 0x7F),
+    "nvfp4_chained": (C["gptoss_decode_nvfp4"].scaled(n=32, d=256, d_ff=320, E=16), 0xFF),
+}
+
+
+@pytest.mark.parametrize("matrix", ["S1", "S2"])
+@pytest.mark.parametrize("name", list(NAN_SCALE_CASES))
+def test_nan_block_scale(lib, name, matrix):
+    cfg, nan_byte = NAN_SCALE_CASES[name]
+    decode = O.e4m3_value if cfg.weight_dtype == "nvfp4" else O.e8m0_value
+    assert torch.isnan(decode(torch.tensor([nan_byte], dtype=torch.uint8))).all()
+    inputs = moe_synth.make_inputs(cfg, seed=3, device="cuda")
+    kept = inputs[matrix][:, 0, 0].clone()
+    inputs[matrix][:, 0, 0] = nan_byte
+    w = lib.make_weights(inputs)
+    ws = lib.alloc_workspace(cfg)
+    y = torch.empty(cfg.n, cfg.d, dtype=torch.bfloat16, device="cuda")
+    lib.moe_forward(cfg, inputs["x"], w, y, ws)
+    st, _ = lib.moe_status_check(ws)
+    if name == "mxfp4_prefill":
+        assert st == 7, lib.status_string(st)           # MOE_ERR_RANGE
+    elif matrix == "S1":
+        assert st == 8, lib.status_string(st)           # MOE_ERR_F16_RANGE
+    else:
+        assert st == 0, lib.status_string(st)
+        yf = y.float()
+        assert not torch.isfinite(yf[:, 0]).any()
+        assert torch.isfinite(yf[:, 1:]).all()
+    inputs[matrix][:, 0, 0] = kept
+    lib.moe_forward(cfg, inputs["x"], w, y, ws)
+    assert lib.moe_status_check(ws)[0] == 0
+    assert torch.isfinite(y.float()).all()
+
+
 @pytest.mark.parametrize("name,x_log2", [("decode", 13), ("decode", -12), ("prefill", 6),
                                          ("prefill", -12)])
 def test_f16_range_edges_match_oracle(lib, name, x_log2):
