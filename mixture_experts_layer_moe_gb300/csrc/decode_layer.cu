@@ -96,9 +96,9 @@ struct LayerArgs {
   int32_t *state, *miss_list, *pool_counts;
 };
 
-// Shared memory of the fused kernel (bytes from the 1024-aligned base).  The
-// ring also holds a selecting warp's logits row before the first weight box
-// lands in it.
+// Shared memory of the fused kernel (bytes from the 1024-aligned base).  Before
+// the first weight box lands in it, the ring also holds a lone router pair's
+// rows (step 1) and the logits the CTA selects from (step 3).
 struct LayerPlan {
   int KBu, KBd;      // MX blocks per row: up (K = d), down (K = d_ff)
   int bpsu, bpsd;    // blocks per reduction split
@@ -450,8 +450,8 @@ decode_layer_kernel(const __grid_constant__ CUtensorMap tm1, const __grid_consta
     return true;
   };
 
-  // raw E8M0 bytes of claim j into buffer j % NRAW (a thread drains the
-  // copies it issued on abort)
+  // raw scale bytes of claim j (E8M0, or E4M3 pairs) into buffer j % NRAW (a
+  // thread drains the copies it issued on abort)
   int raw_mine0 = -1, raw_mine1 = -1;
   auto fetch_raw = [&](int j) {
     const int u = s_claim[j % LY_NQ];
