@@ -35,6 +35,11 @@
  *     at the start of the workspace; kernels then skip the offending access
  *     and later kernels of the same workspace return early.  Read it with
  *     moe_status_check.  No kernel traps.
+ *   - Threads and devices: the library keeps per-process launch settings
+ *     (each kernel's configured shared-memory size and occupancy, the SM
+ *     count) from its first calls.  Call it from one host thread at a time,
+ *     on one device per process (a data-parallel job runs one process per
+ *     GPU).
  *   - Layouts are row-major.  Weights are stored out x in, so the reduction
  *     dimension is contiguous: W1, W3 [E][d_ff][d]; W2 [E][d][d_ff]; Wg [E][d]
  *     (the router's d x E matrix, transposed).  The page's X.W1 uses W1^T of
