@@ -109,6 +109,8 @@ FULL = {
     "gptoss_decode_mxfp4_n16": (C["gptoss_decode_mxfp4"].scaled(n=16), None),
     "gptoss_decode_mxfp4_n64": (C["gptoss_decode_mxfp4"].scaled(n=64), None),
     "gptoss_decode_nvfp4_n1": (C["gptoss_decode_nvfp4"].scaled(n=1), None),
+    "gptoss_decode_nvfp4_n4": (C["gptoss_decode_nvfp4"].scaled(n=4), None),
+    "gptoss_decode_nvfp4_n8": (C["gptoss_decode_nvfp4"].scaled(n=8), None),
     "gptoss_decode_nvfp4_n64": (C["gptoss_decode_nvfp4"].scaled(n=64), None),
     "gptoss_prefill_zipf_mxfp4": (C["gptoss_prefill_zipf_mxfp4"], None),
     "finegrained_shared_bf16": (C["finegrained_shared_bf16"], 1024),
