@@ -319,6 +319,8 @@ def run_ours(args):
         pool_state = torch.empty(cfg.E, dtype=torch.int32, device=device)
         pool_miss = torch.empty(cfg.E, dtype=torch.int32, device=device)
 
+    ccfg = moe.make_config(cfg)   # the C struct once, as a caller would build it
+
     def run_layers(x_in, y_out, hook=None, active=None, batch=0):
         """Layer 0 .. L-1 in sequence; the stage hook instruments layer 0.
         Layer 0 reads x_in, layer l > 0 token batch batch + l of the rotation.
@@ -328,15 +330,15 @@ def run_ours(args):
             out = y_out if l == args.layers - 1 else mid[l % 2]
             if pools:
                 if l == 0 and hook is not None:
-                    moe.moe_forward_pooled_staged(cfg, cur, layer_w[l], pools[l], out, pool_state,
+                    moe.moe_forward_pooled_staged(ccfg, cur, layer_w[l], pools[l], out, pool_state,
                                                   pool_miss, pool_counts[l], ws, hook, stream)
                 else:
-                    moe.moe_forward_pooled(cfg, cur, layer_w[l], pools[l], out, pool_state,
+                    moe.moe_forward_pooled(ccfg, cur, layer_w[l], pools[l], out, pool_state,
                                            pool_miss, pool_counts[l], ws, stream)
             elif l == 0 and hook is not None:
-                moe.moe_forward_staged(cfg, cur, layer_w[l], out, ws, hook, stream)
+                moe.moe_forward_staged(ccfg, cur, layer_w[l], out, ws, hook, stream)
             else:
-                moe.moe_forward(cfg, cur, layer_w[l], out, ws, stream)
+                moe.moe_forward(ccfg, cur, layer_w[l], out, ws, stream)
             if active is not None:
                 torch.cuda.synchronize(device)
                 active.append(int((counts > 0).sum().item()))
