@@ -1054,9 +1054,15 @@ bool decode_layer_supported(const moe_config &c, bool pooled) {
   if (c.n > (c.weight_dtype == MOE_NVFP4 ? LY_MAX_TOKENS_NV : LY_MAX_TOKENS) || c.d > LY_MAX_D)
     return false;
   if (!tensor_maps_available()) return false;
-  int dev = 0, coop = 0;
-  return cudaGetDevice(&dev) == cudaSuccess &&
-         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop;
+  static int coop = -1;   // (per process, as the other launch settings)
+  if (coop < 0) {
+    int dev = 0, v = 0;
+    coop = cudaGetDevice(&dev) == cudaSuccess &&
+                   cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess
+               ? (v != 0)
+               : 0;
+  }
+  return coop != 0;
 }
 
 size_t decode_layer_sync_bytes() { return (size_t)(SY_UPDONE + 256) * sizeof(int); }
